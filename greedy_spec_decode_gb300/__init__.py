@@ -1,0 +1,180 @@
+"""Python binding of libsga.so: vocab-sharded greedy token selection on GB300.
+
+Argument marshalling only.  Each function has the name of the C entry point
+it calls (declared in include/sga.h), takes torch CUDA tensors where the C
+call takes device pointers, passes data_ptr() values and the current torch
+stream, and raises SgaError on a non-zero status.  Every step of the path
+runs in the library's CUDA kernels; there is no fallback: if libsga.so has
+not been built, every call raises.
+
+Stats tensors are int32 [rows, 2] (8 bytes per row: fp32 value bits, int32
+id); ``stat_values``/``stat_ids`` view the two columns.
+
+Method: vLLM PR #34049 (Solution: local argmax per vocab shard, gather of
+(max_value, global_index), cross-rank reduce), PR #39419 (draft-to-target
+map after the local argmax), PR #62604 (Purpose items 1-2: dim-0 gathered
+per-shard stats, one verify kernel; fused get_top_tokens with padding mask
+and torch.argmax order).
+"""
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libsga.so")
+
+SGA_F32, SGA_BF16 = 0, 1
+SGA_MAX_K = 15
+SGA_MAX_VOCAB = 1 << 24
+SGA_DEVERR_K_RANGE, SGA_DEVERR_D2T_RANGE, SGA_DEVERR_TIMEOUT = 1, 2, 4
+
+_lib = None
+
+
+class SgaError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} failed: {status} ({sga_status_string(status)})")
+
+
+def lib():
+    """The loaded libsga.so (ctypes), with argument types set."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -m greedy_spec_decode_gb300.build` (or __graft_entry__.build())")
+        L = ctypes.CDLL(LIB_PATH)
+        i64, i32, vp, sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+        sig = {
+            "sga_version": ([], i32),
+            "sga_status_string": ([i32], ctypes.c_char_p),
+            "sga_local_argmax": ([vp, i32, i64, i64, i64, i64, i64, vp, vp], i32),
+            "sga_shard_reduce": ([vp, i32, i64, vp, vp, vp, i64, vp], i32),
+            "sga_greedy_verify": ([vp, i32, i32, vp, vp, i32, vp, vp, vp, vp, vp, vp], i32),
+            "sga_lmhead_argmax_workspace": ([i64, i64], sz),
+            "sga_lmhead_argmax": ([vp, i64, i64, vp, i64, i64, i64, vp, vp, sz, vp], i32),
+            "sga_device_error": ([ctypes.POINTER(ctypes.c_uint32)], i32),
+            "sga_clear_device_error": ([], i32),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = L
+    return _lib
+
+
+def sga_version():
+    return lib().sga_version()
+
+
+def sga_status_string(status):
+    return lib().sga_status_string(int(status)).decode()
+
+
+def _check(fn, status):
+    if status != 0:
+        raise SgaError(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dtype_code(t):
+    if t.dtype == torch.float32:
+        return SGA_F32
+    if t.dtype == torch.bfloat16:
+        return SGA_BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def new_stats(rows, device="cuda"):
+    """An int32 [rows, 2] tensor that holds `rows` stats."""
+    return torch.empty((rows, 2), dtype=torch.int32, device=device)
+
+
+def stat_values(stats):
+    return stats[..., 0].view(torch.float32)
+
+
+def stat_ids(stats):
+    return stats[..., 1]
+
+
+def sga_local_argmax(logits, shard_start, shard_width, org_vocab, out_stats, stream=None):
+    """Per-shard argmax.  `logits` is a 2-D CUDA tensor whose column 0 is the
+    shard's first id (a column slice of the full matrix, or a per-rank
+    buffer), unit stride along the vocab; out_stats receives one stat per row
+    (pass a slice of the gathered buffer to emulate all_gather on dim 0)."""
+    if logits.dim() != 2 or (logits.size(1) > 1 and logits.stride(1) != 1):
+        raise ValueError("logits must be 2-D with unit stride along the vocab")
+    rows = logits.size(0)
+    ld = logits.stride(0) if rows > 1 else max(logits.stride(0), shard_width)
+    _check("sga_local_argmax", lib().sga_local_argmax(
+        _ptr(logits), _dtype_code(logits), rows, ld, int(shard_start), int(shard_width),
+        int(org_vocab), _ptr(out_stats), _stream(stream)))
+    return out_stats
+
+
+def sga_shard_reduce(stats, num_shards, rows, out_ids, out_vals=None, d2t=None, stream=None):
+    """Global argmax per row from the gathered stats [num_shards * rows];
+    with d2t (int64 CUDA tensor) the ids are mapped k -> k + d2t[k]."""
+    _check("sga_shard_reduce", lib().sga_shard_reduce(
+        _ptr(stats), int(num_shards), int(rows), _ptr(out_vals), _ptr(out_ids), _ptr(d2t),
+        0 if d2t is None else d2t.numel(), _stream(stream)))
+    return out_ids
+
+
+def sga_greedy_verify(stats, num_shards, cu_num_draft, draft_tokens, max_k, out_sampled,
+                      out_num_sampled, out_num_rejected, out_bonus, out_target_ids=None,
+                      stream=None):
+    """Fused cross-shard reduce + greedy verification (see include/sga.h)."""
+    num_reqs = cu_num_draft.numel() - 1
+    _check("sga_greedy_verify", lib().sga_greedy_verify(
+        _ptr(stats), int(num_shards), int(num_reqs), _ptr(cu_num_draft),
+        _ptr(draft_tokens) if draft_tokens is not None and draft_tokens.numel() else None,
+        int(max_k), _ptr(out_sampled), _ptr(out_num_sampled), _ptr(out_num_rejected),
+        _ptr(out_bonus), _ptr(out_target_ids), _stream(stream)))
+
+
+def sga_lmhead_argmax_workspace(M, shard_width):
+    return int(lib().sga_lmhead_argmax_workspace(int(M), int(shard_width)))
+
+
+def sga_lmhead_argmax(hidden, weight_shard, shard_start, org_vocab, out_stats, workspace,
+                      stream=None):
+    """Fused LM-head GEMM + per-shard argmax.  hidden: bf16 [M, H] contiguous;
+    weight_shard: bf16 [shard_width, H] contiguous; workspace: a CUDA tensor of
+    at least sga_lmhead_argmax_workspace(M, shard_width) bytes."""
+    if not (hidden.is_contiguous() and weight_shard.is_contiguous()):
+        raise ValueError("hidden and weight_shard must be contiguous")
+    M, H = hidden.shape
+    width = weight_shard.size(0)
+    if weight_shard.size(1) != H:
+        raise ValueError("hidden and weight_shard must share H")
+    nbytes = workspace.numel() * workspace.element_size()
+    _check("sga_lmhead_argmax", lib().sga_lmhead_argmax(
+        _ptr(hidden), M, H, _ptr(weight_shard), int(shard_start), width, int(org_vocab),
+        _ptr(out_stats), _ptr(workspace), nbytes, _stream(stream)))
+    return out_stats
+
+
+def sga_device_error():
+    """Synchronise the current device and return its error word."""
+    w = ctypes.c_uint32(0)
+    _check("sga_device_error", lib().sga_device_error(ctypes.byref(w)))
+    return w.value
+
+
+def sga_clear_device_error():
+    _check("sga_clear_device_error", lib().sga_clear_device_error())

@@ -1,0 +1,215 @@
+// sga_abi.cu -- the extern "C" entry points of libsga.so: host-side argument
+// validation (before any CUDA call, so a bad call enqueues nothing), the
+// per-device cache (SM count, compute capability, address of the device error
+// word) and dispatch to the kernel launchers.
+#include <mutex>
+
+#include "common.cuh"
+
+// OR-ed by kernels instead of trapping; read by sga_device_error().
+__device__ uint32_t g_sga_error_word;
+
+namespace {
+
+struct DeviceInfo {
+  bool ready;
+  int status;  // SGA_OK or the error the set-up hit
+  int num_sms;
+  uint32_t *err;
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+DeviceInfo g_devices[kMaxDevices];
+
+// Per-device facts for the current device, looked up once.
+int current_device(DeviceInfo *out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SGA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return SGA_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceInfo &d = g_devices[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms = 0;
+    d.status = SGA_OK;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      d.status = SGA_ERR_CUDA;
+    } else if (major != 10 || minor != 3) {
+      d.status = SGA_ERR_DEVICE;  // the library carries sm_103a code only
+    } else {
+      void *p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_sga_error_word) != cudaSuccess) d.status = SGA_ERR_CUDA;
+      d.err = static_cast<uint32_t *>(p);
+      d.num_sms = sms;
+    }
+    d.ready = true;
+  }
+  *out = d;
+  return d.status;
+}
+
+bool misaligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) != 0; }
+
+int check_shard(int64_t shard_start, int64_t shard_width, int64_t org_vocab) {
+  if (shard_start < 0 || shard_width <= 0) return SGA_ERR_SHARD;
+  if (shard_start + shard_width > SGA_MAX_VOCAB) return SGA_ERR_VOCAB;
+  if (org_vocab <= 0 || org_vocab > SGA_MAX_VOCAB) return SGA_ERR_VOCAB;
+  return SGA_OK;
+}
+
+// Number of ids of [shard_start, shard_start + width) below org_vocab.
+int64_t valid_ids(int64_t shard_start, int64_t width, int64_t org_vocab) {
+  int64_t v = org_vocab - shard_start;
+  if (v < 0) v = 0;
+  return v < width ? v : width;
+}
+
+int launch_status(cudaError_t e) {
+  if (e != cudaSuccess) return SGA_ERR_CUDA;
+  return SGA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int sga_version(void) { return SGA_VERSION; }
+
+const char *sga_status_string(int status) {
+  switch (status) {
+    case SGA_OK: return "ok";
+    case SGA_ERR_NULL: return "a required pointer is NULL";
+    case SGA_ERR_SIZE: return "a size or count is negative or out of range";
+    case SGA_ERR_SHARD: return "shard outside the vocabulary or wider than the row stride";
+    case SGA_ERR_VOCAB: return "org_vocab <= 0 or an id would reach 2^24";
+    case SGA_ERR_DTYPE: return "unknown dtype";
+    case SGA_ERR_ALIGN: return "pointer not aligned as required";
+    case SGA_ERR_WORKSPACE: return "workspace too small";
+    case SGA_ERR_MAXK: return "max_k outside [1, SGA_MAX_K]";
+    case SGA_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    case SGA_ERR_DEVICE: return "current device is not compute capability 10.3 (GB300)";
+    case SGA_ERR_UNSUPPORTED: return "shape not supported by this kernel";
+    default: return "unknown status";
+  }
+}
+
+int sga_local_argmax(const void *logits, int dtype, int64_t rows, int64_t ld,
+                     int64_t shard_start, int64_t shard_width, int64_t org_vocab,
+                     sga_stat *out_stats, sga_stream stream) {
+  if (dtype != SGA_F32 && dtype != SGA_BF16) return SGA_ERR_DTYPE;
+  if (rows < 0 || rows > (int64_t(1) << 28)) return SGA_ERR_SIZE;
+  int st = check_shard(shard_start, shard_width, org_vocab);
+  if (st != SGA_OK) return st;
+  if (ld < shard_width) return SGA_ERR_SHARD;
+  if (rows == 0) return SGA_OK;
+  if (logits == nullptr || out_stats == nullptr) return SGA_ERR_NULL;
+  if (misaligned(logits, dtype == SGA_BF16 ? 2 : 4) || misaligned(out_stats, 8))
+    return SGA_ERR_ALIGN;
+  DeviceInfo d;
+  if ((st = current_device(&d)) != SGA_OK) return st;
+  return launch_status(sga::launch_local_argmax(
+      logits, dtype, rows, ld, shard_start, shard_width,
+      valid_ids(shard_start, shard_width, org_vocab), out_stats, d.num_sms,
+      static_cast<cudaStream_t>(stream)));
+}
+
+int sga_shard_reduce(const sga_stat *stats, int num_shards, int64_t rows, float *out_vals,
+                     int32_t *out_ids, const int64_t *d2t, int64_t d2t_len,
+                     sga_stream stream) {
+  if (num_shards < 1 || num_shards > 4096) return SGA_ERR_SIZE;
+  if (rows < 0 || rows > (int64_t(1) << 40)) return SGA_ERR_SIZE;
+  if (d2t != nullptr && d2t_len < 0) return SGA_ERR_SIZE;
+  if (rows == 0) return SGA_OK;
+  if (stats == nullptr || out_ids == nullptr) return SGA_ERR_NULL;
+  if (misaligned(stats, 8) || misaligned(out_ids, 4) || misaligned(out_vals, 4) ||
+      misaligned(d2t, 8))
+    return SGA_ERR_ALIGN;
+  DeviceInfo d;
+  int st = current_device(&d);
+  if (st != SGA_OK) return st;
+  return launch_status(sga::launch_shard_reduce(stats, num_shards, rows, out_vals, out_ids, d2t,
+                                                d2t_len, d.err,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+int sga_greedy_verify(const sga_stat *stats, int num_shards, int num_reqs,
+                      const int32_t *cu_num_draft, const int32_t *draft_tokens, int max_k,
+                      int32_t *out_sampled, int32_t *out_num_sampled,
+                      int32_t *out_num_rejected, int32_t *out_bonus,
+                      int32_t *out_target_ids, sga_stream stream) {
+  if (num_shards < 1 || num_shards > 4096) return SGA_ERR_SIZE;
+  if (num_reqs < 0 || num_reqs > (1 << 26)) return SGA_ERR_SIZE;
+  if (max_k < 1 || max_k > SGA_MAX_K) return SGA_ERR_MAXK;
+  if (num_reqs == 0) return SGA_OK;
+  if (stats == nullptr || cu_num_draft == nullptr || out_sampled == nullptr ||
+      out_num_sampled == nullptr || out_num_rejected == nullptr || out_bonus == nullptr)
+    return SGA_ERR_NULL;
+  if (misaligned(stats, 8) || misaligned(cu_num_draft, 4) || misaligned(draft_tokens, 4) ||
+      misaligned(out_sampled, 4) || misaligned(out_num_sampled, 4) ||
+      misaligned(out_num_rejected, 4) || misaligned(out_bonus, 4) ||
+      misaligned(out_target_ids, 4))
+    return SGA_ERR_ALIGN;
+  DeviceInfo d;
+  int st = current_device(&d);
+  if (st != SGA_OK) return st;
+  return launch_status(sga::launch_greedy_verify(
+      stats, num_shards, num_reqs, cu_num_draft, draft_tokens, max_k, out_sampled,
+      out_num_sampled, out_num_rejected, out_bonus, out_target_ids, d.err,
+      static_cast<cudaStream_t>(stream)));
+}
+
+size_t sga_lmhead_argmax_workspace(int64_t M, int64_t shard_width) {
+  if (M <= 0 || shard_width <= 0) return 0;
+  return sga::lmhead_workspace_bytes(M, shard_width);
+}
+
+int sga_lmhead_argmax(const void *hidden, int64_t M, int64_t H, const void *weight_shard,
+                      int64_t shard_start, int64_t shard_width, int64_t org_vocab,
+                      sga_stat *out_stats, void *workspace, size_t workspace_bytes,
+                      sga_stream stream) {
+  if (M < 0 || M > (int64_t(1) << 20)) return SGA_ERR_SIZE;
+  if (H <= 0 || H % 64 != 0 || H > (int64_t(1) << 20)) return SGA_ERR_SIZE;
+  int st = check_shard(shard_start, shard_width, org_vocab);
+  if (st != SGA_OK) return st;
+  if (M == 0) return SGA_OK;
+  if (hidden == nullptr || weight_shard == nullptr || out_stats == nullptr ||
+      workspace == nullptr)
+    return SGA_ERR_NULL;
+  if (misaligned(hidden, 16) || misaligned(weight_shard, 16) || misaligned(out_stats, 8) ||
+      misaligned(workspace, 8))
+    return SGA_ERR_ALIGN;
+  if (workspace_bytes < sga::lmhead_workspace_bytes(M, shard_width)) return SGA_ERR_WORKSPACE;
+  DeviceInfo d;
+  if ((st = current_device(&d)) != SGA_OK) return st;
+  const cudaError_t e = sga::launch_lmhead_argmax(
+      hidden, M, H, weight_shard, shard_start, shard_width,
+      valid_ids(shard_start, shard_width, org_vocab), out_stats, workspace, d.num_sms, d.err,
+      static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return SGA_ERR_UNSUPPORTED;
+  return launch_status(e);
+}
+
+int sga_device_error(uint32_t *out_word) {
+  if (out_word == nullptr) return SGA_ERR_NULL;
+  DeviceInfo d;
+  int st = current_device(&d);
+  if (st != SGA_OK) return st;
+  if (cudaDeviceSynchronize() != cudaSuccess) return SGA_ERR_CUDA;
+  if (cudaMemcpy(out_word, d.err, sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SGA_ERR_CUDA;
+  return SGA_OK;
+}
+
+int sga_clear_device_error(void) {
+  DeviceInfo d;
+  int st = current_device(&d);
+  if (st != SGA_OK) return st;
+  if (cudaDeviceSynchronize() != cudaSuccess) return SGA_ERR_CUDA;
+  if (cudaMemset(d.err, 0, sizeof(uint32_t)) != cudaSuccess) return SGA_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return SGA_ERR_CUDA;
+  return SGA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,237 @@
+/*
+ * sga.h -- C ABI of libsga.so: vocab-sharded greedy token selection for
+ * speculative decoding, hand-written CUDA kernels for GB300 (sm_103a).
+ *
+ * The method (web pages, cited by title and section):
+ *   vLLM PR #34049 "[Spec Decode] Reduce TP communication for speculative
+ *     decoding draft token generation", Solution: each tensor-parallel rank
+ *     takes the argmax of its own vocab shard, only (max_value, global_index)
+ *     pairs are gathered, and a reduction across ranks gives the global
+ *     argmax.
+ *   vLLM PR #39419 "[SpecDecode] Reduce TP communication for large-vocab
+ *     draft models speculative decoding", review "Refactor local argmax code":
+ *     the draft-to-target id map target_id = k + d2t[k] is applied after the
+ *     local argmax.
+ *   vLLM PR #62604 (sharded greedy verification), Purpose item 1: per-shard
+ *     statistics, all-gathered on dim 0, then ONE kernel for the global
+ *     argmax, the acceptance, the bonus token and the sampled/rejected
+ *     counts; item 2: the padding mask, "lowest id on ties, NaN wins, as
+ *     torch.argmax"; vocabulary < 2^24.
+ *
+ * Tensor-parallel ranks are emulated on one GPU: shard s writes its stats to
+ * rows [s*R, (s+1)*R) of one buffer, which is byte-for-byte what
+ * all_gather(dim=0) of the per-rank [R] stats would produce.
+ *
+ * Conventions for every entry point:
+ *   - Every pointer is a DEVICE pointer unless stated otherwise; the caller
+ *     owns every buffer.  The library allocates no memory and keeps no state
+ *     besides per-device cached kernel attributes and a device error word.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and the call returns without synchronising.
+ *   - Arguments are validated on the host BEFORE anything is launched; a
+ *     negative SGA_ERR_* means nothing was enqueued.  SGA_ERR_CUDA means a
+ *     launch failed (cudaGetLastError); the CUDA error is left for the caller
+ *     to inspect through cudaGetLastError/cudaPeekAtLastError semantics.
+ *   - Inputs are never written.  Outputs are fully written on success.
+ *   - Comparison order ("argmax order"): NaN beats every number and the
+ *     lowest-id NaN wins; among numbers the larger wins (+0 and -0 are equal);
+ *     equal values resolve to the lower global id.  Ids at or past org_vocab
+ *     are padding and count as -inf.  A row (or shard) with no value above
+ *     -inf reports its first id with value -inf.  The reported value is the
+ *     winning element widened exactly to fp32 (its own bits, NaN payload
+ *     kept), or -inf for a padded winner.
+ */
+#ifndef SGA_H
+#define SGA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SGA_VERSION 100 /* 1.0.0 */
+
+/* One per-row statistic of one shard: 8 bytes, {fp32 value bits, int32 id}. */
+typedef struct sga_stat {
+  float v;
+  int32_t id;
+} sga_stat;
+
+/* Logits element types. */
+enum sga_dtype { SGA_F32 = 0, SGA_BF16 = 1 };
+
+/* A cudaStream_t passed as an opaque pointer. */
+typedef void *sga_stream;
+
+/* Status codes (0 = success). */
+enum sga_status {
+  SGA_OK = 0,
+  SGA_ERR_NULL = -1,        /* a required pointer is NULL */
+  SGA_ERR_SIZE = -2,        /* a size or count is negative / out of range */
+  SGA_ERR_SHARD = -3,       /* shard outside the vocab or wider than the row stride */
+  SGA_ERR_VOCAB = -4,       /* org_vocab <= 0, or an id would reach 2^24 */
+  SGA_ERR_DTYPE = -5,       /* unknown dtype */
+  SGA_ERR_ALIGN = -6,       /* pointer not aligned as the entry point requires */
+  SGA_ERR_WORKSPACE = -7,   /* workspace smaller than the *_workspace() size */
+  SGA_ERR_MAXK = -8,        /* max_k outside [1, SGA_MAX_K] */
+  SGA_ERR_CUDA = -9,        /* a CUDA runtime call or launch failed */
+  SGA_ERR_DEVICE = -10,     /* the device has no sm_103 kernels (not a GB300) */
+  SGA_ERR_UNSUPPORTED = -11 /* shape outside what the kernel supports */
+};
+
+/* Largest number of drafts per request the verify kernel handles. */
+#define SGA_MAX_K 15
+
+/* Largest id + 1 any entry point accepts (the pages' vocabulary bound). */
+#define SGA_MAX_VOCAB (1 << 24)
+
+/* Library version, SGA_VERSION of the build. */
+int sga_version(void);
+
+/* Static English text for a status code; never NULL. */
+const char *sga_status_string(int status);
+
+/*
+ * sga_local_argmax -- per-shard argmax with the padding mask.
+ * Page: vLLM PR #34049, Solution step 1 (local argmax on each TP rank's vocab
+ * shard, index made global); vLLM PR #62604, Purpose item 2 (padding mask,
+ * torch.argmax order) and item 1 (per-shard statistics).
+ *
+ *   logits       device, rows x (>= shard_width) elements of `dtype`, row
+ *                stride `ld` ELEMENTS; points at the shard's first column,
+ *                i.e. element (0, shard_start) of the full matrix, or at
+ *                element 0 of a separate per-rank [rows, shard_width] buffer.
+ *                Must be aligned to the element size.  Any row stride and
+ *                any 16-byte misalignment of the rows is handled.
+ *   dtype        SGA_F32 or SGA_BF16.
+ *   rows         >= 0; 0 enqueues nothing and returns SGA_OK.
+ *   ld           >= shard_width.
+ *   shard_start  global id of column 0 of the shard (>= 0).
+ *   shard_width  > 0; shard_start + shard_width <= SGA_MAX_VOCAB.
+ *   org_vocab    1 .. SGA_MAX_VOCAB; global ids >= org_vocab are padding.
+ *   out_stats    device, `rows` entries, 8-byte aligned: out_stats[r] =
+ *                argmax (value, GLOBAL id) of row r over the shard.  To
+ *                emulate the dim-0 all-gather pass stats + s*rows.
+ * Reads each non-padding logit of the shard once; padding ids are not read.
+ */
+int sga_local_argmax(const void *logits, int dtype, int64_t rows, int64_t ld,
+                     int64_t shard_start, int64_t shard_width, int64_t org_vocab,
+                     sga_stat *out_stats, sga_stream stream);
+
+/*
+ * sga_shard_reduce -- global argmax from the gathered shard statistics,
+ * optionally mapped from draft ids to target ids.
+ * Page: vLLM PR #34049, Solution step 3 (reduce across ranks to the global
+ * argmax); vLLM PR #62604, Purpose item 2 (dim-0 all-gather layout, same
+ * result as torch.argmax); vLLM PR #39419, "Refactor local argmax code"
+ * (target_id = k + draft_id_to_target_id[k], after the local argmax).
+ *
+ *   stats       device, num_shards * rows entries, shard-major
+ *               (stats[s*rows + r]); shards in ascending id order.
+ *   num_shards  1 .. 4096.
+ *   rows        >= 0 (0: nothing enqueued).
+ *   out_vals    device fp32 [rows] (nullable): value of the winner.
+ *   out_ids     device int32 [rows]: global id of the winner, after d2t.
+ *   d2t         device int64 [d2t_len] or NULL.  When given, out_ids[r] =
+ *               k + d2t[k] for the winning id k; an id outside [0, d2t_len)
+ *               is left unmapped and sets the device error word (see
+ *               sga_device_error).
+ */
+int sga_shard_reduce(const sga_stat *stats, int num_shards, int64_t rows, float *out_vals,
+                     int32_t *out_ids, const int64_t *d2t, int64_t d2t_len,
+                     sga_stream stream);
+
+/*
+ * sga_greedy_verify -- one fused kernel: cross-shard reduce of every target
+ * row, greedy acceptance, bonus token and sampled/rejected counts.
+ * Page: vLLM PR #62604, Purpose item 1 (one kernel finishes the global
+ * argmax, acceptance, bonus token and sampled/rejected counts) and Test Plan
+ * (compared with rejection_sample + get_num_sampled_and_rejected on the full
+ * logits; placeholder drafts).
+ *
+ *   stats          device, num_shards * R_tot entries, shard-major, where
+ *                  R_tot = cu_num_draft[num_reqs] + num_reqs.
+ *   num_shards     1 .. 4096.
+ *   num_reqs       >= 0 (0: nothing enqueued).
+ *   cu_num_draft   device int32 [num_reqs + 1], cu[0] = 0, non-decreasing:
+ *                  request i has K_i = cu[i+1] - cu[i] drafts and owns target
+ *                  rows b_i .. b_i + K_i with b_i = cu[i] + i (K_i draft
+ *                  positions, then its bonus row).  K_i must lie in
+ *                  [0, max_k]; a request that breaks this gets num_sampled =
+ *                  num_rejected = 0, bonus = -1, sampled all -1, and the
+ *                  device error word is set.
+ *   draft_tokens   device int32 [cu[num_reqs]] (may be NULL when every K_i is
+ *                  0).  A negative id is a placeholder and never matches.
+ *   max_k          1 .. SGA_MAX_K: row length - 1 of out_sampled.
+ *   out_sampled    device int32 [num_reqs, max_k + 1]: with a_i = number of
+ *                  leading drafts equal to the target argmax of their row,
+ *                  entries 0..a_i are the target argmaxes of rows
+ *                  b_i .. b_i + a_i, the rest -1.
+ *   out_num_sampled, out_num_rejected   device int32 [num_reqs]: a_i + 1 and
+ *                  K_i - a_i.
+ *   out_bonus      device int32 [num_reqs]: the last emitted token, the target
+ *                  argmax of row b_i + a_i.
+ *   out_target_ids device int32 [R_tot] or NULL: every row's global argmax.
+ * All int32 pointers must be 4-byte aligned, stats 8-byte aligned.
+ */
+int sga_greedy_verify(const sga_stat *stats, int num_shards, int num_reqs,
+                      const int32_t *cu_num_draft, const int32_t *draft_tokens, int max_k,
+                      int32_t *out_sampled, int32_t *out_num_sampled,
+                      int32_t *out_num_rejected, int32_t *out_bonus,
+                      int32_t *out_target_ids, sga_stream stream);
+
+/*
+ * sga_lmhead_argmax -- fused LM-head GEMM + per-shard argmax: the shard's
+ * logits hidden . weight_shard^T are computed on the tensor cores (tcgen05,
+ * fp32 accumulation in tensor memory) and reduced to per-row statistics in
+ * the epilogue; the logits are never written to global memory.
+ * Page: vLLM PR #62604, Purpose (vocab-parallel LM head: each rank holds a
+ * vocab slice of the weight) and item 2 (fused get_top_tokens); vLLM PR
+ * #39419, Changes (get_top_tokens on the model: lm_head applied to the hidden
+ * states, then the local argmax).
+ *
+ *   hidden        device bf16 [M, H] row-major (row stride H), 16-byte aligned.
+ *   M             0 .. 1048576 (0: nothing enqueued).
+ *   H             hidden size: a positive multiple of 64.
+ *   weight_shard  device bf16 [shard_width, H] row-major, 16-byte aligned; row j
+ *                 holds global id shard_start + j.
+ *   shard_start, shard_width, org_vocab   as for sga_local_argmax.
+ *   out_stats     device [M], 8-byte aligned: argmax (value, global id) of
+ *                 each row's logits over the shard.  The value is the fp32
+ *                 accumulator of the winning logit; accumulation order is
+ *                 the kernel's, so values match an exact dot product only to
+ *                 fp32 rounding and near-ties may resolve to either id.
+ *   workspace     device, >= sga_lmhead_argmax_workspace(M, shard_width)
+ *                 bytes, 8-byte aligned; holds per-tile partial statistics.
+ *                 Contents on entry are ignored; the caller must not use it
+ *                 concurrently from two calls.
+ * Requires a GPU of compute capability 10.3 (SGA_ERR_DEVICE otherwise).
+ */
+size_t sga_lmhead_argmax_workspace(int64_t M, int64_t shard_width);
+int sga_lmhead_argmax(const void *hidden, int64_t M, int64_t H, const void *weight_shard,
+                      int64_t shard_start, int64_t shard_width, int64_t org_vocab,
+                      sga_stat *out_stats, void *workspace, size_t workspace_bytes,
+                      sga_stream stream);
+
+/*
+ * Device error word of the current device.  Kernels OR bits into it instead
+ * of trapping: SGA_DEVERR_K_RANGE (a request's K_i outside [0, max_k]),
+ * SGA_DEVERR_D2T_RANGE (a winning id outside the d2t table),
+ * SGA_DEVERR_TIMEOUT (a bounded wait inside a pipelined kernel gave up; its
+ * outputs are not valid).  sga_device_error synchronises the current device
+ * and copies the word to *out_word (host pointer); sga_clear_device_error
+ * synchronises and zeroes it.  Both return SGA_OK or SGA_ERR_CUDA.
+ */
+#define SGA_DEVERR_K_RANGE 1u
+#define SGA_DEVERR_D2T_RANGE 2u
+#define SGA_DEVERR_TIMEOUT 4u
+int sga_device_error(uint32_t *out_word);
+int sga_clear_device_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGA_H */

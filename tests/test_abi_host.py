@@ -1,0 +1,101 @@
+"""Host-side checks of the C ABI (no GPU needed, no compute call made).
+
+The library must load, export every function include/sga.h declares, and
+reject bad arguments with the documented status before touching CUDA.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sga.h")
+
+BAD_F32 = ctypes.c_void_p(0x1002)  # not 4-byte aligned; never dereferenced
+FAKE = ctypes.c_void_p(0x10000)    # aligned; never dereferenced
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sga_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_path(sga_lib):
+    names = declared_functions()
+    for n in ("sga_local_argmax", "sga_shard_reduce", "sga_greedy_verify", "sga_lmhead_argmax"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(sga_lib):
+    L = sga_lib.lib()
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_version_and_status_strings(sga_lib):
+    assert sga_lib.sga_version() == 100
+    texts = {sga_lib.sga_status_string(s) for s in range(0, -12, -1)}
+    assert len(texts) == 12 and all(texts)
+    assert sga_lib.sga_status_string(-99) == "unknown status"
+
+
+def test_local_argmax_validation(sga_lib):
+    f = sga_lib.lib().sga_local_argmax
+    ok = dict(logits=FAKE, dtype=1, rows=4, ld=10, start=0, width=10, org=10, out=FAKE)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["logits"], a["dtype"], a["rows"], a["ld"], a["start"], a["width"], a["org"],
+                 a["out"], None)
+
+    assert call(dtype=7) == -5
+    assert call(rows=-1) == -2
+    assert call(width=0) == -3
+    assert call(start=-1) == -3
+    assert call(ld=9) == -3
+    assert call(org=0) == -4
+    assert call(start=(1 << 24) - 5) == -4
+    assert call(rows=0) == 0            # empty batch: nothing enqueued
+    assert call(logits=None) == -1
+    assert call(out=None) == -1
+    assert call(dtype=0, logits=BAD_F32) == -6
+    assert call(out=ctypes.c_void_p(0x10004)) == -6
+
+
+def test_shard_reduce_and_verify_validation(sga_lib):
+    L = sga_lib.lib()
+    assert L.sga_shard_reduce(FAKE, 0, 4, FAKE, FAKE, None, 0, None) == -2
+    assert L.sga_shard_reduce(FAKE, 2, -1, FAKE, FAKE, None, 0, None) == -2
+    assert L.sga_shard_reduce(FAKE, 2, 0, FAKE, FAKE, None, 0, None) == 0
+    assert L.sga_shard_reduce(None, 2, 4, FAKE, FAKE, None, 0, None) == -1
+    assert L.sga_shard_reduce(FAKE, 2, 4, None, ctypes.c_void_p(0x10002), None, 0, None) == -6
+    v = L.sga_greedy_verify
+    assert v(FAKE, 2, 3, FAKE, FAKE, 0, FAKE, FAKE, FAKE, FAKE, None, None) == -8
+    assert v(FAKE, 2, 3, FAKE, FAKE, 16, FAKE, FAKE, FAKE, FAKE, None, None) == -8
+    assert v(FAKE, 0, 3, FAKE, FAKE, 3, FAKE, FAKE, FAKE, FAKE, None, None) == -2
+    assert v(FAKE, 2, -1, FAKE, FAKE, 3, FAKE, FAKE, FAKE, FAKE, None, None) == -2
+    assert v(FAKE, 2, 0, FAKE, FAKE, 3, FAKE, FAKE, FAKE, FAKE, None, None) == 0
+    assert v(FAKE, 2, 3, None, FAKE, 3, FAKE, FAKE, FAKE, FAKE, None, None) == -1
+    assert v(FAKE, 2, 3, FAKE, FAKE, 3, FAKE, FAKE, FAKE, ctypes.c_void_p(0x10001), None, None) == -6
+
+
+def test_lmhead_validation(sga_lib):
+    L = sga_lib.lib()
+    ws = L.sga_lmhead_argmax_workspace(512, 75968)
+    assert ws >= 512 * 8
+    f = L.sga_lmhead_argmax
+    assert f(FAKE, 512, 100, FAKE, 0, 64, 64, FAKE, FAKE, ws, None) == -2   # H % 64
+    assert f(FAKE, -1, 64, FAKE, 0, 64, 64, FAKE, FAKE, ws, None) == -2
+    assert f(FAKE, 0, 64, FAKE, 0, 64, 64, FAKE, FAKE, ws, None) == 0
+    assert f(ctypes.c_void_p(0x10008), 4, 64, FAKE, 0, 64, 64, FAKE, FAKE, ws, None) == -6
+    assert f(FAKE, 512, 64, FAKE, 0, 75968, 75968, FAKE, FAKE, ws - 8, None) == -7
+    assert f(FAKE, 4, 64, FAKE, 0, 64, 0, FAKE, FAKE, ws, None) == -4
+
+
+def test_missing_library_fails_loudly(monkeypatch, sga_lib):
+    monkeypatch.setattr(sga_lib, "_lib", None)
+    monkeypatch.setattr(sga_lib, "LIB_PATH", os.path.join(ROOT, "nonexistent", "libsga.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        sga_lib.lib()

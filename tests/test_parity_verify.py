@@ -1,0 +1,100 @@
+"""GPU parity of sga_greedy_verify (fused cross-shard reduce + greedy
+acceptance) against the CPU oracle: accepted tokens, bonus token,
+num_sampled / num_rejected and per-row target ids, all bit-exact.
+
+Coverage follows vLLM PR #62604, Test Plan: TP 2/3/4/8 emulated in one
+process, compared with the full-logits result; K = 1/3/5 (and 15);
+placeholder drafts; planted cross-shard ties; plus variable K per request,
+requests with no drafts, max_k larger than every K, and the error word for a
+request whose K exceeds max_k.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+import gpu_helpers as gh
+
+pytestmark = pytest.mark.gpu
+
+
+def check_verify(stats_dev, stats_np, num_shards, cu, drafts, max_k):
+    got = gh.gpu_verify(stats_dev, num_shards, cu, drafts, max_k)
+    exp = oracle.greedy_verify(stats_np, num_shards, cu, drafts, max_k)
+    for key in ("sampled", "num_sampled", "num_rejected", "bonus", "target_ids"):
+        assert (got[key] == exp[key]).all(), key
+    ns, nr = got["num_sampled"], got["num_rejected"]
+    assert (ns + nr == np.diff(cu) + 1).all()
+    return got
+
+
+def run_workload(c):
+    x = c["logits"]
+    x_dev = gh.to_device(x)
+    stats_dev = gh.gpu_gathered_stats(x_dev, c["shards"], c["org_vocab"])
+    stats_np = oracle.gathered_stats(x, c["shards"], c["org_vocab"])
+    gh.assert_stats_equal(gh.stats_to_numpy(stats_dev), stats_np)
+    _, t = oracle.full_argmax(x, c["org_vocab"])
+    drafts = wl.compose_drafts(t, c["cu_num_draft"], c["flags"], c["rand_ids"])
+    return check_verify(stats_dev, stats_np, len(c["shards"]), c["cu_num_draft"], drafts, c["k"])
+
+
+def test_greedy_verify_workload(sga_lib):
+    got = run_workload(wl.greedy_verify_small())
+    assert 0 < got["num_rejected"].sum() < 24 * 3
+
+
+def test_large_verify_workload(sga_lib):
+    got = run_workload(wl.large_verify())
+    assert got["num_sampled"].max() > 1
+
+
+def random_stats(rng, rows, num_shards, vocab):
+    """Gathered stats of random logits rows (the oracle computes them)."""
+    x = wl.discrete_logits(int(rng.integers(1 << 30)), rows, vocab, "bf16", p_nan=0.002)
+    shards = wl.random_shards(int(rng.integers(1 << 30)), vocab, num_shards)
+    return oracle.gathered_stats(x, shards, vocab), x, shards
+
+
+@pytest.mark.parametrize("num_shards", [1, 2, 3, 4, 8])
+def test_random_variable_k_and_placeholders(sga_lib, num_shards):
+    rng = np.random.default_rng(num_shards)
+    for trial in range(6):
+        n = int(rng.integers(1, 300))
+        max_k = int(rng.choice([1, 3, 5, 15]))
+        ks = rng.integers(0, max_k + 1, n)
+        cu = np.concatenate([[0], np.cumsum(ks)]).astype(np.int32)
+        total = int(cu[-1]) + n
+        stats_np, _, _ = random_stats(rng, total, num_shards, 257)
+        _, t = oracle.shard_reduce(stats_np, num_shards, total)
+        flags = rng.random(int(cu[-1])) < 0.85
+        rand = rng.integers(-1, 257, int(cu[-1])).astype(np.int32)   # -1 = placeholder
+        drafts = wl.compose_drafts(t, cu, flags, rand)
+        stats_dev = torch.from_numpy(stats_np.view(np.int32).reshape(-1, 2).copy()).cuda()
+        check_verify(stats_dev, stats_np, num_shards, cu, drafts, max_k)
+
+
+def test_target_ids_optional(sga_lib):
+    rng = np.random.default_rng(5)
+    cu = np.array([0, 3, 6], np.int32)
+    stats_np, _, _ = random_stats(rng, 8, 2, 100)
+    stats_dev = torch.from_numpy(stats_np.view(np.int32).reshape(-1, 2).copy()).cuda()
+    got = gh.gpu_verify(stats_dev, 2, cu, np.zeros(6, np.int32), 3, with_target_ids=False)
+    exp = oracle.greedy_verify(stats_np, 2, cu, np.zeros(6, np.int32), 3)
+    assert (got["sampled"] == exp["sampled"]).all()
+    assert (got["target_ids"] == -99).all()   # untouched
+
+
+def test_k_above_max_k_sets_error_word(sga_lib):
+    sga_lib.sga_clear_device_error()
+    rng = np.random.default_rng(6)
+    cu = np.array([0, 2, 6, 7], np.int32)   # request 1 has K = 4 > max_k = 3
+    stats_np, _, _ = random_stats(rng, 10, 1, 50)
+    stats_dev = torch.from_numpy(stats_np.view(np.int32).reshape(-1, 2).copy()).cuda()
+    got = gh.gpu_verify(stats_dev, 1, cu, np.zeros(7, np.int32), 3)
+    assert sga_lib.sga_device_error() & sga_lib.SGA_DEVERR_K_RANGE
+    assert got["num_sampled"][1] == 0 and got["bonus"][1] == -1 and (got["sampled"][1] == -1).all()
+    assert got["num_sampled"][0] >= 1 and got["num_sampled"][2] >= 1
+    sga_lib.sga_clear_device_error()
+    assert sga_lib.sga_device_error() == 0
