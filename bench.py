@@ -1,0 +1,466 @@
+"""Benchmark of the sharded greedy token-selection hot path on GB300.
+
+One step = one pass of the whole path over one batch: sga_local_argmax for
+every vocab shard (tensor-parallel ranks emulated as vocab slices of one
+logits matrix, stats written in shard order as all_gather(dim=0) would) and
+the fused sga_greedy_verify.  Default workload: 256 requests x (15 drafts + 1
+bonus) = 4096 rows x vocab 202048 bf16 N(0,3), 3 uneven shards, 1% planted
+cross-shard-edge ties, drafts copying the target w.p. 0.6 (synthetic; the
+inputs, 1.66 GB, are larger than the 129 MB L2, so no flush is needed).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload large_verify|lmhead]
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own batch
+(rows are independent: weak scaling, no data-path collective); the barrier
+and the max-over-ranks time use torch.distributed.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "logit rows/s and achieved HBM GB/s (frac of roofline) for sharded argmax+verify"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=["large_verify", "lmhead"], default="large_verify")
+    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="target CPU time of the oracle baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--rows", type=int, default=None,
+                   help="keep only the first rows (whole requests) of the workload; "
+                        "for small profiling captures")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS}, "fallback"
+
+
+def source_digest(*rel_paths):
+    h = hashlib.sha256()
+    for rel in rel_paths:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(profile_name, kernel_sources):
+    """DRAM bytes per launch recorded by an ncu capture in profiles/, or None
+    when the kernel source changed since that capture."""
+    path = os.path.join(ROOT, "profiles", profile_name)
+    try:
+        fields = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and line.strip().startswith("- "):
+                    k, v = line.strip()[2:].split(":", 1)
+                    fields[k.strip()] = v.strip().strip("`")
+        if fields.get("source_digest") != source_digest(*kernel_sources):
+            return None
+        return float(fields["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while running."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_max": max(power) if power else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# process group (torchrun) helpers: barrier and max over ranks only
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def init_dist(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value, world, device=None):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# the device path (our kernels through the binding)
+# ---------------------------------------------------------------------------
+
+class VerifyPath:
+    """Device buffers and one step of the large-verify path."""
+
+    def __init__(self, c, torch, sga):
+        self.torch, self.sga = torch, sga
+        self.rows = c["logits"].shape[0]
+        self.shards = c["shards"]
+        self.org = c["org_vocab"]
+        self.k = c["k"]
+        self.cu_host = c["cu_num_draft"]
+        self.n = self.cu_host.size - 1
+        self.x = torch.from_numpy(c["logits"].view(np.int16)).view(torch.bfloat16).cuda()
+        self.stats = sga.new_stats(len(self.shards) * self.rows)
+        self.cu = torch.from_numpy(self.cu_host).cuda()
+        # drafts: copy the target's greedy token where the plan says so; the
+        # target tokens come from one untimed pass of the device path
+        t = torch.empty(self.rows, dtype=torch.int32, device="cuda")
+        self.run_argmax()
+        sga.sga_shard_reduce(self.stats, len(self.shards), self.rows, t)
+        self.drafts_host = wl.compose_drafts(t.cpu().numpy(), self.cu_host, c["flags"], c["rand_ids"])
+        self.drafts = torch.from_numpy(self.drafts_host).cuda()
+        i32 = dict(dtype=torch.int32, device="cuda")
+        self.sampled = torch.empty((self.n, self.k + 1), **i32)
+        self.num_sampled = torch.empty(self.n, **i32)
+        self.num_rejected = torch.empty(self.n, **i32)
+        self.bonus = torch.empty(self.n, **i32)
+        self.launches_per_step = len(self.shards) + 1
+        elt = 2
+        self.argmax_bytes = [self.rows * (w * elt + 8) for _, w in self.shards]
+        self.step_bytes = (sum(self.argmax_bytes) + 8 * len(self.shards) * self.rows
+                           + 4 * int(self.cu_host[-1]) + 4 * (self.n + 1)
+                           + 4 * self.n * (self.k + 1) + 12 * self.n)
+
+    def run_argmax(self, events=None):
+        for s, (o, w) in enumerate(self.shards):
+            if events is not None:
+                events[2 * s].record()
+            self.sga.sga_local_argmax(self.x[:, o:o + w], o, w, self.org,
+                                      self.stats[s * self.rows:(s + 1) * self.rows])
+            if events is not None:
+                events[2 * s + 1].record()
+
+    def run_verify(self):
+        self.sga.sga_greedy_verify(self.stats, len(self.shards), self.cu, self.drafts, self.k,
+                                   self.sampled, self.num_sampled, self.num_rejected, self.bonus)
+
+    def step(self, events=None):
+        self.run_argmax(events)
+        self.run_verify()
+
+
+def time_device_steps(path, steps, warmup, torch, world, rank):
+    for _ in range(warmup):
+        path.step()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    S = len(path.shards)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * S)] for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(torch.cuda.current_device()).start()
+    time.sleep(0.3)
+    start.record()
+    for i in range(steps):
+        path.step(ev[i])
+    end.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    barrier(world)
+    total_ms = start.elapsed_time(end)
+    argmax_ms = [sum(ev[i][2 * s].elapsed_time(ev[i][2 * s + 1]) for i in range(steps)) / steps
+                 for s in range(S)]
+    return total_ms, argmax_ms, clocks
+
+
+def time_e2e(path, c, steps, torch):
+    """Same metric through the public API with host buffers: every step
+    copies the step's inputs from pinned host memory to the device and reads
+    the results back."""
+    logits_h = torch.from_numpy(c["logits"].view(np.int16)).pin_memory()
+    drafts_h = torch.from_numpy(path.drafts_host).pin_memory()
+    cu_h = torch.from_numpy(path.cu_host).pin_memory()
+    outs_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory()
+              for t in (path.sampled, path.num_sampled, path.num_rejected, path.bonus)]
+    x_i16 = path.x.view(torch.int16)
+
+    def one():
+        x_i16.copy_(logits_h, non_blocking=True)
+        path.drafts.copy_(drafts_h, non_blocking=True)
+        path.cu.copy_(cu_h, non_blocking=True)
+        path.step()
+        for h, d in zip(outs_h, (path.sampled, path.num_sampled, path.num_rejected, path.bonus)):
+            h.copy_(d, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        one()
+    end.record()
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / steps
+    h2d = logits_h.numel() * 2 + drafts_h.numel() * 4 + cu_h.numel() * 4
+    d2h = sum(h.numel() * 4 for h in outs_h)
+    return ms, h2d, d2h
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle as a timed baseline (rank 0 only)
+# ---------------------------------------------------------------------------
+
+def oracle_verify_step(oracle, x, shards, org, cu, drafts, k):
+    st = oracle.gathered_stats(x, shards, org)
+    return oracle.greedy_verify(st, len(shards), cu, drafts, k)
+
+
+def oracle_sample(c, n_reqs):
+    """The first n_reqs requests of the workload (whole requests)."""
+    k = c["k"]
+    rows = n_reqs * (k + 1)
+    cu = c["cu_num_draft"][:n_reqs + 1]
+    return c["logits"][:rows], cu, c["flags"][:n_reqs * k], c["rand_ids"][:n_reqs * k]
+
+
+def oracle_drafts(oracle, x, shards, org, cu, flags, rand_ids):
+    st = oracle.gathered_stats(x, shards, org)
+    _, t = oracle.shard_reduce(st, len(shards), x.shape[0])
+    return wl.compose_drafts(t, cu, flags, rand_ids)
+
+
+def cpu_baseline(c, target_seconds):
+    import oracle
+    x, cu = c["logits"], c["cu_num_draft"]
+    shards, org, k = c["shards"], c["org_vocab"], c["k"]
+    drafts = oracle_drafts(oracle, x, shards, org, cu, c["flags"], c["rand_ids"])
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle_verify_step(oracle, x, shards, org, cu, drafts, k)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= target_seconds or reps >= 500:
+            break
+    rows = x.shape[0]
+    return {"value": rows * reps / el, "unit": "rows/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"the whole workload ({rows} rows x {x.shape[1]} bf16 logits, "
+                      f"{len(shards)} shard argmaxes + verify of {cu.size - 1} requests) "
+                      f"repeated {reps} times in {el:.1f} s"}
+
+
+def run_reference(args, c_builder):
+    """--impl reference: the CPU oracle, as it stands, on the host cores, on
+    the same workload; each step is a bounded sample of whole requests sized so
+    the whole run takes about two minutes at most."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    c = c_builder()
+    k = c["k"]
+    n_total = c["cu_num_draft"].size - 1
+    # calibrate on 16 requests
+    x, cu, fl, rd = oracle_sample(c, min(16, n_total))
+    d = oracle_drafts(oracle, x, c["shards"], c["org_vocab"], cu, fl, rd)
+    t0 = time.perf_counter()
+    oracle_verify_step(oracle, x, c["shards"], c["org_vocab"], cu, d, k)
+    per_req = (time.perf_counter() - t0) / min(16, n_total)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n_reqs = int(max(1, min(n_total, budget / max(per_req, 1e-9))))
+    x, cu, fl, rd = oracle_sample(c, n_reqs)
+    d = oracle_drafts(oracle, x, c["shards"], c["org_vocab"], cu, fl, rd)
+    for _ in range(args.warmup):
+        oracle_verify_step(oracle, x, c["shards"], c["org_vocab"], cu, d, k)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_verify_step(oracle, x, c["shards"], c["org_vocab"], cu, d, k)
+    el = time.perf_counter() - t0
+    rows = x.shape[0]
+    value = rows * args.steps / el
+    sample = (f"first {n_reqs} of {n_total} requests ({rows} rows x {x.shape[1]} bf16) per "
+              f"step: {len(c['shards'])} shard argmaxes + verify")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": c["name"], "sample_rows_per_step": rows},
+            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours_verify(args):
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    from greedy_spec_decode_gb300 import build as sga_build
+    if rank == 0 or world == 1:
+        sga_build.build()
+    barrier(world)
+    import greedy_spec_decode_gb300 as sga
+
+    c = wl.large_verify(rows_limit=args.rows)
+    if args.rows is not None:
+        c["name"] += f" (first {c['logits'].shape[0]} rows)"
+    path = VerifyPath(c, torch, sga)
+    total_ms, argmax_ms, clocks = time_device_steps(path, args.steps, args.warmup, torch, world, rank)
+    total_ms = max_over_ranks(total_ms, world, "cuda")
+    step_ms = total_ms / args.steps
+    rows_per_s = world * path.rows / (step_ms * 1e-3)
+
+    pk, pk_src = peaks()
+    hbm = float(pk.get("hbm_gbs", FALLBACK_HBM_GBS))
+    argmax_bytes = sum(path.argmax_bytes)
+    argmax_s = sum(argmax_ms) * 1e-3
+    achieved = argmax_bytes / argmax_s / 1e9
+    traffic = ncu_traffic("local_argmax_large_verify.md",
+                          ["greedy_spec_decode_gb300/csrc/argmax.cu",
+                           "greedy_spec_decode_gb300/csrc/common.cuh"])
+    e2e_ms, h2d, d2h = time_e2e(path, c, args.e2e_steps, torch)
+    e2e_ms = max_over_ranks(e2e_ms, world, "cuda")
+
+    # parity of the timed outputs is the tests' job; here only a sanity check
+    # that the timed launches produced a full set of counts
+    ns = path.num_sampled.cpu().numpy()
+    assert ((ns >= 1) & (ns <= path.k + 1)).all(), "verify produced invalid counts"
+    assert sga.sga_device_error() == 0, "device error word set during the bench"
+
+    line = {
+        "metric": METRIC, "value": rows_per_s, "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": c["name"], "rows": path.rows, "vocab": int(c["logits"].shape[1]),
+                   "shards": [w for _, w in path.shards], "requests": path.n, "k": path.k,
+                   "l2": f"inputs ({c['logits'].nbytes / 1e9:.2f} GB) larger than L2 (129 MB); no flush",
+                   "parallelism": f"{world} independent replica(s), emulated TP{len(path.shards)} per GPU"},
+        "step_gbs": path.step_bytes / (step_ms * 1e-3) / 1e9,
+        "step_frac_of_hbm": path.step_bytes / (step_ms * 1e-3) / 1e9 / hbm,
+        "kernel_us": {"local_argmax_per_shard": [round(m * 1e3, 2) for m in argmax_ms],
+                      "verify_and_gaps": round((step_ms - sum(argmax_ms)) * 1e3, 2)},
+        "roofline": {"bound": "hbm", "kernel": "local_argmax_kernel<bf16>",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": traffic,
+                     "peak_source": f"{pk_src} hbm_gbs (MEASURED_PEAKS.json copy bandwidth)"
+                     if pk_src == "measured" else "fallback 6.8 TB/s",
+                     "bytes_per_launch": argmax_bytes / len(path.shards)},
+        "e2e": {"value": world * path.rows / (e2e_ms * 1e-3), "unit": "rows/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps * path.launches_per_step,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(c, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args, wl.large_verify if args.workload == "large_verify"
+                             else wl.large_verify)
+    if args.workload == "lmhead":
+        raise SystemExit("the lmhead workload is not wired into the bench yet")
+    return run_ours_verify(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,16 +1,458 @@
-// lmhead.cu -- fused LM-head GEMM + per-shard argmax (tcgen05 / TMEM / TMA).
+// lmhead.cu -- fused LM-head GEMM + per-shard argmax on the 5th-generation
+// tensor cores (tcgen05), operands staged by TMA, accumulators in TMEM.
+//
+// vLLM PR #62604, Purpose: with a vocab-parallel LM head each rank holds a
+// vocab slice of the weight; item 2 fuses get_top_tokens.  vLLM PR #39419,
+// Changes: get_top_tokens applies lm_head to the hidden states and keeps only
+// the local argmax.  Here the logits hidden . W_shard^T never reach global
+// memory: each 128 x 256 logits tile is accumulated in tensor memory and the
+// epilogue keeps a running (max, id) per row.
+//
+// Kernel structure (one CTA per SM, persistent, warp-specialised):
+//   warp 0      TMA producer: A (hidden, 128 x 64) and B (weight, 256 x 64)
+//               bf16 tiles, 128-byte swizzle, into a 4-stage shared ring.
+//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators)
+//               and issues tcgen05.mma (M=128, N=256, K=16) from one lane.
+//   warps 2..5  epilogue: tcgen05.ld of each accumulator row (one TMEM lane
+//               per thread), argmax over the tile's valid columns, partial
+//               stat to the workspace, then release the accumulator so the
+//               MMA of the next tile overlaps this epilogue.
+// Work items are (vocab tile, row tile) with the row tile fastest, so the CTAs
+// running at the same time share weight tiles through L2 and the weight is
+// streamed from HBM about once.  A small second kernel reduces the per-tile
+// partials of each row in id order.
+//
+// Every mbarrier wait is bounded in time; on expiry the CTA records
+// SGA_DEVERR_TIMEOUT, stops issuing work, waits (bounded) for its own copies
+// and MMAs in flight, frees its TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "common.cuh"
 
 namespace sga {
+namespace {
+
+constexpr int BM = 128;          // rows of hidden per tile (TMEM lanes)
+constexpr int BN = 256;          // vocab ids per tile (TMEM columns)
+constexpr int BK = 64;           // bf16 elements per 128-byte swizzled row
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;   // 16 KB
+constexpr int B_BYTES = BN * BK * 2;   // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int THREADS = 192;           // 6 warps
+constexpr int TMEM_COLS = 2 * BN;      // double-buffered accumulator
+constexpr int SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 256 /*barriers*/;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of `parity` to complete, at most kWaitLimitNs.  Returns
+// false on expiry (and on an abort raised by another role of this CTA).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          const volatile int *abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile stored as 128-byte rows
+// with the 128-byte swizzle (what TMA writes with CU_TENSOR_MAP_SWIZZLE_128B):
+// start address >> 4, leading offset unused (1), stride between 8-row groups
+// 1024 B, descriptor version 1, swizzle mode 2 (128 B).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(1) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, bf16 A
+// and B, both K-major, N = BN, M = BM.
+constexpr uint32_t kInstrDesc = (1u << 4)            // D format: f32
+                                | (1u << 7)          // A format: bf16
+                                | (1u << 10)         // B format: bf16
+                                | ((BN >> 3) << 17)  // N >> 3
+                                | ((BM >> 4) << 24); // M >> 4
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(kInstrDesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05.mma issued so far has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+struct Shared {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ void raise_abort(Shared *sh, uint32_t *err) {
+  *reinterpret_cast<volatile int *>(&sh->abort) = 1;
+  atomicOr(err, SGA_DEVERR_TIMEOUT);
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    lmhead_argmax_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                         const __grid_constant__ CUtensorMap tmap_b, int M, int num_kb,
+                         int m_tiles, int n_tiles, int valid, int shard_start,
+                         sga_stat *__restrict__ ws, uint32_t *err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *base = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *a_tiles = base;
+  uint8_t *b_tiles = base + STAGES * A_BYTES;
+  Shared *sh = reinterpret_cast<Shared *>(base + STAGES * STAGE_BYTES);
+  const volatile int *abort_flag = &sh->abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&sh->full[s]), 1);
+      mbar_init(smem_u32(&sh->empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&sh->tmem_full[b]), 1);
+      mbar_init(smem_u32(&sh->tmem_empty[b]), 4 * 32);
+    }
+    mbar_init(smem_u32(&sh->drain), 1);
+    sh->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&sh->tmem_base)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = sh->tmem_base;
+  const int total = m_tiles * n_tiles;
+
+  int prod_stage = 0;
+  uint32_t prod_phase = 0;
+  long long issued = 0;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      for (int item = blockIdx.x; item < total && !*abort_flag; item += gridDim.x) {
+        const int n = item / m_tiles, m = item % m_tiles;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(smem_u32(&sh->empty[prod_stage]), prod_phase ^ 1, abort_flag)) {
+            raise_abort(sh, err);
+            break;
+          }
+          const uint32_t full = smem_u32(&sh->full[prod_stage]);
+          mbar_expect_tx(full, STAGE_BYTES);
+          tma_load_2d(smem_u32(a_tiles + prod_stage * A_BYTES), &tmap_a, kb * BK, m * BM, full);
+          tma_load_2d(smem_u32(b_tiles + prod_stage * B_BYTES), &tmap_b, kb * BK, n * BN, full);
+          ++issued;
+          if (++prod_stage == STAGES) {
+            prod_stage = 0;
+            prod_phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ----------------------------------------------------------- MMA issuer
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      for (int item = blockIdx.x; item < total && !*abort_flag; item += gridDim.x) {
+        if (!mbar_wait(smem_u32(&sh->tmem_empty[acc]), acc_phase ^ 1, abort_flag)) {
+          raise_abort(sh, err);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(smem_u32(&sh->full[stage]), phase, abort_flag)) {
+            raise_abort(sh, err);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t a_desc = smem_desc_sw128(smem_u32(a_tiles + stage * A_BYTES));
+          const uint64_t b_desc = smem_desc_sw128(smem_u32(b_tiles + stage * B_BYTES));
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)  // 16 bf16 = 32 bytes = 2 descriptor units
+            mma_bf16(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, (kb | kk) != 0);
+          mma_commit(smem_u32(&sh->empty[stage]));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&sh->tmem_full[acc]));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 belong to this warp
+    const int row_in_tile = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int item = blockIdx.x; item < total; item += gridDim.x) {
+      const int n = item / m_tiles, m = item % m_tiles;
+      bool ok = mbar_wait(smem_u32(&sh->tmem_full[acc]), acc_phase, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        if (lane == 0) raise_abort(sh, err);
+        break;
+      }
+      tc_fence_after();
+      float best = __int_as_float(0xff800000);
+      int32_t best_id = kNoId;
+      const int col0 = n * BN;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(taddr + c * 32, r);
+        tmem_ld_wait();
+        const int cbase = col0 + c * 32;
+        if (cbase < valid) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float x = __uint_as_float(r[i]);
+            if (cbase + i < valid && scan_better(x, best)) {
+              best = x;
+              best_id = shard_start + cbase + i;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sh->tmem_empty[acc]));
+      const int row = m * BM + row_in_tile;
+      if (row < M) {
+        sga_stat st;
+        st.v = best;
+        st.id = best_id;
+        ws[static_cast<size_t>(n) * M + row] = st;
+      }
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  __syncthreads();
+  if (*abort_flag) {
+    // Let this CTA's own copies and MMAs land before its shared memory and
+    // tensor memory are released (bounded as well).
+    const int zero = 0;
+    if (warp == 0 && lane == 0) {
+      const long long outstanding = issued < STAGES ? issued : STAGES;
+      for (long long i = 1; i <= outstanding; ++i) {
+        int s = prod_stage - static_cast<int>(i);
+        uint32_t ph = prod_phase;
+        if (s < 0) {
+          s += STAGES;
+          ph ^= 1;
+        }
+        mbar_wait(smem_u32(&sh->full[s]), ph, &zero);
+      }
+    }
+    if (warp == 1 && lane == 0) {
+      mma_commit(smem_u32(&sh->drain));
+      mbar_wait(smem_u32(&sh->drain), 0, &zero);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+__global__ void lmhead_finalize_kernel(const sga_stat *__restrict__ ws, int M, int n_tiles,
+                                       int shard_start, sga_stat *__restrict__ out) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= M) return;
+  float bv = __int_as_float(0xff800000);
+  int32_t bi = kNoId;
+  for (int n = 0; n < n_tiles; ++n) {
+    const sga_stat c = ws[static_cast<size_t>(n) * M + r];
+    if (pair_beats(c.v, c.id, bv, bi)) {
+      bv = c.v;
+      bi = c.id;
+    }
+  }
+  sga_stat s;
+  s.v = bv;
+  s.id = bi == kNoId ? shard_start : bi;
+  out[r] = s;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix, box = box_rows x 64
+// columns (128 bytes, swizzled), zero fill outside.
+bool make_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, int box_rows) {
+  auto encode = get_encode_fn();
+  if (encode == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
 
 size_t lmhead_workspace_bytes(int64_t M, int64_t width) {
-  const int64_t n_tiles = (width + 255) / 256;
+  const int64_t n_tiles = (width + BN - 1) / BN;
   return static_cast<size_t>(n_tiles * M) * sizeof(sga_stat);
 }
 
-cudaError_t launch_lmhead_argmax(const void *, int64_t, int64_t, const void *, int64_t, int64_t,
-                                 int64_t, sga_stat *, void *, int, uint32_t *, cudaStream_t) {
-  return cudaErrorNotSupported;
+cudaError_t launch_lmhead_argmax(const void *hidden, int64_t M, int64_t H, const void *weight,
+                                 int64_t shard_start, int64_t width, int64_t valid,
+                                 sga_stat *out, void *workspace, int num_sms, uint32_t *err,
+                                 cudaStream_t stream) {
+  (void)width;
+  sga_stat *ws = static_cast<sga_stat *>(workspace);
+  const int m_tiles = static_cast<int>((M + BM - 1) / BM);
+  const int n_tiles = static_cast<int>((valid + BN - 1) / BN);
+  if (n_tiles > 0) {
+    CUtensorMap map_a, map_b;
+    if (!make_map(&map_a, hidden, M, H, BM) || !make_map(&map_b, weight, valid, H, BN))
+      return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(lmhead_argmax_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int total = m_tiles * n_tiles;
+    const int grid = total < num_sms ? total : num_sms;
+    lmhead_argmax_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(
+        map_a, map_b, static_cast<int>(M), static_cast<int>(H / BK), m_tiles, n_tiles,
+        static_cast<int>(valid), static_cast<int>(shard_start), ws, err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const int threads = 256;
+  lmhead_finalize_kernel<<<static_cast<unsigned>((M + threads - 1) / threads), threads, 0, stream>>>(
+      ws, static_cast<int>(M), n_tiles, static_cast<int>(shard_start), out);
+  return cudaGetLastError();
 }
 
 }  // namespace sga
