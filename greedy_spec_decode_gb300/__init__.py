@@ -178,3 +178,28 @@ def sga_device_error():
 
 def sga_clear_device_error():
     _check("sga_clear_device_error", lib().sga_clear_device_error())
+
+
+def sga_lmhead_argmax_noalloc(hidden, weight_shard, shard_start, org_vocab, out_stats,
+                              stream=None):
+    """sga_lmhead_argmax without a workspace, for callers that cannot allocate
+    device memory on their decode path (a server or plugin that owns a
+    pre-sized memory pool, or a loop where cudaMalloc would synchronise the
+    device).  Partial statistics go to a fixed 4 MiB scratch array inside the
+    library, shared by every call on the device: calls that overlap on the
+    GPU race.  Rejects M * ceil(width / 256) * 8 > 4 MiB with SGA_ERR_WORKSPACE.
+    The first call on a device resolves the scratch address for that device;
+    make it before any stream capture."""
+    fn = lib().sga_lmhead_argmax_noalloc
+    i64, vp = ctypes.c_int64, ctypes.c_void_p
+    fn.argtypes = [vp, i64, i64, vp, i64, i64, i64, vp, vp]
+    fn.restype = ctypes.c_int
+    if not (hidden.is_contiguous() and weight_shard.is_contiguous()):
+        raise ValueError("hidden and weight_shard must be contiguous")
+    M, H = hidden.shape
+    if weight_shard.size(1) != H:
+        raise ValueError("hidden and weight_shard must share H")
+    _check("sga_lmhead_argmax_noalloc", fn(
+        _ptr(hidden), M, H, _ptr(weight_shard), int(shard_start), weight_shard.size(0),
+        int(org_vocab), _ptr(out_stats), _stream(stream)))
+    return out_stats

@@ -95,4 +95,10 @@ cudaError_t launch_lmhead_argmax(const void *hidden, int64_t M, int64_t H, const
                                  sga_stat *out, void *workspace, int num_sms, uint32_t *err,
                                  cudaStream_t stream);
 
+
+// Scratch of the no-allocation LM-head entry point (lmhead.cu): its size and
+// the device address of the array on the current device.
+size_t lmhead_noalloc_scratch_bytes();
+cudaError_t lmhead_noalloc_scratch(sga_stat **out);
+
 }  // namespace sga

@@ -456,3 +456,41 @@ cudaError_t launch_lmhead_argmax(const void *hidden, int64_t M, int64_t H, const
 }
 
 }  // namespace sga
+
+// ---------------------------------------------------------------------------
+// Scratch for sga_lmhead_argmax_noalloc: the per-tile partial statistics live
+// in this fixed array instead of a caller-provided workspace.  Host code must
+// not use the array's name as a device pointer (on the host it only stands in
+// for the symbol); lmhead_noalloc_scratch() looks up its device address once
+// per device, with that device current.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr size_t kNoallocScratchBytes = SGA_LMHEAD_NOALLOC_SCRATCH_BYTES;
+constexpr int kNoallocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+sga_stat *g_noalloc_ptr[kNoallocMaxDevices];
+}  // namespace
+
+static __device__ __align__(256) sga_stat g_lmhead_noalloc_scratch[kNoallocScratchBytes / sizeof(sga_stat)];
+
+namespace sga {
+
+size_t lmhead_noalloc_scratch_bytes() { return kNoallocScratchBytes; }
+
+cudaError_t lmhead_noalloc_scratch(sga_stat **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kNoallocMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_lmhead_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = static_cast<sga_stat *>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace sga

@@ -191,6 +191,34 @@ int sga_lmhead_argmax(const void *hidden, int64_t M, int64_t H, const void *weig
   return launch_status(e);
 }
 
+// Same work as sga_lmhead_argmax, with the library's fixed scratch array in
+// place of a caller workspace, for callers that cannot allocate device memory.
+int sga_lmhead_argmax_noalloc(const void *hidden, int64_t M, int64_t H,
+                              const void *weight_shard, int64_t shard_start,
+                              int64_t shard_width, int64_t org_vocab, sga_stat *out_stats,
+                              sga_stream stream) {
+  if (M < 0 || M > (int64_t(1) << 20)) return SGA_ERR_SIZE;
+  if (H <= 0 || H % 64 != 0 || H > (int64_t(1) << 20)) return SGA_ERR_SIZE;
+  int st = check_shard(shard_start, shard_width, org_vocab);
+  if (st != SGA_OK) return st;
+  if (M == 0) return SGA_OK;
+  if (sga::lmhead_workspace_bytes(M, shard_width) > sga::lmhead_noalloc_scratch_bytes())
+    return SGA_ERR_WORKSPACE;
+  if (hidden == nullptr || weight_shard == nullptr || out_stats == nullptr) return SGA_ERR_NULL;
+  if (misaligned(hidden, 16) || misaligned(weight_shard, 16) || misaligned(out_stats, 8))
+    return SGA_ERR_ALIGN;
+  DeviceInfo d;
+  if ((st = current_device(&d)) != SGA_OK) return st;
+  sga_stat *scratch = nullptr;
+  if (sga::lmhead_noalloc_scratch(&scratch) != cudaSuccess) return SGA_ERR_CUDA;
+  const cudaError_t e = sga::launch_lmhead_argmax(
+      hidden, M, H, weight_shard, shard_start, shard_width,
+      valid_ids(shard_start, shard_width, org_vocab), out_stats, scratch, d.num_sms, d.err,
+      static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return SGA_ERR_UNSUPPORTED;
+  return launch_status(e);
+}
+
 int sga_device_error(uint32_t *out_word) {
   if (out_word == nullptr) return SGA_ERR_NULL;
   DeviceInfo d;

@@ -216,6 +216,40 @@ int sga_lmhead_argmax(const void *hidden, int64_t M, int64_t H, const void *weig
                       sga_stream stream);
 
 /*
+ * sga_lmhead_argmax_noalloc -- sga_lmhead_argmax for callers that must not
+ * allocate device memory.  The pages have no counterpart to this entry point.
+ *
+ * Some callers of this code cannot call cudaMalloc on their decode path: an
+ * inference server or framework plugin that owns a device memory pool sized
+ * at start-up and forbids allocations outside it, or a latency-critical loop
+ * where cudaMalloc/cudaFree would synchronise the device.  Such a caller may
+ * have no way to provide the workspace that sga_lmhead_argmax needs.  This
+ * entry point takes the same inputs and outputs but keeps its per-tile
+ * partial statistics in a fixed scratch array inside the library's device
+ * image (SGA_LMHEAD_NOALLOC_SCRATCH_BYTES = 4 MiB, held on every GPU that
+ * loads the library until the process exits).  It calls no allocating
+ * routine.
+ *
+ *   Arguments and results: as sga_lmhead_argmax, without workspace.
+ *   Limit: M * ceil(shard_width / 256) * 8 bytes must not exceed
+ *          SGA_LMHEAD_NOALLOC_SCRATCH_BYTES; larger calls return
+ *          SGA_ERR_WORKSPACE and enqueue nothing.
+ *   Set-up: the first call on a device looks up the device address of the
+ *          scratch array for that device (with that device current), so make
+ *          the first call on each device before any stream capture.
+ *   Sharing: every call on a device uses the same scratch array, which keeps
+ *          the last call's contents; each call writes every scratch entry it
+ *          reads, so nothing has to start at zero.  Calls whose kernels
+ *          overlap on the GPU (different streams, no ordering between them)
+ *          race on the scratch array and may return wrong results.
+ */
+#define SGA_LMHEAD_NOALLOC_SCRATCH_BYTES (4u << 20)
+int sga_lmhead_argmax_noalloc(const void *hidden, int64_t M, int64_t H,
+                              const void *weight_shard, int64_t shard_start,
+                              int64_t shard_width, int64_t org_vocab, sga_stat *out_stats,
+                              sga_stream stream);
+
+/*
  * Device error word of the current device.  Kernels OR bits into it instead
  * of trapping: SGA_DEVERR_K_RANGE (a request's K_i outside [0, max_k]),
  * SGA_DEVERR_D2T_RANGE (a winning id outside the d2t table),
