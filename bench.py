@@ -36,6 +36,7 @@ import workloads as wl  # noqa: E402
 METRIC = "logit rows/s and achieved HBM GB/s (frac of roofline) for sharded argmax+verify"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+EVENT_STRIDE = 8
 
 
 def parse_args():
@@ -49,6 +50,8 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--lmhead-vocab", type=int, default=151936,
+                   help="vocab of the fused LM-head workload (smaller for profiling)")
     p.add_argument("--rows", type=int, default=None,
                    help="keep only the first rows (whole requests) of the workload; "
                         "for small profiling captures")
@@ -212,7 +215,7 @@ class VerifyPath:
         self.num_sampled = torch.empty(self.n, **i32)
         self.num_rejected = torch.empty(self.n, **i32)
         self.bonus = torch.empty(self.n, **i32)
-        self.launches_per_step = len(self.shards) + 1
+        self.launches_per_step = 2
         elt = 2
         self.argmax_bytes = [self.rows * (w * elt + 8) for _, w in self.shards]
         self.step_bytes = (sum(self.argmax_bytes) + 8 * len(self.shards) * self.rows
@@ -220,13 +223,18 @@ class VerifyPath:
                            + 4 * self.n * (self.k + 1) + 12 * self.n)
 
     def run_argmax(self, events=None):
+        """All shards of this GPU in one launch (sga_local_argmax_shards)."""
+        if events is not None:
+            events[0].record()
+        self.sga.sga_local_argmax_shards(self.x, self.shards, self.org, self.stats)
+        if events is not None:
+            events[1].record()
+
+    def run_argmax_per_shard(self):
+        """One launch per shard, as separate tensor-parallel ranks would."""
         for s, (o, w) in enumerate(self.shards):
-            if events is not None:
-                events[2 * s].record()
             self.sga.sga_local_argmax(self.x[:, o:o + w], o, w, self.org,
                                       self.stats[s * self.rows:(s + 1) * self.rows])
-            if events is not None:
-                events[2 * s + 1].record()
 
     def run_verify(self):
         self.sga.sga_greedy_verify(self.stats, len(self.shards), self.cu, self.drafts, self.k,
@@ -236,6 +244,10 @@ class VerifyPath:
         self.run_argmax(events)
         self.run_verify()
 
+    def step_per_shard(self):
+        self.run_argmax_per_shard()
+        self.run_verify()
+
 
 def time_device_steps(path, steps, warmup, torch, world, rank):
     for _ in range(warmup):
@@ -243,22 +255,38 @@ def time_device_steps(path, steps, warmup, torch, world, rank):
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    S = len(path.shards)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * S)] for _ in range(steps)]
+    # Kernel events on every EVENT_STRIDE-th step only: an event recorded
+    # between two kernels stops the next one from launching early
+    # (programmatic dependent launch), so most steps run back to back.
+    sampled = list(range(0, steps, EVENT_STRIDE))
+    ev = {i: [torch.cuda.Event(enable_timing=True) for _ in range(2)] for i in sampled}
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(torch.cuda.current_device()).start()
     time.sleep(0.3)
     start.record()
     for i in range(steps):
-        path.step(ev[i])
+        path.step(ev.get(i))
     end.record()
     torch.cuda.synchronize()
     clocks = sampler.stop()
     barrier(world)
     total_ms = start.elapsed_time(end)
-    argmax_ms = [sum(ev[i][2 * s].elapsed_time(ev[i][2 * s + 1]) for i in range(steps)) / steps
-                 for s in range(S)]
+    argmax_ms = sum(ev[i][0].elapsed_time(ev[i][1]) for i in sampled) / len(sampled)
     return total_ms, argmax_ms, clocks
+
+
+def time_per_shard_steps(path, steps, torch):
+    """The same step with one argmax launch per shard (emulated ranks)."""
+    for _ in range(3):
+        path.step_per_shard()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        path.step_per_shard()
+    end.record()
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps
 
 
 def time_e2e(path, c, steps, torch):
@@ -404,8 +432,8 @@ def run_ours_verify(args):
     pk, pk_src = peaks()
     hbm = float(pk.get("hbm_gbs", FALLBACK_HBM_GBS))
     argmax_bytes = sum(path.argmax_bytes)
-    argmax_s = sum(argmax_ms) * 1e-3
-    achieved = argmax_bytes / argmax_s / 1e9
+    achieved = argmax_bytes / (argmax_ms * 1e-3) / 1e9
+    per_shard_ms = time_per_shard_steps(path, max(20, min(500, args.steps // 4)), torch)
     traffic = ncu_traffic("local_argmax_large_verify.md",
                           ["greedy_spec_decode_gb300/csrc/argmax.cu",
                            "greedy_spec_decode_gb300/csrc/common.cuh"])
@@ -429,14 +457,17 @@ def run_ours_verify(args):
                    "parallelism": f"{world} independent replica(s), emulated TP{len(path.shards)} per GPU"},
         "step_gbs": path.step_bytes / (step_ms * 1e-3) / 1e9,
         "step_frac_of_hbm": path.step_bytes / (step_ms * 1e-3) / 1e9 / hbm,
-        "kernel_us": {"local_argmax_per_shard": [round(m * 1e3, 2) for m in argmax_ms],
-                      "verify_and_gaps": round((step_ms - sum(argmax_ms)) * 1e3, 2)},
-        "roofline": {"bound": "hbm", "kernel": "local_argmax_kernel<bf16>",
+        "kernel_us": {"local_argmax_all_shards": round(argmax_ms * 1e3, 2),
+                      "verify_and_gaps": round((step_ms - argmax_ms) * 1e3, 2)},
+        "per_shard_launches": {"ms_per_step": per_shard_ms,
+                               "rows_per_s": world * path.rows / (per_shard_ms * 1e-3),
+                               "note": "same step with one sga_local_argmax launch per shard"},
+        "roofline": {"bound": "hbm", "kernel": "local_argmax_kernel<bf16> (all shards, one launch)",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": traffic,
                      "peak_source": f"{pk_src} hbm_gbs (MEASURED_PEAKS.json copy bandwidth)"
                      if pk_src == "measured" else "fallback 6.8 TB/s",
-                     "bytes_per_launch": argmax_bytes / len(path.shards)},
+                     "bytes_per_launch": argmax_bytes},
         "e2e": {"value": world * path.rows / (e2e_ms * 1e-3), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": args.steps * path.launches_per_step,
@@ -468,7 +499,7 @@ def run_ours_lmhead(args):
     barrier(world)
     import greedy_spec_decode_gb300 as sga
 
-    c = wl.fused_lmhead()
+    c = wl.fused_lmhead(vocab=args.lmhead_vocab)
     hidden = torch.from_numpy(c["hidden"].view(np.int16)).view(torch.bfloat16).cuda()
     weight = torch.from_numpy(c["weight"].view(np.int16)).view(torch.bfloat16).cuda()
     M, H = hidden.shape

@@ -52,6 +52,7 @@ def lib():
             "sga_version": ([], i32),
             "sga_status_string": ([i32], ctypes.c_char_p),
             "sga_local_argmax": ([vp, i32, i64, i64, i64, i64, i64, vp, vp], i32),
+            "sga_local_argmax_shards": ([vp, i32, i64, i64, i32, vp, vp, i64, vp, vp], i32),
             "sga_shard_reduce": ([vp, i32, i64, vp, vp, vp, i64, vp], i32),
             "sga_greedy_verify": ([vp, i32, i32, vp, vp, i32, vp, vp, vp, vp, vp, vp], i32),
             "sga_lmhead_argmax_workspace": ([i64, i64], sz),
@@ -123,6 +124,24 @@ def sga_local_argmax(logits, shard_start, shard_width, org_vocab, out_stats, str
     _check("sga_local_argmax", lib().sga_local_argmax(
         _ptr(logits), _dtype_code(logits), rows, ld, int(shard_start), int(shard_width),
         int(org_vocab), _ptr(out_stats), _stream(stream)))
+    return out_stats
+
+
+def sga_local_argmax_shards(logits, shards, org_vocab, out_stats, stream=None):
+    """Per-shard argmax of several shards in one launch.  `logits` is a 2-D
+    CUDA tensor whose column 0 is global id shards[0][0] (unit stride along
+    the vocab); shards = [(start, width), ...] ascending; out_stats receives
+    len(shards) * rows stats in shard-major (all_gather dim 0) order."""
+    if logits.dim() != 2 or (logits.size(1) > 1 and logits.stride(1) != 1):
+        raise ValueError("logits must be 2-D with unit stride along the vocab")
+    n = len(shards)
+    starts = (ctypes.c_int64 * n)(*[int(o) for o, _ in shards])
+    widths = (ctypes.c_int64 * n)(*[int(w) for _, w in shards])
+    rows = logits.size(0)
+    ld = logits.stride(0) if rows > 1 else max(logits.stride(0), logits.size(1))
+    _check("sga_local_argmax_shards", lib().sga_local_argmax_shards(
+        _ptr(logits), _dtype_code(logits), rows, ld, n, starts, widths, int(org_vocab),
+        _ptr(out_stats), _stream(stream)))
     return out_stats
 
 

@@ -60,6 +60,15 @@ __device__ __forceinline__ uint32_t max_nan_bf16x2(uint32_t a, uint32_t b) {
   return r;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while the previous kernel of the stream drains;
+// pdl_wait() blocks until that kernel has completed and its writes are
+// visible, pdl_launch_dependents() lets the next kernel start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void warp_argmax(float &v, int32_t &id) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
@@ -77,7 +86,16 @@ __device__ __forceinline__ void warp_argmax(float &v, int32_t &id) {
 // ---------------------------------------------------------------------------
 cudaError_t launch_local_argmax(const void *logits, int dtype, int64_t rows, int64_t ld,
                                 int64_t shard_start, int64_t width, int64_t valid,
-                                sga_stat *out, int num_sms, cudaStream_t stream);
+                                sga_stat *out, int num_sms, uint32_t *err, cudaStream_t stream);
+
+// Several shards of one logits buffer in one launch: shard s covers global
+// ids [starts[s], starts[s] + ...) held at column cols[s] of `logits`, with
+// valids[s] non-padding ids; its stats go to out[s * rows + r].
+constexpr int kMaxShardsPerLaunch = 64;
+cudaError_t launch_local_argmax_table(const void *logits, int dtype, int64_t rows, int64_t ld,
+                                      int num_shards, const int64_t *starts,
+                                      const int64_t *cols, const int64_t *valids, sga_stat *out,
+                                      int num_sms, uint32_t *err, cudaStream_t stream);
 
 cudaError_t launch_shard_reduce(const sga_stat *stats, int num_shards, int64_t rows,
                                 float *out_vals, int32_t *out_ids, const int64_t *d2t,

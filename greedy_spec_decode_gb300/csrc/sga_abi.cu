@@ -111,8 +111,38 @@ int sga_local_argmax(const void *logits, int dtype, int64_t rows, int64_t ld,
   if ((st = current_device(&d)) != SGA_OK) return st;
   return launch_status(sga::launch_local_argmax(
       logits, dtype, rows, ld, shard_start, shard_width,
-      valid_ids(shard_start, shard_width, org_vocab), out_stats, d.num_sms,
+      valid_ids(shard_start, shard_width, org_vocab), out_stats, d.num_sms, d.err,
       static_cast<cudaStream_t>(stream)));
+}
+
+int sga_local_argmax_shards(const void *logits, int dtype, int64_t rows, int64_t ld,
+                            int num_shards, const int64_t *shard_starts,
+                            const int64_t *shard_widths, int64_t org_vocab,
+                            sga_stat *out_stats, sga_stream stream) {
+  if (dtype != SGA_F32 && dtype != SGA_BF16) return SGA_ERR_DTYPE;
+  if (num_shards < 1 || num_shards > sga::kMaxShardsPerLaunch) return SGA_ERR_SIZE;
+  if (rows < 0 || rows * num_shards > (int64_t(1) << 28)) return SGA_ERR_SIZE;
+  if (shard_starts == nullptr || shard_widths == nullptr) return SGA_ERR_NULL;
+  int64_t cols[sga::kMaxShardsPerLaunch], valids[sga::kMaxShardsPerLaunch];
+  for (int s = 0; s < num_shards; ++s) {
+    const int st = check_shard(shard_starts[s], shard_widths[s], org_vocab);
+    if (st != SGA_OK) return st;
+    if (s > 0 && shard_starts[s] < shard_starts[s - 1] + shard_widths[s - 1]) return SGA_ERR_SHARD;
+    cols[s] = shard_starts[s] - shard_starts[0];
+    valids[s] = valid_ids(shard_starts[s], shard_widths[s], org_vocab);
+  }
+  if (cols[num_shards - 1] + shard_widths[num_shards - 1] > ld) return SGA_ERR_SHARD;
+  if (rows == 0) return SGA_OK;
+  if (logits == nullptr || out_stats == nullptr) return SGA_ERR_NULL;
+  if (misaligned(logits, dtype == SGA_BF16 ? 2 : 4) || misaligned(out_stats, 8))
+    return SGA_ERR_ALIGN;
+  DeviceInfo d;
+  const int st = current_device(&d);
+  if (st != SGA_OK) return st;
+  return launch_status(sga::launch_local_argmax_table(logits, dtype, rows, ld, num_shards,
+                                                      shard_starts, cols, valids, out_stats,
+                                                      d.num_sms, d.err,
+                                                      static_cast<cudaStream_t>(stream)));
 }
 
 int sga_shard_reduce(const sga_stat *stats, int num_shards, int64_t rows, float *out_vals,

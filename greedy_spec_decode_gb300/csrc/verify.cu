@@ -27,6 +27,7 @@ __global__ void __launch_bounds__(kThreads)
                          int32_t *__restrict__ out_sampled, int32_t *__restrict__ out_num_sampled,
                          int32_t *__restrict__ out_num_rejected, int32_t *__restrict__ out_bonus,
                          int32_t *__restrict__ out_target_ids, uint32_t *err) {
+  pdl_wait();  // the stats of the previous kernels in the stream are visible
   const int lane = threadIdx.x & 31;
   const int group = lane >> 4;  // request slot within the warp
   const int j = lane & 15;      // row (draft position) within the request
@@ -88,10 +89,18 @@ cudaError_t launch_greedy_verify(const sga_stat *stats, int num_shards, int num_
                                  int32_t *out_target_ids, uint32_t *err, cudaStream_t stream) {
   const int64_t threads_needed = static_cast<int64_t>(num_reqs) * 16;
   const unsigned blocks = static_cast<unsigned>((threads_needed + kThreads - 1) / kThreads);
-  greedy_verify_kernel<<<blocks, kThreads, 0, stream>>>(
-      stats, num_shards, num_reqs, cu_num_draft, draft_tokens, max_k, out_sampled,
-      out_num_sampled, out_num_rejected, out_bonus, out_target_ids, err);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, greedy_verify_kernel, stats, num_shards, num_reqs, cu_num_draft,
+                            draft_tokens, max_k, out_sampled, out_num_sampled, out_num_rejected,
+                            out_bonus, out_target_ids, err);
 }
 
 }  // namespace sga

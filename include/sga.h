@@ -121,6 +121,31 @@ int sga_local_argmax(const void *logits, int dtype, int64_t rows, int64_t ld,
                      sga_stat *out_stats, sga_stream stream);
 
 /*
+ * sga_local_argmax_shards -- sga_local_argmax for several shards of one
+ * logits buffer in a single launch (one GPU holding the vocab slices of
+ * several tensor-parallel ranks).  Same statistics, same layout: shard s of
+ * row r goes to out_stats[s*rows + r], exactly the dim-0 all-gather order.
+ * Page: as sga_local_argmax (vLLM PR #34049, Solution; vLLM PR #62604,
+ * Purpose items 1-2 and Test Plan: TP ranks emulated in one process with the
+ * per-shard statistics concatenated in rank order).
+ *
+ *   logits        device; element (r, 0) holds global id shard_starts[0] of
+ *                 row r; global id g sits at column g - shard_starts[0].
+ *   num_shards    1 .. 64.
+ *   shard_starts, shard_widths   HOST arrays of num_shards entries; shards
+ *                 ascending and non-overlapping (shard_starts[s] >=
+ *                 shard_starts[s-1] + shard_widths[s-1]); every width > 0;
+ *                 the last shard must end at or before column ld.
+ *   rows          0 .. 2^28 / num_shards.
+ *   out_stats     device, num_shards * rows entries, 8-byte aligned.
+ * Other arguments and the errors as sga_local_argmax.
+ */
+int sga_local_argmax_shards(const void *logits, int dtype, int64_t rows, int64_t ld,
+                            int num_shards, const int64_t *shard_starts,
+                            const int64_t *shard_widths, int64_t org_vocab,
+                            sga_stat *out_stats, sga_stream stream);
+
+/*
  * sga_shard_reduce -- global argmax from the gathered shard statistics,
  * optionally mapped from draft ids to target ids.
  * Page: vLLM PR #34049, Solution step 3 (reduce across ranks to the global

@@ -32,6 +32,15 @@ def gpu_gathered_stats(x_dev, shards, org_vocab, separate_buffers=False):
     return stats
 
 
+def gpu_gathered_stats_one_launch(x_dev, shards, org_vocab):
+    """All shards in one sga_local_argmax_shards launch."""
+    rows = x_dev.size(0)
+    stats = sga.new_stats(len(shards) * rows)
+    stats.fill_(-12345)
+    sga.sga_local_argmax_shards(x_dev[:, shards[0][0]:], shards, org_vocab, stats)
+    return stats
+
+
 def gpu_reduce(stats, num_shards, rows, d2t=None):
     ids = torch.full((rows,), -777, dtype=torch.int32, device="cuda")
     vals = torch.full((rows,), 7.0, dtype=torch.float32, device="cuda")

@@ -99,3 +99,24 @@ def test_missing_library_fails_loudly(monkeypatch, sga_lib):
     monkeypatch.setattr(sga_lib, "LIB_PATH", os.path.join(ROOT, "nonexistent", "libsga.so"))
     with pytest.raises(RuntimeError, match="missing"):
         sga_lib.lib()
+
+
+def test_local_argmax_shards_validation(sga_lib):
+    f = sga_lib.lib().sga_local_argmax_shards
+
+    def call(starts, widths, rows=4, ld=100, org=100, dtype=1, logits=FAKE, out=FAKE):
+        n = len(starts)
+        st = (ctypes.c_int64 * n)(*starts)
+        wd = (ctypes.c_int64 * n)(*widths)
+        return f(logits, dtype, rows, ld, n, st, wd, org, out, None)
+
+    assert call([0, 40], [50, 50]) == -3          # overlap
+    assert call([0, 50], [50, 60]) == -3          # past ld
+    assert call([0, 50], [50, 0]) == -3           # empty shard
+    assert call([0], [100], dtype=3) == -5
+    assert call([0], [100], rows=-1) == -2
+    assert call([0], [100], rows=0) == 0
+    assert call([0], [100], logits=None) == -1
+    assert f(FAKE, 1, 4, 100, 0, None, None, 100, FAKE, None) == -2
+    assert f(FAKE, 1, 4, 100, 65, None, None, 100, FAKE, None) == -2
+    assert f(FAKE, 1, 4, 100, 2, None, None, 100, FAKE, None) == -1

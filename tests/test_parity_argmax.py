@@ -27,6 +27,9 @@ def run_and_compare(x, shards, org_vocab, separate_buffers=False, x_dev=None):
     stats = gh.gpu_gathered_stats(x_dev, shards, org_vocab, separate_buffers)
     exp = oracle.gathered_stats(x, shards, org_vocab)
     gh.assert_stats_equal(gh.stats_to_numpy(stats), exp)
+    if len(shards) <= 64 and not separate_buffers:
+        one = gh.gpu_gathered_stats_one_launch(x_dev, shards, org_vocab)
+        gh.assert_stats_equal(gh.stats_to_numpy(one), exp)
     vals, ids = gh.gpu_reduce(stats, len(shards), rows)
     evals, eids = oracle.shard_reduce(exp, len(shards), rows)
     fvals, fids = oracle.full_argmax(x, org_vocab)
@@ -125,3 +128,23 @@ def test_large_verify_workload_all_rows(sga_lib):
     ids = run_and_compare(c["logits"], c["shards"], c["org_vocab"])
     for r in range(0, 4096, 100):
         assert ids[r] == c["shards"][1 + (r // 100) % 2][0] - 1
+
+
+def test_one_launch_rejects_overlapping_shards(sga_lib):
+    x_dev = torch.zeros((4, 100), dtype=torch.bfloat16, device="cuda")
+    stats = sga_lib.new_stats(8)
+    with pytest.raises(sga_lib.SgaError):
+        sga_lib.sga_local_argmax_shards(x_dev, [(0, 60), (50, 50)], 100, stats)
+    with pytest.raises(sga_lib.SgaError):
+        sga_lib.sga_local_argmax_shards(x_dev, [(0, 60), (60, 50)], 110, stats)
+
+
+def test_one_launch_subset_of_shards_with_gap(sga_lib):
+    # a GPU holding shards 1 and 3 of 4: columns are global ids minus the first start
+    x = wl.discrete_logits(77, 9, 4000, "bf16", p_nan=1e-3)
+    shards = wl.even_shards(4000, 4)
+    held = [shards[1], shards[3]]
+    x_dev = gh.to_device(x)
+    one = gh.gpu_gathered_stats_one_launch(x_dev, held, 3990)
+    exp = np.concatenate([oracle.shard_argmax(x, o, w, 3990) for o, w in held])
+    gh.assert_stats_equal(gh.stats_to_numpy(one), exp)
