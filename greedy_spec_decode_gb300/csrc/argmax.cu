@@ -20,10 +20,10 @@
 //     read element by element.
 //   * in the body a thread keeps only the NaN-propagating maximum of the best
 //     vector it has seen and that vector's index (strictly greater replaces,
-//     so ties keep the earliest vector); after the loop it reloads that one
-//     vector and picks its first element equal to the maximum (or its first
-//     NaN).  Ids ascend along each thread's sequence, so this is exactly the
-//     scan rule of the oracle.
+//     so ties keep the earliest vector) together with that vector's 16 bytes;
+//     after the loop it picks the vector's first element equal to the maximum
+//     (or its first NaN).  Ids ascend along each thread's sequence, so this is
+//     exactly the scan rule of the oracle.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -217,6 +217,7 @@ __global__ void __launch_bounds__(kThreads + (kBulk ? 32 : 0), kBulk ? 2048 / (k
   const uint4 *vp = reinterpret_cast<const uint4 *>(p + head * kElt);
   float vbest = __int_as_float(0xff800000);
   int vbest_idx = -1;
+  uint4 vraw = make_uint4(0u, 0u, 0u, 0u);  // the best vector itself
   if (!kBulk) {
     int v = v0 + tid;
     for (; v + (kUnroll - 1) * kThreads < v1; v += kUnroll * kThreads) {
@@ -229,14 +230,17 @@ __global__ void __launch_bounds__(kThreads + (kBulk ? 32 : 0), kBulk ? 2048 / (k
         if (scan_better(m, vbest)) {
           vbest = m;
           vbest_idx = v + u * kThreads;
+          vraw = a[u];
         }
       }
     }
     for (; v < v1; v += kThreads) {
-      const float m = vec_max<kBf16>(ld_body(vp + v));
+      const uint4 a = ld_body(vp + v);
+      const float m = vec_max<kBf16>(a);
       if (scan_better(m, vbest)) {
         vbest = m;
         vbest_idx = v;
+        vraw = a;
       }
     }
   } else {
@@ -297,10 +301,12 @@ __global__ void __launch_bounds__(kThreads + (kBulk ? 32 : 0), kBulk ? 2048 / (k
         const int n = min(kStageVec, nbody - j * kStageVec);
         const uint4 *st = ring + slot * kStageVec;
         for (int i = tid; i < n; i += kThreads) {
-          const float m = vec_max<kBf16>(st[i]);
+          const uint4 a = st[i];
+          const float m = vec_max<kBf16>(a);
           if (scan_better(m, vbest)) {
             vbest = m;
             vbest_idx = v0 + j * kStageVec + i;
+            vraw = a;
           }
         }
         __syncwarp();
@@ -320,8 +326,7 @@ __global__ void __launch_bounds__(kThreads + (kBulk ? 32 : 0), kBulk ? 2048 / (k
     }
   }
   pdl_launch_dependents();
-  if (vbest_idx >= 0)
-    scan_vec<kBf16>(__ldg(vp + vbest_idx), id0 + head + vbest_idx * kVec, best, best_id);
+  if (vbest_idx >= 0) scan_vec<kBf16>(vraw, id0 + head + vbest_idx * kVec, best, best_id);
 
   if (chunk == chunks - 1 && tid < tail) {
     const int j = head + nvec * kVec + tid;
@@ -407,7 +412,14 @@ __global__ void shard_reduce_kernel(const sga_stat *__restrict__ stats, int num_
 #endif
 int pick_chunks(int64_t rs_count, int64_t max_valid, int elt, int num_sms) {
   const int64_t nvec = max_valid * elt / 16;
-  const int64_t want_ctas = static_cast<int64_t>(num_sms) * kMinBlocks * SGA_ARGMAX_WAVES;
+  // resident CTAs per SM: bounded by threads, and for the ring by shared memory
+  int64_t per_sm = kMinBlocks;
+  if (SGA_ARGMAX_BULK) {
+    const int64_t by_threads = 2048 / (kThreads + 32);
+    const int64_t by_smem = (227 * 1024) / (kStages * kStageVec * 16 + 1024 + 256);
+    per_sm = by_threads < by_smem ? by_threads : by_smem;
+  }
+  const int64_t want_ctas = static_cast<int64_t>(num_sms) * per_sm * SGA_ARGMAX_WAVES;
   int chunks = 1;
   while (chunks < kMaxChunks && nvec / (2 * chunks) >= kThreads && rs_count * chunks < want_ctas)
     chunks *= 2;

@@ -19,8 +19,8 @@
 //               MMA of the next tile overlaps this epilogue.
 // Work items are (vocab tile, row tile) with the row tile fastest, so the CTAs
 // running at the same time share weight tiles through L2 and the weight is
-// streamed from HBM about once.  A small second kernel reduces the per-tile
-// partials of each row in id order.
+// streamed from HBM about once.  A small second kernel reduces each row's
+// per-tile partials (one warp per row, row-major workspace).
 //
 // Every mbarrier wait is bounded in time; on expiry the CTA records
 // SGA_DEVERR_TIMEOUT, stops issuing work, waits (bounded) for its own copies
@@ -38,13 +38,24 @@ namespace {
 constexpr int BM = 128;          // rows of hidden per tile (TMEM lanes)
 constexpr int BN = 256;          // vocab ids per tile (TMEM columns)
 constexpr int BK = 64;           // bf16 elements per 128-byte swizzled row
-constexpr int STAGES = 4;
+#ifndef SGA_LMHEAD_STAGES
+#define SGA_LMHEAD_STAGES 4
+#endif
+#ifndef SGA_LMHEAD_MAX_CTAS
+#define SGA_LMHEAD_MAX_CTAS 0  // 0: one CTA per SM
+#endif
+#ifndef SGA_LMHEAD_2SM
+#define SGA_LMHEAD_2SM 1  // 2-SM tiles when M > 128
+#endif
+constexpr int STAGES = SGA_LMHEAD_STAGES;
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB
 constexpr int B_BYTES = BN * BK * 2;   // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;           // 6 warps
 constexpr int TMEM_COLS = 2 * BN;      // double-buffered accumulator
-constexpr int SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 256 /*barriers*/;
+// At least 120 KB so that one CTA (holding all 512 TMEM columns) runs per SM.
+constexpr int SMEM_NEEDED = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 256 /*barriers*/;
+constexpr int SMEM_BYTES = SMEM_NEEDED > 120 * 1024 ? SMEM_NEEDED : 120 * 1024;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
 // ---------------------------------------------------------------- PTX helpers
@@ -334,7 +345,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         sga_stat st;
         st.v = best;
         st.id = best_id;
-        ws[static_cast<size_t>(n) * M + row] = st;
+        ws[static_cast<size_t>(row) * n_tiles + n] = st;
       }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
@@ -372,23 +383,327 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// 2-SM variant (tcgen05 cta_group::2): a cluster of two CTAs computes a
+// 256-row x 256-id tile.  Each CTA stages its own 128 rows of hidden and its
+// own 128 weight rows (half of the tile's ids), so per SM the shared-memory
+// stage is 32 KB instead of 48 KB and the L2 traffic per MMA is 2/3 of the
+// 1-SM kernel's; six stages fit.  The even CTA (leader) issues every MMA; the
+// tile's rows 0..127 accumulate in the leader's TMEM and rows 128..255 in the
+// follower's, all 256 ids in both.
+//   full[s]       leader only: 1 arrival (the leader's expect_tx of the
+//                 pair's 64 KB); both CTAs' TMA copies complete their bytes
+//                 on it (cta_group::2 copies may signal the peer's barrier).
+//   empty[s]      1 arrival in each CTA, from the leader's multicast commit.
+//   tmem_full[b]  1 arrival in each CTA, from the leader's multicast commit.
+//   tmem_empty[b] leader only: 8 arrivals, one per epilogue warp of the pair.
+// ---------------------------------------------------------------------------
+#ifndef SGA_LMHEAD_STAGES2
+#define SGA_LMHEAD_STAGES2 6
+#endif
+constexpr int STAGES2 = SGA_LMHEAD_STAGES2;
+constexpr int A2_BYTES = 128 * BK * 2;  // 16 KB
+constexpr int B2_BYTES = 128 * BK * 2;  // 16 KB (half of the 256-id tile)
+constexpr int STAGE2_BYTES = A2_BYTES + B2_BYTES;
+constexpr int SMEM2_BYTES = 1024 + STAGES2 * STAGE2_BYTES + 256;
+constexpr uint32_t kInstrDesc2 = (1u << 4) | (1u << 7) | (1u << 10) | ((256u >> 3) << 17) |
+                                 ((256u >> 4) << 24);  // M = 256 across the pair, N = 256
+
+struct Shared2 {
+  uint64_t full[STAGES2];
+  uint64_t empty[STAGES2];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address of the same shared variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+// TMA tile copy into this CTA's shared memory whose completion is counted on
+// an mbarrier that may live in the peer CTA of the pair (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                                 uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(kInstrDesc2), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on `bar` in both CTAs of the pair when the MMAs issued so far
+// have completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+  const uint16_t mask = 0x3;
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ void raise_abort2(Shared2 *sh, uint32_t *err) {
+  *reinterpret_cast<volatile int *>(&sh->abort) = 1;
+  atomicOr(err, SGA_DEVERR_TIMEOUT);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    lmhead_argmax_2sm_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                             const __grid_constant__ CUtensorMap tmap_b, int M, int num_kb,
+                             int m_pairs, int n_tiles, int valid, int shard_start,
+                             sga_stat *__restrict__ ws, uint32_t *err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *base = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *a_tiles = base;
+  uint8_t *b_tiles = base + STAGES2 * A2_BYTES;
+  Shared2 *sh = reinterpret_cast<Shared2 *>(base + STAGES2 * STAGE2_BYTES);
+  const volatile int *abort_flag = &sh->abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1;
+  const int num_pairs = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES2; ++s) {
+      mbar_init(smem_u32(&sh->full[s]), 1);
+      mbar_init(smem_u32(&sh->empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&sh->tmem_full[b]), 1);
+      mbar_init(smem_u32(&sh->tmem_empty[b]), 8);
+    }
+    mbar_init(smem_u32(&sh->drain), 1);
+    sh->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&sh->tmem_base)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+  tc_fence_after();
+  const uint32_t tmem_base = sh->tmem_base;
+  const int total = m_pairs * n_tiles;
+
+  int prod_stage = 0;
+  uint32_t prod_phase = 0;
+  long long issued = 0;
+
+  if (warp == 0 && lane == 0) {
+    // -------------------------------------------------------------- producer
+    for (int item = pair; item < total && !*abort_flag; item += num_pairs) {
+      const int n = item / m_pairs, mp = item % m_pairs;
+      for (int kb = 0; kb < num_kb; ++kb) {
+        if (!mbar_wait(smem_u32(&sh->empty[prod_stage]), prod_phase ^ 1, abort_flag)) {
+          raise_abort2(sh, err);
+          break;
+        }
+        const uint32_t full_leader = map_to_rank(smem_u32(&sh->full[prod_stage]), 0);
+        if (leader) mbar_expect_tx(smem_u32(&sh->full[prod_stage]), 2 * STAGE2_BYTES);
+        tma_load_2d_pair(smem_u32(a_tiles + prod_stage * A2_BYTES), &tmap_a, kb * BK,
+                         mp * 256 + static_cast<int>(rank) * 128, full_leader);
+        tma_load_2d_pair(smem_u32(b_tiles + prod_stage * B2_BYTES), &tmap_b, kb * BK,
+                         n * 256 + static_cast<int>(rank) * 128, full_leader);
+        ++issued;
+        if (++prod_stage == STAGES2) {
+          prod_stage = 0;
+          prod_phase ^= 1;
+        }
+      }
+    }
+  } else if (warp == 1 && lane == 0 && leader) {
+    // -------------------------------------------------- MMA issuer (leader)
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    for (int item = pair; item < total && !*abort_flag; item += num_pairs) {
+      if (!mbar_wait(smem_u32(&sh->tmem_empty[acc]), acc_phase ^ 1, abort_flag)) {
+        raise_abort2(sh, err);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      bool ok = true;
+      for (int kb = 0; kb < num_kb; ++kb) {
+        if (!mbar_wait(smem_u32(&sh->full[stage]), phase, abort_flag)) {
+          raise_abort2(sh, err);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t a_desc = smem_desc_sw128(smem_u32(a_tiles + stage * A2_BYTES));
+        const uint64_t b_desc = smem_desc_sw128(smem_u32(b_tiles + stage * B2_BYTES));
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          mma_bf16_pair(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, (kb | kk) != 0);
+        mma_commit_pair(smem_u32(&sh->empty[stage]));
+        if (++stage == STAGES2) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+      mma_commit_pair(smem_u32(&sh->tmem_full[acc]));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  } else if (warp >= 2) {
+    // -------------------------------------------------- epilogue (both CTAs)
+    const int quarter = warp & 3;
+    const int row_in_tile = static_cast<int>(rank) * 128 + quarter * 32 + lane;
+    const uint32_t empty_leader[2] = {map_to_rank(smem_u32(&sh->tmem_empty[0]), 0),
+                                      map_to_rank(smem_u32(&sh->tmem_empty[1]), 0)};
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int item = pair; item < total; item += num_pairs) {
+      const int n = item / m_pairs, mp = item % m_pairs;
+      bool ok = mbar_wait(smem_u32(&sh->tmem_full[acc]), acc_phase, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        if (lane == 0) raise_abort2(sh, err);
+        break;
+      }
+      tc_fence_after();
+      float best = __int_as_float(0xff800000);
+      int32_t best_id = kNoId;
+      const int col0 = n * BN;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(taddr + c * 32, r);
+        tmem_ld_wait();
+        const int cbase = col0 + c * 32;
+        if (cbase < valid) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float x = __uint_as_float(r[i]);
+            if (cbase + i < valid && scan_better(x, best)) {
+              best = x;
+              best_id = shard_start + cbase + i;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader)
+          mbar_arrive(smem_u32(&sh->tmem_empty[acc]));
+        else
+          mbar_arrive_remote(empty_leader[acc]);
+      }
+      const int row = mp * 256 + row_in_tile;
+      if (row < M) {
+        sga_stat st;
+        st.v = best;
+        st.id = best_id;
+        ws[static_cast<size_t>(row) * n_tiles + n] = st;
+      }
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  __syncthreads();
+  if (*abort_flag) {
+    const int zero = 0;
+    if (warp == 0 && lane == 0) {
+      if (leader) {
+        // the leader's full barriers count the copies of both CTAs
+        const long long outstanding = issued < STAGES2 ? issued : STAGES2;
+        for (long long i = 1; i <= outstanding; ++i) {
+          int s = prod_stage - static_cast<int>(i);
+          uint32_t ph = prod_phase;
+          if (s < 0) {
+            s += STAGES2;
+            ph ^= 1;
+          }
+          mbar_wait(smem_u32(&sh->full[s]), ph, &zero);
+        }
+      } else if (issued > 0) {
+        // the follower's copies complete on the leader's barriers, which it
+        // cannot wait on: give them a bounded 1 ms to land
+        const unsigned long long t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 1000000ull) {
+        }
+      }
+    }
+    if (warp == 1 && lane == 0 && leader) {
+      mma_commit_pair(smem_u32(&sh->drain));
+      mbar_wait(smem_u32(&sh->drain), 0, &zero);
+    }
+  }
+  // the peer may still read this CTA's shared memory or write its TMEM
+  tc_fence_before();
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// One warp per row: lanes stride over the row's per-tile partials (contiguous,
+// row-major workspace) and merge them with the (value, id) order.
 __global__ void lmhead_finalize_kernel(const sga_stat *__restrict__ ws, int M, int n_tiles,
                                        int shard_start, sga_stat *__restrict__ out) {
-  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
   if (r >= M) return;
   float bv = __int_as_float(0xff800000);
   int32_t bi = kNoId;
-  for (int n = 0; n < n_tiles; ++n) {
-    const sga_stat c = ws[static_cast<size_t>(n) * M + r];
+  const sga_stat *row = ws + static_cast<size_t>(r) * n_tiles;
+  for (int n = lane; n < n_tiles; n += 32) {
+    const sga_stat c = row[n];
     if (pair_beats(c.v, c.id, bv, bi)) {
       bv = c.v;
       bi = c.id;
     }
   }
-  sga_stat s;
-  s.v = bv;
-  s.id = bi == kNoId ? shard_start : bi;
-  out[r] = s;
+  warp_argmax(bv, bi);
+  if (lane == 0) {
+    sga_stat s;
+    s.v = bv;
+    s.id = bi == kNoId ? shard_start : bi;
+    out[r] = s;
+  }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
@@ -419,6 +734,29 @@ bool make_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, int
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Number of 2-CTA clusters of the 2-SM kernel that fit on the current device
+// at once (queried once per device).
+int resident_pairs(int num_sms) {
+  static std::mutex mu;
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * (num_sms / 2)));
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM2_BYTES;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, lmhead_argmax_2sm_kernel, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    cache[dev] = n > num_sms / 2 ? num_sms / 2 : n;
+  }
+  return cache[dev];
+}
+
 }  // namespace
 
 size_t lmhead_workspace_bytes(int64_t M, int64_t width) {
@@ -434,7 +772,27 @@ cudaError_t launch_lmhead_argmax(const void *hidden, int64_t M, int64_t H, const
   sga_stat *ws = static_cast<sga_stat *>(workspace);
   const int m_tiles = static_cast<int>((M + BM - 1) / BM);
   const int n_tiles = static_cast<int>((valid + BN - 1) / BN);
-  if (n_tiles > 0) {
+  if (n_tiles > 0 && SGA_LMHEAD_2SM && M > BM && num_sms >= 2) {
+    // 2-SM tiles (256 rows per CTA pair)
+    CUtensorMap map_a, map_b;
+    if (!make_map(&map_a, hidden, M, H, 128) || !make_map(&map_b, weight, valid, H, 128))
+      return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(lmhead_argmax_2sm_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM2_BYTES);
+    if (e != cudaSuccess) return e;
+    const int m_pairs = static_cast<int>((M + 255) / 256);
+    const int total = m_pairs * n_tiles;
+    // A persistent grid must be fully resident: a cluster needs both CTAs in
+    // one GPC, so fewer than num_sms / 2 pairs may fit at once.
+    const int resident = resident_pairs(num_sms);
+    if (resident <= 0) return cudaErrorLaunchOutOfResources;
+    const int pairs = total < resident ? total : resident;
+    lmhead_argmax_2sm_kernel<<<2 * pairs, THREADS, SMEM2_BYTES, stream>>>(
+        map_a, map_b, static_cast<int>(M), static_cast<int>(H / BK), m_pairs, n_tiles,
+        static_cast<int>(valid), static_cast<int>(shard_start), ws, err);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  } else if (n_tiles > 0) {
     CUtensorMap map_a, map_b;
     if (!make_map(&map_a, hidden, M, H, BM) || !make_map(&map_b, weight, valid, H, BN))
       return cudaErrorInvalidValue;
@@ -442,15 +800,16 @@ cudaError_t launch_lmhead_argmax(const void *hidden, int64_t M, int64_t H, const
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int total = m_tiles * n_tiles;
-    const int grid = total < num_sms ? total : num_sms;
+    int grid = total < num_sms ? total : num_sms;
+    if (SGA_LMHEAD_MAX_CTAS > 0 && grid > SGA_LMHEAD_MAX_CTAS) grid = SGA_LMHEAD_MAX_CTAS;
     lmhead_argmax_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(
         map_a, map_b, static_cast<int>(M), static_cast<int>(H / BK), m_tiles, n_tiles,
         static_cast<int>(valid), static_cast<int>(shard_start), ws, err);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  const int threads = 256;
-  lmhead_finalize_kernel<<<static_cast<unsigned>((M + threads - 1) / threads), threads, 0, stream>>>(
+  const int threads = 256;  // 8 rows per block
+  lmhead_finalize_kernel<<<static_cast<unsigned>((M + 7) / 8), threads, 0, stream>>>(
       ws, static_cast<int>(M), n_tiles, static_cast<int>(shard_start), out);
   return cudaGetLastError();
 }
