@@ -352,6 +352,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   }
 
+  pdl_launch_dependents();
   __syncthreads();
   if (*abort_flag) {
     // Let this CTA's own copies and MMAs land before its shared memory and
@@ -640,6 +641,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
   }
 
+  pdl_launch_dependents();
   __syncthreads();
   if (*abort_flag) {
     const int zero = 0;
@@ -684,6 +686,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 // row-major workspace) and merge them with the (value, id) order.
 __global__ void lmhead_finalize_kernel(const sga_stat *__restrict__ ws, int M, int n_tiles,
                                        int shard_start, sga_stat *__restrict__ out) {
+  pdl_wait();  // the partials of the GEMM kernel are complete and visible
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= M) return;
@@ -808,10 +811,19 @@ cudaError_t launch_lmhead_argmax(const void *hidden, int64_t M, int64_t H, const
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  const int threads = 256;  // 8 rows per block
-  lmhead_finalize_kernel<<<static_cast<unsigned>((M + 7) / 8), threads, 0, stream>>>(
-      ws, static_cast<int>(M), n_tiles, static_cast<int>(shard_start), out);
-  return cudaGetLastError();
+  // 8 rows per block; programmatic dependent launch lets the blocks become
+  // resident while the GEMM kernel drains (they wait in pdl_wait()).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((M + 7) / 8));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, lmhead_finalize_kernel, static_cast<const sga_stat *>(ws),
+                            static_cast<int>(M), n_tiles, static_cast<int>(shard_start), out);
 }
 
 }  // namespace sga
