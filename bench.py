@@ -50,6 +50,8 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--lmhead-rows", type=int, default=512,
+                   help="rows (hidden states) of the fused LM-head workload")
     p.add_argument("--lmhead-vocab", type=int, default=151936,
                    help="vocab of the fused LM-head workload (smaller for profiling)")
     p.add_argument("--rows", type=int, default=None,
@@ -506,7 +508,7 @@ def run_ours_lmhead(args):
     barrier(world)
     import greedy_spec_decode_gb300 as sga
 
-    c = wl.fused_lmhead(vocab=args.lmhead_vocab)
+    c = wl.fused_lmhead(m=args.lmhead_rows, vocab=args.lmhead_vocab)
     hidden = torch.from_numpy(c["hidden"].view(np.int16)).view(torch.bfloat16).cuda()
     weight = torch.from_numpy(c["weight"].view(np.int16)).view(torch.bfloat16).cuda()
     M, H = hidden.shape
@@ -575,6 +577,7 @@ def run_ours_lmhead(args):
                    "l2": "weight (1.24 GB) larger than L2 (129 MB); no flush",
                    "parallelism": f"{world} independent replica(s), emulated TP{S} per GPU"},
         "tflops_step": flops / (step_ms * 1e-3) / 1e12,
+        "weight_gbs": weight.numel() * 2 / (kern_ms * 1e-3) / 1e9,
         "kernel_us": {"lmhead_argmax_per_step": round(kern_ms * 1e3, 2),
                       "reduce_and_gaps": round((step_ms - kern_ms) * 1e3, 2)},
         "roofline": {"bound": "tensor", "kernel": "lmhead_argmax_kernel",

@@ -59,6 +59,7 @@ def lib():
             "sga_lmhead_argmax": ([vp, i64, i64, vp, i64, i64, i64, vp, vp, sz, vp], i32),
             "sga_device_error": ([ctypes.POINTER(ctypes.c_uint32)], i32),
             "sga_clear_device_error": ([], i32),
+            "sga_selftest_wait_timeout": ([ctypes.c_uint64, vp, vp], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -197,6 +198,12 @@ def sga_device_error():
 
 def sga_clear_device_error():
     _check("sga_clear_device_error", lib().sga_clear_device_error())
+
+
+def sga_selftest_wait_timeout(limit_ns, waited_ns=None, stream=None):
+    """Run the bounded-wait self-test kernel (see include/sga.h)."""
+    _check("sga_selftest_wait_timeout", lib().sga_selftest_wait_timeout(
+        int(limit_ns), _ptr(waited_ns), _stream(stream)))
 
 
 def sga_lmhead_argmax_noalloc(hidden, weight_shard, shard_start, org_vocab, out_stats,

@@ -114,6 +114,10 @@ cudaError_t launch_lmhead_argmax(const void *hidden, int64_t M, int64_t H, const
                                  cudaStream_t stream);
 
 
+// Bounded-wait self-test (lmhead.cu).
+cudaError_t launch_selftest_timeout(unsigned long long limit_ns, uint32_t *err,
+                                    unsigned long long *waited_ns, cudaStream_t stream);
+
 // Scratch of the no-allocation LM-head entry point (lmhead.cu): its size and
 // the device address of the array on the current device.
 size_t lmhead_noalloc_scratch_bytes();

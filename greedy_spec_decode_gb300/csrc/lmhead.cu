@@ -95,16 +95,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase of `parity` to complete, at most kWaitLimitNs.  Returns
+// Wait for the phase of `parity` to complete, at most limit_ns.  Returns
 // false on expiry (and on an abort raised by another role of this CTA).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          const volatile int *abort_flag) {
+                                          const volatile int *abort_flag,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -709,6 +710,22 @@ __global__ void lmhead_finalize_kernel(const sga_stat *__restrict__ ws, int M, i
   }
 }
 
+// Self-test of the bounded wait: one thread waits on an mbarrier that nothing
+// ever arrives at; the wait gives up after limit_ns, the kernel records
+// SGA_DEVERR_TIMEOUT and returns, and the context stays usable.
+__global__ void selftest_timeout_kernel(unsigned long long limit_ns, uint32_t *err,
+                                        unsigned long long *waited_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int no_abort;
+  if (threadIdx.x != 0) return;
+  no_abort = 0;
+  mbar_init(smem_u32(&bar), 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  const unsigned long long t0 = global_timer_ns();
+  if (!mbar_wait(smem_u32(&bar), 0, &no_abort, limit_ns)) atomicOr(err, SGA_DEVERR_TIMEOUT);
+  if (waited_ns) *waited_ns = global_timer_ns() - t0;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -761,6 +778,12 @@ int resident_pairs(int num_sms) {
 }
 
 }  // namespace
+
+cudaError_t launch_selftest_timeout(unsigned long long limit_ns, uint32_t *err,
+                                    unsigned long long *waited_ns, cudaStream_t stream) {
+  selftest_timeout_kernel<<<1, 32, 0, stream>>>(limit_ns, err, waited_ns);
+  return cudaGetLastError();
+}
 
 size_t lmhead_workspace_bytes(int64_t M, int64_t width) {
   const int64_t n_tiles = (width + BN - 1) / BN;

@@ -249,6 +249,17 @@ int sga_lmhead_argmax_noalloc(const void *hidden, int64_t M, int64_t H,
   return launch_status(e);
 }
 
+int sga_selftest_wait_timeout(uint64_t limit_ns, uint64_t *waited_ns, sga_stream stream) {
+  if (limit_ns < 1000 || limit_ns > 1000000000ull) return SGA_ERR_SIZE;
+  if (misaligned(waited_ns, 8)) return SGA_ERR_ALIGN;
+  DeviceInfo d;
+  const int st = current_device(&d);
+  if (st != SGA_OK) return st;
+  return launch_status(sga::launch_selftest_timeout(
+      limit_ns, d.err, reinterpret_cast<unsigned long long *>(waited_ns),
+      static_cast<cudaStream_t>(stream)));
+}
+
 int sga_device_error(uint32_t *out_word) {
   if (out_word == nullptr) return SGA_ERR_NULL;
   DeviceInfo d;

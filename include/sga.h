@@ -289,6 +289,17 @@ int sga_lmhead_argmax_noalloc(const void *hidden, int64_t M, int64_t H,
 int sga_device_error(uint32_t *out_word);
 int sga_clear_device_error(void);
 
+/*
+ * sga_selftest_wait_timeout -- exercises the bounded-wait path that every
+ * pipelined kernel of this library uses (the pages have no counterpart): one
+ * thread waits on a shared-memory mbarrier that nothing arrives at; after
+ * limit_ns (1 us .. 1 s) the wait gives up, SGA_DEVERR_TIMEOUT is OR-ed into
+ * the device error word and the kernel returns normally.  waited_ns (device,
+ * nullable, 8-byte aligned) receives the time the wait took.  The context stays
+ * usable: no trap, no fault.
+ */
+int sga_selftest_wait_timeout(uint64_t limit_ns, uint64_t *waited_ns, sga_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -148,3 +148,36 @@ def test_one_launch_subset_of_shards_with_gap(sga_lib):
     one = gh.gpu_gathered_stats_one_launch(x_dev, held, 3990)
     exp = np.concatenate([oracle.shard_argmax(x, o, w, 3990) for o, w in held])
     gh.assert_stats_equal(gh.stats_to_numpy(one), exp)
+
+
+def block_pieces(shards, block):
+    """Intersections of the shards with global blocks [k*block, (k+1)*block)."""
+    pieces = []
+    for o, w in shards:
+        start = o
+        while start < o + w:
+            end = min(o + w, (start // block + 1) * block)
+            pieces.append((start, end - start))
+            start = end
+    return pieces
+
+
+@pytest.mark.parametrize("block", [8192, 1024])
+def test_block_granular_stats_on_global_boundaries(sga_lib, block):
+    # per-block statistics on global block boundaries, also across shard edges
+    # (vLLM PR #62604, Purpose item 1): every block stat is the oracle's, and
+    # the reduce over blocks is the unsharded argmax
+    c = wl.large_verify(rows_limit=160)
+    x = c["logits"]
+    pieces = block_pieces(c["shards"], block)
+    x_dev = gh.to_device(x)
+    stats = sga_lib.new_stats(len(pieces) * x.shape[0])
+    for k in range(0, len(pieces), 64):
+        part = pieces[k:k + 64]
+        sga_lib.sga_local_argmax_shards(x_dev[:, part[0][0]:], part, c["org_vocab"],
+                                        stats[k * x.shape[0]:(k + len(part)) * x.shape[0]])
+    exp = oracle.gathered_stats(x, pieces, c["org_vocab"])
+    gh.assert_stats_equal(gh.stats_to_numpy(stats), exp)
+    _, ids = gh.gpu_reduce(stats, len(pieces), x.shape[0])
+    _, full = oracle.full_argmax(x, c["org_vocab"])
+    assert (ids == full).all()
