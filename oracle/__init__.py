@@ -39,27 +39,31 @@ F32, BF16 = 0, 1
 _lib = None
 
 
+def configure(L):
+    """Set the ctypes signatures of a loaded oracle library; returns it."""
+    i64, vp, cint = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+    sig = {
+        "oracle_full_argmax": ([vp, cint, i64, i64, i64, i64, vp, vp], None),
+        "oracle_shard_argmax": ([vp, cint, i64, i64, i64, i64, i64, vp], None),
+        "oracle_shard_reduce": ([vp, cint, i64, vp, vp], None),
+        "oracle_greedy_verify": ([vp, cint, cint, vp, vp, cint, vp, vp, vp, vp, vp], cint),
+        "oracle_d2t_map": ([vp, i64, vp, i64, vp], cint),
+        "oracle_lmhead_logits": ([vp, i64, vp, i64, vp, i64, vp], None),
+        "oracle_argmax_f64": ([vp, i64, i64, i64, i64, vp, vp, vp], None),
+        "oracle_num_threads": ([], cint),
+        "oracle_set_num_threads": ([cint], None),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = res
+    return L
+
+
 def lib():
     global _lib
     if _lib is None:
-        L = ctypes.CDLL(_build.build())
-        i64, vp, cint = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
-        sig = {
-            "oracle_full_argmax": ([vp, cint, i64, i64, i64, i64, vp, vp], None),
-            "oracle_shard_argmax": ([vp, cint, i64, i64, i64, i64, i64, vp], None),
-            "oracle_shard_reduce": ([vp, cint, i64, vp, vp], None),
-            "oracle_greedy_verify": ([vp, cint, cint, vp, vp, cint, vp, vp, vp, vp, vp], cint),
-            "oracle_d2t_map": ([vp, i64, vp, i64, vp], cint),
-            "oracle_lmhead_logits": ([vp, i64, vp, i64, vp, i64, vp], None),
-            "oracle_argmax_f64": ([vp, i64, i64, i64, i64, vp, vp, vp], None),
-            "oracle_num_threads": ([], cint),
-            "oracle_set_num_threads": ([cint], None),
-        }
-        for name, (args, res) in sig.items():
-            fn = getattr(L, name)
-            fn.argtypes = args
-            fn.restype = res
-        _lib = L
+        _lib = configure(ctypes.CDLL(_build.build()))
     return _lib
 
 
