@@ -754,6 +754,25 @@ bool make_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, int
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Raise a kernel's dynamic shared-memory limit once per device (slot picks the
+// kernel), so that later calls, including calls inside a stream capture, make
+// no function-attribute call.
+cudaError_t set_smem_once(const void *kernel, int bytes, int slot) {
+  static std::mutex mu;
+  static bool done[2][64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!done[slot][dev]) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    done[slot][dev] = true;
+  }
+  return cudaSuccess;
+}
+
 // Number of 2-CTA clusters of the 2-SM kernel that fit on the current device
 // at once (queried once per device).
 int resident_pairs(int num_sms) {
@@ -803,8 +822,8 @@ cudaError_t launch_lmhead_argmax(const void *hidden, int64_t M, int64_t H, const
     CUtensorMap map_a, map_b;
     if (!make_map(&map_a, hidden, M, H, 128) || !make_map(&map_b, weight, valid, H, 128))
       return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(lmhead_argmax_2sm_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM2_BYTES);
+    cudaError_t e = set_smem_once(reinterpret_cast<const void *>(lmhead_argmax_2sm_kernel),
+                                  SMEM2_BYTES, 0);
     if (e != cudaSuccess) return e;
     const int m_pairs = static_cast<int>((M + 255) / 256);
     const int total = m_pairs * n_tiles;
@@ -822,8 +841,8 @@ cudaError_t launch_lmhead_argmax(const void *hidden, int64_t M, int64_t H, const
     CUtensorMap map_a, map_b;
     if (!make_map(&map_a, hidden, M, H, BM) || !make_map(&map_b, weight, valid, H, BN))
       return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(lmhead_argmax_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = set_smem_once(reinterpret_cast<const void *>(lmhead_argmax_kernel),
+                                  SMEM_BYTES, 1);
     if (e != cudaSuccess) return e;
     const int total = m_tiles * n_tiles;
     int grid = total < num_sms ? total : num_sms;
