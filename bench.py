@@ -442,7 +442,7 @@ def run_ours_verify(args):
     per_shard_ms = time_per_shard_steps(path, max(20, min(500, args.steps // 4)), torch)
     traffic = ncu_traffic("local_argmax_large_verify.md",
                           ["greedy_spec_decode_gb300/csrc/argmax.cu",
-                           "greedy_spec_decode_gb300/csrc/common.cuh"])
+                           "greedy_spec_decode_gb300/csrc/common.cuh"])  # device code only
     e2e_ms, h2d, d2h = time_e2e(path, c, args.e2e_steps, torch)
     e2e_ms = max_over_ranks(e2e_ms, world, "cuda")
 
@@ -582,7 +582,11 @@ def run_ours_lmhead(args):
                       "reduce_and_gaps": round((step_ms - kern_ms) * 1e3, 2)},
         "roofline": {"bound": "tensor", "kernel": "lmhead_argmax_kernel",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak,
+                     "traffic": ncu_traffic("lmhead_fused.md",
+                                            ["greedy_spec_decode_gb300/csrc/lmhead.cu",
+                                             "greedy_spec_decode_gb300/csrc/common.cuh"]),
+                     "traffic_unit": "DRAM bytes per launch of the GEMM kernel",
                      "peak_source": (f"{pk_src} bf16_tflops_sustained (cuBLAS bf16, timed in a "
                                      f"long loop)") if pk_src == "measured" else "fallback",
                      "frac_of_burst": achieved / float(pk.get("bf16_tflops", FALLBACK_BF16_TFLOPS)),

@@ -1,5 +1,6 @@
-// common.cuh -- device helpers shared by the sga kernels and the internal
-// launcher declarations used by sga_abi.cu.
+// common.cuh -- device helpers shared by the sga kernels (argmax order,
+// widening, loads, warp merge, programmatic dependent launch) and, through
+// launchers.h, the internal launcher declarations used by sga_abi.cu.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -81,46 +82,6 @@ __device__ __forceinline__ void warp_argmax(float &v, int32_t &id) {
   }
 }
 
-// ---------------------------------------------------------------------------
-// Launchers (host).  Arguments are already validated by sga_abi.cu.
-// ---------------------------------------------------------------------------
-cudaError_t launch_local_argmax(const void *logits, int dtype, int64_t rows, int64_t ld,
-                                int64_t shard_start, int64_t width, int64_t valid,
-                                sga_stat *out, int num_sms, uint32_t *err, cudaStream_t stream);
-
-// Several shards of one logits buffer in one launch: shard s covers global
-// ids [starts[s], starts[s] + ...) held at column cols[s] of `logits`, with
-// valids[s] non-padding ids; its stats go to out[s * rows + r].
-constexpr int kMaxShardsPerLaunch = 64;
-cudaError_t launch_local_argmax_table(const void *logits, int dtype, int64_t rows, int64_t ld,
-                                      int num_shards, const int64_t *starts,
-                                      const int64_t *cols, const int64_t *valids, sga_stat *out,
-                                      int num_sms, uint32_t *err, cudaStream_t stream);
-
-cudaError_t launch_shard_reduce(const sga_stat *stats, int num_shards, int64_t rows,
-                                float *out_vals, int32_t *out_ids, const int64_t *d2t,
-                                int64_t d2t_len, uint32_t *err, cudaStream_t stream);
-
-cudaError_t launch_greedy_verify(const sga_stat *stats, int num_shards, int num_reqs,
-                                 const int32_t *cu_num_draft, const int32_t *draft_tokens,
-                                 int max_k, int32_t *out_sampled, int32_t *out_num_sampled,
-                                 int32_t *out_num_rejected, int32_t *out_bonus,
-                                 int32_t *out_target_ids, uint32_t *err, cudaStream_t stream);
-
-size_t lmhead_workspace_bytes(int64_t M, int64_t width);
-cudaError_t launch_lmhead_argmax(const void *hidden, int64_t M, int64_t H, const void *weight,
-                                 int64_t shard_start, int64_t width, int64_t valid,
-                                 sga_stat *out, void *workspace, int num_sms, uint32_t *err,
-                                 cudaStream_t stream);
-
-
-// Bounded-wait self-test (lmhead.cu).
-cudaError_t launch_selftest_timeout(unsigned long long limit_ns, uint32_t *err,
-                                    unsigned long long *waited_ns, cudaStream_t stream);
-
-// Scratch of the no-allocation LM-head entry point (lmhead.cu): its size and
-// the device address of the array on the current device.
-size_t lmhead_noalloc_scratch_bytes();
-cudaError_t lmhead_noalloc_scratch(sga_stat **out);
-
 }  // namespace sga
+
+#include "launchers.h"
