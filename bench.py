@@ -45,7 +45,8 @@ def parse_args():
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["large_verify", "lmhead"], default="large_verify")
+    p.add_argument("--workload", choices=["large_verify", "lmhead", "draft_top_tokens",
+                                          "greedy_verify"], default="large_verify")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
@@ -605,6 +606,98 @@ def run_ours_lmhead(args):
     return 0
 
 
+def run_ours_small(args, builder):
+    """L2-resident workloads (draft get_top_tokens, small greedy verify): one
+    step = the one-launch shard argmax + the reduce (no drafts) or the fused
+    verify.  Each timed step follows an L2 flush (a 256 MB write) and is timed
+    alone with CUDA events; value = rows / mean step time."""
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    from greedy_spec_decode_gb300 import build as sga_build
+    if rank == 0 or world == 1:
+        sga_build.build()
+    barrier(world)
+    import greedy_spec_decode_gb300 as sga
+
+    c = builder()
+    x_np = c["logits"]
+    x = (torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16) if x_np.dtype == np.uint16
+         else torch.from_numpy(x_np)).cuda()
+    rows, shards, org = x.shape[0], c["shards"], c["org_vocab"]
+    S = len(shards)
+    stats = sga.new_stats(S * rows)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    verify = "k" in c
+    if verify:
+        k, cu_np = c["k"], c["cu_num_draft"]
+        n = cu_np.size - 1
+        cu = torch.from_numpy(cu_np).cuda()
+        t = torch.empty(rows, **i32)
+        sga.sga_local_argmax_shards(x, shards, org, stats)
+        sga.sga_shard_reduce(stats, S, rows, t)
+        drafts = torch.from_numpy(wl.compose_drafts(t.cpu().numpy(), cu_np, c["flags"],
+                                                    c["rand_ids"])).cuda()
+        outs = [torch.empty((n, k + 1), **i32)] + [torch.empty(n, **i32) for _ in range(3)]
+    else:
+        ids = torch.empty(rows, **i32)
+
+    def step():
+        sga.sga_local_argmax_shards(x, shards, org, stats)
+        if verify:
+            sga.sga_greedy_verify(stats, S, cu, drafts, k, *outs)
+        else:
+            sga.sga_shard_reduce(stats, S, rows, ids)
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    sampler = ClockSampler(torch.cuda.current_device()).start()
+    time.sleep(0.3)
+    for a, b in evs:
+        flush.zero_()
+        a.record()
+        step()
+        b.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    barrier(world)
+    times = [a.elapsed_time(b) for a, b in evs]
+    step_ms = max_over_ranks(sum(times) / len(times), world, "cuda")
+    elt = x.element_size()
+    step_bytes = sum(rows * (w * elt + 8) for _, w in shards)
+    pk, pk_src = peaks()
+    hbm = float(pk.get("hbm_gbs", FALLBACK_HBM_GBS))
+    assert sga.sga_device_error() == 0
+    line = {
+        "metric": METRIC, "value": world * rows / (step_ms * 1e-3), "unit": "rows/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "us_per_step_min": min(times) * 1e3, "us_per_step_median": sorted(times)[len(times) // 2] * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if elt == 2 else "f32", "data": "synthetic",
+        "config": {"workload": c["name"], "rows": rows, "shards": [w for _, w in shards],
+                   "l2": "inputs fit in L2: 256 MB flush before every timed step",
+                   "step": "one-launch shard argmax + " + ("fused verify" if verify else "shard reduce")},
+        "step_gbs": step_bytes / (step_ms * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "achieved": step_bytes / (step_ms * 1e-3) / 1e9, "peak": hbm,
+                     "unit": "GB/s", "frac": step_bytes / (step_ms * 1e-3) / 1e9 / hbm,
+                     "traffic": None, "note": "latency-bound at this size; whole step timed"},
+        "gpu_launches": args.steps * 2,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -612,6 +705,10 @@ def main():
                              else wl.large_verify)
     if args.workload == "lmhead":
         return run_ours_lmhead(args)
+    if args.workload == "draft_top_tokens":
+        return run_ours_small(args, wl.draft_top_tokens)
+    if args.workload == "greedy_verify":
+        return run_ours_small(args, wl.greedy_verify_small)
     return run_ours_verify(args)
 
 
