@@ -45,7 +45,10 @@ constexpr int BK = 64;           // bf16 elements per 128-byte swizzled row
 #define SGA_LMHEAD_MAX_CTAS 0  // 0: one CTA per SM
 #endif
 #ifndef SGA_LMHEAD_2SM
-#define SGA_LMHEAD_2SM 1  // 2-SM tiles when M > 128
+#define SGA_LMHEAD_2SM 1  // 2-SM tiles when M >= SGA_LMHEAD_2SM_MIN_M
+#endif
+#ifndef SGA_LMHEAD_2SM_MIN_M
+#define SGA_LMHEAD_2SM_MIN_M 129
 #endif
 constexpr int STAGES = SGA_LMHEAD_STAGES;
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB
@@ -817,7 +820,7 @@ cudaError_t launch_lmhead_argmax(const void *hidden, int64_t M, int64_t H, const
   sga_stat *ws = static_cast<sga_stat *>(workspace);
   const int m_tiles = static_cast<int>((M + BM - 1) / BM);
   const int n_tiles = static_cast<int>((valid + BN - 1) / BN);
-  if (n_tiles > 0 && SGA_LMHEAD_2SM && M > BM && num_sms >= 2) {
+  if (n_tiles > 0 && SGA_LMHEAD_2SM && M >= SGA_LMHEAD_2SM_MIN_M && num_sms >= 2) {
     // 2-SM tiles (256 rows per CTA pair)
     CUtensorMap map_a, map_b;
     if (!make_map(&map_a, hidden, M, H, 128) || !make_map(&map_b, weight, valid, H, 128))
