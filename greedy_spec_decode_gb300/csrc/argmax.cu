@@ -37,33 +37,18 @@ namespace {
 // (4096 x 202048 bf16, 3 shards in one launch): the cp.async.bulk ring (128
 // consumer threads + 1 copy warp, 4 stages of 8 KB) streams at 7.0 TB/s; the
 // plain 16-byte-load body peaks at 6.0 TB/s (256 threads, 8 loads in flight).
-// SGA_ARGMAX_THREADS: consumer threads per CTA; SGA_ARGMAX_UNROLL and
-// SGA_ARGMAX_PREFETCH apply to the plain-load body only.
+// SGA_ARGMAX_THREADS: consumer threads per CTA; SGA_ARGMAX_UNROLL applies to
+// the plain-load body only (SGA_ARGMAX_BULK=0).
 #ifndef SGA_ARGMAX_THREADS
 #define SGA_ARGMAX_THREADS 128
 #endif
 #ifndef SGA_ARGMAX_UNROLL
 #define SGA_ARGMAX_UNROLL 8
 #endif
-#ifndef SGA_ARGMAX_PREFETCH
-#define SGA_ARGMAX_PREFETCH 0
-#endif
 constexpr int kThreads = SGA_ARGMAX_THREADS;
 constexpr int kUnroll = SGA_ARGMAX_UNROLL;
 constexpr int kMinBlocks = 2048 / kThreads;
 constexpr int kMaxChunks = 8;
-
-__device__ __forceinline__ uint4 ld_body(const uint4 *p) {
-#if SGA_ARGMAX_PREFETCH
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-#else
-  return ld_stream_v4(p);
-#endif
-}
 
 struct ShardTable {
   int n;
@@ -223,7 +208,7 @@ __global__ void __launch_bounds__(kThreads + (kBulk ? 32 : 0), kBulk ? 2048 / (k
     for (; v + (kUnroll - 1) * kThreads < v1; v += kUnroll * kThreads) {
       uint4 a[kUnroll];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) a[u] = ld_body(vp + v + u * kThreads);
+      for (int u = 0; u < kUnroll; ++u) a[u] = ld_stream_v4(vp + v + u * kThreads);
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const float m = vec_max<kBf16>(a[u]);
@@ -235,7 +220,7 @@ __global__ void __launch_bounds__(kThreads + (kBulk ? 32 : 0), kBulk ? 2048 / (k
       }
     }
     for (; v < v1; v += kThreads) {
-      const uint4 a = ld_body(vp + v);
+      const uint4 a = ld_stream_v4(vp + v);
       const float m = vec_max<kBf16>(a);
       if (scan_better(m, vbest)) {
         vbest = m;

@@ -41,9 +41,6 @@ constexpr int BK = 64;           // bf16 elements per 128-byte swizzled row
 #ifndef SGA_LMHEAD_STAGES
 #define SGA_LMHEAD_STAGES 4
 #endif
-#ifndef SGA_LMHEAD_MAX_CTAS
-#define SGA_LMHEAD_MAX_CTAS 0  // 0: one CTA per SM
-#endif
 #ifndef SGA_LMHEAD_2SM
 #define SGA_LMHEAD_2SM 1  // 2-SM tiles when M >= SGA_LMHEAD_2SM_MIN_M
 #endif
@@ -848,8 +845,7 @@ cudaError_t launch_lmhead_argmax(const void *hidden, int64_t M, int64_t H, const
                                   SMEM_BYTES, 1);
     if (e != cudaSuccess) return e;
     const int total = m_tiles * n_tiles;
-    int grid = total < num_sms ? total : num_sms;
-    if (SGA_LMHEAD_MAX_CTAS > 0 && grid > SGA_LMHEAD_MAX_CTAS) grid = SGA_LMHEAD_MAX_CTAS;
+    const int grid = total < num_sms ? total : num_sms;
     lmhead_argmax_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(
         map_a, map_b, static_cast<int>(M), static_cast<int>(H / BK), m_tiles, n_tiles,
         static_cast<int>(valid), static_cast<int>(shard_start), ws, err);
