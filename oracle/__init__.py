@@ -50,6 +50,8 @@ def configure(L):
         "oracle_d2t_map": ([vp, i64, vp, i64, vp], cint),
         "oracle_lmhead_logits": ([vp, i64, vp, i64, vp, i64, vp], None),
         "oracle_argmax_f64": ([vp, i64, i64, i64, i64, vp, vp, vp], None),
+        "oracle_e4m3_value": ([ctypes.c_uint8], ctypes.c_double),
+        "oracle_lmhead_logits_fp8": ([vp, vp, i64, vp, ctypes.c_double, i64, vp, i64, vp], None),
         "oracle_num_threads": ([], cint),
         "oracle_set_num_threads": ([cint], None),
     }
@@ -215,3 +217,28 @@ def lmhead_argmax(hidden_bits, weight_bits, rows_sel, shard_start, org_vocab):
     """Per selected row: (top1, top2, id) of one shard's fp64 logits."""
     logits = lmhead_logits(hidden_bits, weight_bits, rows_sel)
     return argmax_f64(logits, shard_start, org_vocab)
+
+
+def e4m3_value(code):
+    """Exact value of one FP8 E4M3 code (uint8)."""
+    return lib().oracle_e4m3_value(int(code))
+
+
+def lmhead_logits_fp8(hidden_q, hidden_scale, weight_q, weight_scale, rows_sel):
+    """fp64 logits of the fp8 LM head for the selected rows: E4M3 codes
+    (uint8) of hidden [M, H] and of one weight shard [w, H], a positive fp32
+    scale per hidden row and one positive weight scale."""
+    hidden_q = np.ascontiguousarray(hidden_q, np.uint8)
+    weight_q = np.ascontiguousarray(weight_q, np.uint8)
+    scale = np.ascontiguousarray(hidden_scale, np.float32)
+    rows_sel = np.ascontiguousarray(rows_sel, np.int64)
+    H = hidden_q.shape[1]
+    if weight_q.shape[1] != H:
+        raise ValueError("hidden and weight must share H")
+    w = weight_q.shape[0]
+    out = np.empty((rows_sel.size, w), np.float64)
+    if rows_sel.size and w:
+        lib().oracle_lmhead_logits_fp8(_ptr(hidden_q), _ptr(scale), H, _ptr(weight_q),
+                                       float(weight_scale), w, _ptr(rows_sel), rows_sel.size,
+                                       _ptr(out))
+    return out

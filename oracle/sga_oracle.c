@@ -294,3 +294,42 @@ void oracle_set_num_threads(int n) {
   (void)n;
 #endif
 }
+
+/* OCP FP8 E4M3 (the "e4m3fn" variant) decoded exactly: sign bit, 4 exponent
+ * bits with bias 7, 3 mantissa bits; exponent 0 is subnormal (m/8 * 2^-6);
+ * S.1111.111 is NaN; there is no infinity.  Every value is exact in double. */
+static double e4m3_value(uint8_t c) {
+  const int sign = c >> 7, e = (c >> 3) & 0xF, m = c & 0x7;
+  double v;
+  if (e == 0xF && m == 0x7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m / 8.0, -6);
+  else
+    v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return sign ? -v : v;
+}
+
+double oracle_e4m3_value(uint8_t c) { return e4m3_value(c); }
+
+/* Logits of the fp8 LM-head variant: hidden and weight stored as E4M3 codes
+ * with positive scales (one per hidden row, one per weight tensor):
+ * logit[r][j] = hidden_scale[r] * weight_scale * sum_k dec(h[r][k]) * dec(w[j][k]),
+ * products and the sum in fp64 in k order.  Positive scales do not change
+ * which id is the argmax of a row, only the value. */
+void oracle_lmhead_logits_fp8(const uint8_t *hidden, const float *hidden_scale, int64_t H,
+                              const uint8_t *weight, double weight_scale, int64_t shard_width,
+                              const int64_t *rows_sel, int64_t n_sel, double *out_logits) {
+  for (int64_t q = 0; q < n_sel; ++q) {
+    const uint8_t *h = hidden + rows_sel[q] * H;
+    const double scale = (double)hidden_scale[rows_sel[q]] * weight_scale;
+    double *out = out_logits + q * shard_width;
+    int64_t j;
+#pragma omp parallel for schedule(static)
+    for (j = 0; j < shard_width; ++j) {
+      const uint8_t *w = weight + j * H;
+      double acc = 0.0;
+      for (int64_t k = 0; k < H; ++k) acc += e4m3_value(h[k]) * e4m3_value(w[k]);
+      out[j] = scale * acc;
+    }
+  }
+}

@@ -5,7 +5,8 @@ Each case below plants one mistake in a temporary copy of oracle/sga_oracle.c
 local instead of a global id, a transposed stats layout, acceptance that keeps
 counting after a mismatch, a missing bonus-row offset, a wrong count, a dropped
 dot-product term, a wrong bf16 widening, a runner-up equal to the winner, the
-bonus taken from the wrong row), builds it with gcc, points the oracle wrapper
+bonus taken from the wrong row, a wrong E4M3 exponent bias, the fp8 scales
+dropped), builds it with gcc, points the oracle wrapper
 at it, and runs the pin tests of tests/test_oracle_pins.py: at least one pin
 must fail for every mutant.  The committed oracle source is never modified.
 """
@@ -38,6 +39,9 @@ MUTANTS = {
     "bf16_widen_shift": ("u = ((uint32_t)b) << 16;", "u = ((uint32_t)b) << 15;"),
     "top2_includes_winner": ("if (j != best_j && c > second) second = c;",
                              "if (c > second) second = c;"),
+    "e4m3_bias_off_by_one": ("v = ldexp(1.0 + (double)m / 8.0, e - 7);",
+                             "v = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+    "fp8_scale_dropped": ("out[j] = scale * acc;", "out[j] = acc;"),
 }
 
 PIN_CALLS = [
@@ -55,6 +59,8 @@ PIN_CALLS = [
     pins.test_verify_reduces_stats_across_shards_first,
     pins.test_lmhead_logits_match_numpy_fp64_matmul,
     pins.test_lmhead_one_hot_weight_is_exact_column_pick,
+    pins.test_e4m3_decode_matches_torch_float8_for_every_code,
+    pins.test_lmhead_fp8_logits_match_numpy_with_scales,
 ]
 
 

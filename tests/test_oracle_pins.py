@@ -285,3 +285,35 @@ def test_lmhead_one_hot_weight_is_exact_column_pick():
         j = int(np.flatnonzero(row == row.max())[0])
         assert ids[r] == 100 + j and top1[r] == row.max()
         assert top2[r] == np.sort(np.delete(row, j))[-1]
+
+
+def test_e4m3_decode_matches_torch_float8_for_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    got = np.array([oracle.e4m3_value(c) for c in codes])
+    both_nan = np.isnan(ref) & np.isnan(got)
+    assert (both_nan | (got == ref)).all()
+    assert np.isnan(got).sum() == 2                          # 0x7F and 0xFF
+    assert (np.signbit(got[128:]) | np.isnan(got[128:])).all()  # -0 included
+
+
+def test_lmhead_fp8_logits_match_numpy_with_scales():
+    rng = np.random.default_rng(3)
+    hq = rng.integers(0, 256, (5, 128), dtype=np.uint8)
+    hq[hq & 0x7F == 0x7F] = 0x3C                       # no NaN codes
+    wq = rng.integers(0, 256, (37, 128), dtype=np.uint8)
+    wq[wq & 0x7F == 0x7F] = 0x41
+    hs = rng.uniform(0.01, 2.0, 5).astype(np.float32)
+    ws = 0.0037
+    rows = np.array([4, 0, 2], np.int64)
+    got = oracle.lmhead_logits_fp8(hq, hs, wq, ws, rows)
+    dec = lambda a: torch.from_numpy(a).view(torch.float8_e4m3fn).double().numpy()
+    ref = (dec(hq[rows]) @ dec(wq).T) * hs[rows, None].astype(np.float64) * ws
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-300)
+
+
+def test_e4m3_quantizer_of_the_generators_matches_torch():
+    x = np.random.default_rng(4).standard_normal(50000).astype(np.float32) * 60
+    x = np.clip(x, -448, 448)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert (wl.f32_to_e4m3(x) == ref).all()

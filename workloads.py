@@ -225,3 +225,73 @@ def random_shards(seed, vocab, num_shards):
     cuts = np.sort(rng.choice(np.arange(1, vocab), num_shards - 1, replace=False))
     edges = [0] + [int(c) for c in cuts] + [vocab]
     return [(edges[i], edges[i + 1] - edges[i]) for i in range(num_shards)]
+
+
+# --------------------------------------------------------------------------
+# FP8 (OCP E4M3, "e4m3fn") inputs for the fp8 LM head: values are scaled so
+# that the largest magnitude maps to 448 (the largest finite E4M3 value) and
+# rounded to the nearest code, ties to the even code.
+# --------------------------------------------------------------------------
+
+def _e4m3_positive_table():
+    codes = np.arange(0x7F, dtype=np.uint8)          # +0 .. 448, NaN (0x7F) excluded
+    e = ((codes >> 3) & 0xF).astype(np.int32)
+    m = (codes & 0x7).astype(np.float64)
+    v = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    return codes, v
+
+
+def f32_to_e4m3(x):
+    """Round finite values with |x| <= 448 to E4M3 codes (nearest, ties to even)."""
+    codes, v = _e4m3_positive_table()
+    a = np.abs(np.asarray(x, np.float64))
+    i = np.clip(np.searchsorted(v, a), 1, len(v) - 1)
+    lo, hi = v[i - 1], v[i]
+    pick_hi = (a - lo > hi - a) | ((a - lo == hi - a) & (codes[i] % 2 == 0))
+    c = np.where(pick_hi, codes[i], codes[i - 1]).astype(np.uint8)
+    c = np.where(a == 0, np.uint8(0), c)
+    return (c | (np.signbit(x).astype(np.uint8) << 7)).astype(np.uint8)
+
+
+def quantize_rows_e4m3(x, threads=None, chunk_rows=1024):
+    """Per-row scale s_r = max|x_r| / 448 and codes of x_r / s_r."""
+    out = np.empty(x.shape, np.uint8)
+    scale = np.empty(x.shape[0], np.float32)
+
+    def work(c):
+        r0, r1 = c * chunk_rows, min(x.shape[0], (c + 1) * chunk_rows)
+        m = np.abs(x[r0:r1]).max(axis=1).astype(np.float32)
+        s = np.where(m > 0, m / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+        scale[r0:r1] = s
+        out[r0:r1] = f32_to_e4m3(x[r0:r1] / s[:, None])
+
+    n = (x.shape[0] + chunk_rows - 1) // chunk_rows
+    with ThreadPoolExecutor(threads or min(16, os.cpu_count() or 1)) as ex:
+        list(ex.map(work, range(n)))
+    return out, scale
+
+
+def quantize_tensor_e4m3(x, threads=None, chunk_rows=1024):
+    """One scale s = max|x| / 448 for the whole tensor, and codes of x / s."""
+    s = np.float32(np.abs(x).max() / 448.0) or np.float32(1.0)
+    out = np.empty(x.shape, np.uint8)
+
+    def work(c):
+        r0, r1 = c * chunk_rows, min(x.shape[0], (c + 1) * chunk_rows)
+        out[r0:r1] = f32_to_e4m3(x[r0:r1] / s)
+
+    n = (x.shape[0] + chunk_rows - 1) // chunk_rows
+    with ThreadPoolExecutor(threads or min(16, os.cpu_count() or 1)) as ex:
+        list(ex.map(work, range(n)))
+    return out, s
+
+
+def fused_lmhead_fp8(m=512, h=4096, vocab=151936, num_shards=2):
+    """The fused LM-head shapes with E4M3 operands: hidden N(0,1) quantized
+    per row, weight N(0, 0.02) quantized per tensor."""
+    hq, hs = quantize_rows_e4m3(normal_matrix(5, m, h, 1.0, dtype="f32"))
+    wq, ws = quantize_tensor_e4m3(normal_matrix(50005, vocab, h, 0.02, dtype="f32", chunk_rows=1024))
+    return dict(name=f"fused LM-head + argmax, fp8 e4m3: {m} x {h} . [{vocab} x {h}]^T, "
+                     f"{num_shards} shards",
+                hidden=hq, hidden_scale=hs, weight=wq, weight_scale=float(ws),
+                shards=even_shards(vocab, num_shards), org_vocab=vocab)
