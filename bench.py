@@ -45,8 +45,9 @@ def parse_args():
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["large_verify", "lmhead", "draft_top_tokens",
-                                          "greedy_verify"], default="large_verify")
+    p.add_argument("--workload", choices=["large_verify", "lmhead", "lmhead_fp8",
+                                          "draft_top_tokens", "greedy_verify"],
+                   default="large_verify")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
@@ -494,11 +495,16 @@ def run_ours_verify(args):
 
 
 LMHEAD_METRIC = "fused LM-head + argmax rows/s and TFLOP/s (frac of bf16 tensor peak)"
+LMHEAD_METRIC_FP8 = "fused fp8 LM-head + argmax rows/s and TFLOP/s (frac of fp8 tensor peak)"
 
 
-def run_ours_lmhead(args):
+FP8_TO_BF16_NOMINAL = 4.5 / 2.25   # dense tensor peaks, PFLOP/s per GPU
+
+
+def run_ours_lmhead(args, fp8=False):
     """Fused LM-head + argmax: 512 rows, hidden 4096, vocab 151936 in 2 shards;
-    one step = sga_lmhead_argmax per shard + sga_shard_reduce."""
+    one step = sga_lmhead_argmax (or its fp8 variant) per shard +
+    sga_shard_reduce."""
     import torch
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
@@ -509,9 +515,15 @@ def run_ours_lmhead(args):
     barrier(world)
     import greedy_spec_decode_gb300 as sga
 
-    c = wl.fused_lmhead(m=args.lmhead_rows, vocab=args.lmhead_vocab)
-    hidden = torch.from_numpy(c["hidden"].view(np.int16)).view(torch.bfloat16).cuda()
-    weight = torch.from_numpy(c["weight"].view(np.int16)).view(torch.bfloat16).cuda()
+    if fp8:
+        c = wl.fused_lmhead_fp8(m=args.lmhead_rows, vocab=args.lmhead_vocab)
+        hidden = torch.from_numpy(c["hidden"]).cuda()
+        weight = torch.from_numpy(c["weight"]).cuda()
+        hscale = torch.from_numpy(c["hidden_scale"]).cuda()
+    else:
+        c = wl.fused_lmhead(m=args.lmhead_rows, vocab=args.lmhead_vocab)
+        hidden = torch.from_numpy(c["hidden"].view(np.int16)).view(torch.bfloat16).cuda()
+        weight = torch.from_numpy(c["weight"].view(np.int16)).view(torch.bfloat16).cuda()
     M, H = hidden.shape
     shards = c["shards"]
     S = len(shards)
@@ -525,8 +537,12 @@ def run_ours_lmhead(args):
         for s, (o, w) in enumerate(shards):
             if ev is not None:
                 ev[2 * s].record()
-            sga.sga_lmhead_argmax(hidden, w_views[s], o, c["org_vocab"],
-                                  stats[s * M:(s + 1) * M], ws)
+            if fp8:
+                sga.sga_lmhead_argmax_fp8(hidden, hscale, w_views[s], c["weight_scale"], o,
+                                          c["org_vocab"], stats[s * M:(s + 1) * M], ws)
+            else:
+                sga.sga_lmhead_argmax(hidden, w_views[s], o, c["org_vocab"],
+                                      stats[s * M:(s + 1) * M], ws)
             if ev is not None:
                 ev[2 * s + 1].record()
         sga.sga_shard_reduce(stats, S, M, ids)
@@ -552,17 +568,26 @@ def run_ours_lmhead(args):
     flops = 2.0 * M * H * sum(w for _, w in shards)
     pk, pk_src = peaks()
     peak = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops", FALLBACK_BF16_TFLOPS)))
+    burst = float(pk.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    if fp8:
+        peak *= FP8_TO_BF16_NOMINAL
+        burst *= FP8_TO_BF16_NOMINAL
     achieved = flops / (kern_ms * 1e-3) / 1e12
     assert sga.sga_device_error() == 0, "device error word set during the bench"
 
     # end to end: hidden states in from pinned host memory, ids back
-    hid_h = torch.from_numpy(c["hidden"].view(np.int16)).pin_memory()
+    hid_h = (torch.from_numpy(c["hidden"]) if fp8 else
+             torch.from_numpy(c["hidden"].view(np.int16))).pin_memory()
     ids_h = torch.empty(M, dtype=torch.int32).pin_memory()
-    hid_i16 = hidden.view(torch.int16)
+    hid_i16 = hidden if fp8 else hidden.view(torch.int16)
+    scale_h = torch.from_numpy(c["hidden_scale"]).pin_memory() if fp8 else None
+    h2d_bytes = hid_h.numel() * hid_h.element_size() + (scale_h.numel() * 4 if fp8 else 0)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(args.e2e_steps):
         hid_i16.copy_(hid_h, non_blocking=True)
+        if fp8:
+            hscale.copy_(scale_h, non_blocking=True)
         step()
         ids_h.copy_(ids, non_blocking=True)
     e1.record()
@@ -570,7 +595,8 @@ def run_ours_lmhead(args):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world, "cuda")
 
     line = {
-        "metric": LMHEAD_METRIC, "value": world * M / (step_ms * 1e-3), "unit": "rows/s",
+        "metric": LMHEAD_METRIC_FP8 if fp8 else LMHEAD_METRIC,
+        "value": world * M / (step_ms * 1e-3), "unit": "rows/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
@@ -578,22 +604,24 @@ def run_ours_lmhead(args):
                    "l2": "weight (1.24 GB) larger than L2 (129 MB); no flush",
                    "parallelism": f"{world} independent replica(s), emulated TP{S} per GPU"},
         "tflops_step": flops / (step_ms * 1e-3) / 1e12,
-        "weight_gbs": weight.numel() * 2 / (kern_ms * 1e-3) / 1e9,
+        "weight_gbs": weight.numel() * weight.element_size() / (kern_ms * 1e-3) / 1e9,
         "kernel_us": {"lmhead_argmax_per_step": round(kern_ms * 1e3, 2),
                       "reduce_and_gaps": round((step_ms - kern_ms) * 1e3, 2)},
-        "roofline": {"bound": "tensor", "kernel": "lmhead_argmax_kernel",
+        "roofline": {"bound": "tensor",
+                     "kernel": "lmhead_argmax_2sm_kernel<fp8>" if fp8 else "lmhead_argmax_2sm_kernel",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
-                     "traffic": ncu_traffic("lmhead_fused.md",
-                                            ["greedy_spec_decode_gb300/csrc/lmhead.cu",
+                     "traffic": None if fp8 else ncu_traffic(
+                         "lmhead_fused.md", ["greedy_spec_decode_gb300/csrc/lmhead.cu",
                                              "greedy_spec_decode_gb300/csrc/common.cuh"]),
                      "traffic_unit": "DRAM bytes per launch of the GEMM kernel",
-                     "peak_source": (f"{pk_src} bf16_tflops_sustained (cuBLAS bf16, timed in a "
-                                     f"long loop)") if pk_src == "measured" else "fallback",
-                     "frac_of_burst": achieved / float(pk.get("bf16_tflops", FALLBACK_BF16_TFLOPS)),
+                     "peak_source": ((f"{pk_src} bf16_tflops_sustained (cuBLAS bf16, timed in a "
+                                      f"long loop)") if pk_src == "measured" else "fallback")
+                                    + (" x 2 (nominal fp8 / bf16 dense ratio)" if fp8 else ""),
+                     "frac_of_burst": achieved / burst,
                      "flops_per_step": flops},
         "e2e": {"value": world * M / (e2e_ms * 1e-3), "unit": "rows/s",
-                "h2d_bytes_per_step": hid_h.numel() * 2, "d2h_bytes_per_step": M * 4,
+                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": M * 4,
                 "ms_per_step": e2e_ms},
         "gpu_launches": args.steps * (2 * S + 1),
         "clocks": clocks,
@@ -705,6 +733,8 @@ def main():
                              else wl.large_verify)
     if args.workload == "lmhead":
         return run_ours_lmhead(args)
+    if args.workload == "lmhead_fp8":
+        return run_ours_lmhead(args, fp8=True)
     if args.workload == "draft_top_tokens":
         return run_ours_small(args, wl.draft_top_tokens)
     if args.workload == "greedy_verify":

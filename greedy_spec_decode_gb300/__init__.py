@@ -57,6 +57,8 @@ def lib():
             "sga_greedy_verify": ([vp, i32, i32, vp, vp, i32, vp, vp, vp, vp, vp, vp], i32),
             "sga_lmhead_argmax_workspace": ([i64, i64], sz),
             "sga_lmhead_argmax": ([vp, i64, i64, vp, i64, i64, i64, vp, vp, sz, vp], i32),
+            "sga_lmhead_argmax_fp8": ([vp, vp, i64, i64, vp, ctypes.c_float, i64, i64, i64, vp,
+                                       vp, sz, vp], i32),
             "sga_device_error": ([ctypes.POINTER(ctypes.c_uint32)], i32),
             "sga_clear_device_error": ([], i32),
             "sga_selftest_wait_timeout": ([ctypes.c_uint64, vp, vp], i32),
@@ -186,6 +188,27 @@ def sga_lmhead_argmax(hidden, weight_shard, shard_start, org_vocab, out_stats, w
     _check("sga_lmhead_argmax", lib().sga_lmhead_argmax(
         _ptr(hidden), M, H, _ptr(weight_shard), int(shard_start), width, int(org_vocab),
         _ptr(out_stats), _ptr(workspace), nbytes, _stream(stream)))
+    return out_stats
+
+
+def sga_lmhead_argmax_fp8(hidden_q, hidden_scale, weight_q, weight_scale, shard_start,
+                          org_vocab, out_stats, workspace, stream=None):
+    """Fused fp8 (E4M3) LM-head GEMM + per-shard argmax.  hidden_q: uint8 [M, H]
+    codes, hidden_scale: float32 [M] CUDA tensor or None, weight_q: uint8
+    [shard_width, H] codes, weight_scale: positive float (see include/sga.h)."""
+    if not (hidden_q.is_contiguous() and weight_q.is_contiguous()):
+        raise ValueError("hidden_q and weight_q must be contiguous")
+    if hidden_q.dtype != torch.uint8 or weight_q.dtype != torch.uint8:
+        raise TypeError("fp8 operands are passed as uint8 E4M3 codes")
+    M, H = hidden_q.shape
+    width = weight_q.size(0)
+    if weight_q.size(1) != H:
+        raise ValueError("hidden_q and weight_q must share H")
+    nbytes = workspace.numel() * workspace.element_size()
+    _check("sga_lmhead_argmax_fp8", lib().sga_lmhead_argmax_fp8(
+        _ptr(hidden_q), _ptr(hidden_scale), M, H, _ptr(weight_q), float(weight_scale),
+        int(shard_start), width, int(org_vocab), _ptr(out_stats), _ptr(workspace), nbytes,
+        _stream(stream)))
     return out_stats
 
 

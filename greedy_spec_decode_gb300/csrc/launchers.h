@@ -36,10 +36,14 @@ cudaError_t launch_greedy_verify(const sga_stat *stats, int num_shards, int num_
                                  int32_t *out_target_ids, uint32_t *err, cudaStream_t stream);
 
 size_t lmhead_workspace_bytes(int64_t M, int64_t width);
+// fp8 = false: bf16 hidden/weight (row_scale, w_scale unused).  fp8 = true:
+// E4M3 codes; the reported values are scaled by row_scale[r] (nullable: 1)
+// times w_scale.
 cudaError_t launch_lmhead_argmax(const void *hidden, int64_t M, int64_t H, const void *weight,
                                  int64_t shard_start, int64_t width, int64_t valid,
                                  sga_stat *out, void *workspace, int num_sms, uint32_t *err,
-                                 cudaStream_t stream);
+                                 cudaStream_t stream, bool fp8 = false,
+                                 const float *row_scale = nullptr, float w_scale = 1.0f);
 
 
 // Bounded-wait self-test (lmhead.cu).

@@ -37,7 +37,10 @@ namespace {
 
 constexpr int BM = 128;          // rows of hidden per tile (TMEM lanes)
 constexpr int BN = 256;          // vocab ids per tile (TMEM columns)
-constexpr int BK = 64;           // bf16 elements per 128-byte swizzled row
+constexpr int ROW_BYTES = 128;   // one 128-byte swizzled K-block row of a tile
+// K-block in elements: 64 bf16 or 128 fp8 (E4M3) per 128-byte row
+template <bool kFp8>
+constexpr int kBk = kFp8 ? 128 : 64;
 #ifndef SGA_LMHEAD_STAGES
 #define SGA_LMHEAD_STAGES 4
 #endif
@@ -48,8 +51,8 @@ constexpr int BK = 64;           // bf16 elements per 128-byte swizzled row
 #define SGA_LMHEAD_2SM_MIN_M 129
 #endif
 constexpr int STAGES = SGA_LMHEAD_STAGES;
-constexpr int A_BYTES = BM * BK * 2;   // 16 KB
-constexpr int B_BYTES = BN * BK * 2;   // 32 KB
+constexpr int A_BYTES = BM * ROW_BYTES;   // 16 KB
+constexpr int B_BYTES = BN * ROW_BYTES;   // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;           // 6 warps
 constexpr int TMEM_COLS = 2 * BN;      // double-buffered accumulator
@@ -139,22 +142,35 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
   return d;
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, bf16 A
-// and B, both K-major, N = BN, M = BM.
-constexpr uint32_t kInstrDesc = (1u << 4)            // D format: f32
-                                | (1u << 7)          // A format: bf16
-                                | (1u << 10)         // B format: bf16
-                                | ((BN >> 3) << 17)  // N >> 3
-                                | ((BM >> 4) << 24); // M >> 4
+// Instruction descriptor of tcgen05.mma: fp32 accumulator (bits 4-5 = 1),
+// A/B formats (bits 7-9, 10-12: bf16 = 1 for kind::f16, E4M3 = 0 for
+// kind::f8f6f4), both operands K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+template <bool kFp8>
+__host__ __device__ constexpr uint32_t instr_desc(uint32_t m, uint32_t n) {
+  return (1u << 4) | (kFp8 ? 0u : ((1u << 7) | (1u << 10))) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(kInstrDesc), "r"(accumulate)
-      : "memory");
+// One MMA of a K step (16 bf16 or 32 fp8 = 32 bytes of each row), M = BM,
+// N = BN, issued by one thread of this CTA.
+template <bool kFp8>
+__device__ __forceinline__ void mma_1sm(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t accumulate) {
+  constexpr uint32_t idesc = instr_desc<kFp8>(BM, BN);
+  if constexpr (kFp8) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
 }
 
 // Arrive once on `bar` when every tcgen05.mma issued so far has completed.
@@ -197,6 +213,7 @@ __device__ __forceinline__ void raise_abort(Shared *sh, uint32_t *err) {
   atomicOr(err, SGA_DEVERR_TIMEOUT);
 }
 
+template <bool kFp8>
 __global__ void __launch_bounds__(THREADS, 1)
     lmhead_argmax_kernel(const __grid_constant__ CUtensorMap tmap_a,
                          const __grid_constant__ CUtensorMap tmap_b, int M, int num_kb,
@@ -256,8 +273,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           const uint32_t full = smem_u32(&sh->full[prod_stage]);
           mbar_expect_tx(full, STAGE_BYTES);
-          tma_load_2d(smem_u32(a_tiles + prod_stage * A_BYTES), &tmap_a, kb * BK, m * BM, full);
-          tma_load_2d(smem_u32(b_tiles + prod_stage * B_BYTES), &tmap_b, kb * BK, n * BN, full);
+          tma_load_2d(smem_u32(a_tiles + prod_stage * A_BYTES), &tmap_a, kb * kBk<kFp8>, m * BM,
+                      full);
+          tma_load_2d(smem_u32(b_tiles + prod_stage * B_BYTES), &tmap_b, kb * kBk<kFp8>, n * BN,
+                      full);
           ++issued;
           if (++prod_stage == STAGES) {
             prod_stage = 0;
@@ -289,8 +308,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint64_t a_desc = smem_desc_sw128(smem_u32(a_tiles + stage * A_BYTES));
           const uint64_t b_desc = smem_desc_sw128(smem_u32(b_tiles + stage * B_BYTES));
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)  // 16 bf16 = 32 bytes = 2 descriptor units
-            mma_bf16(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, (kb | kk) != 0);
+          for (int kk = 0; kk < ROW_BYTES / 32; ++kk)  // 32 bytes = 2 descriptor units
+            mma_1sm<kFp8>(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, (kb | kk) != 0);
           mma_commit(smem_u32(&sh->empty[stage]));
           if (++stage == STAGES) {
             stage = 0;
@@ -404,12 +423,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 #define SGA_LMHEAD_STAGES2 6
 #endif
 constexpr int STAGES2 = SGA_LMHEAD_STAGES2;
-constexpr int A2_BYTES = 128 * BK * 2;  // 16 KB
-constexpr int B2_BYTES = 128 * BK * 2;  // 16 KB (half of the 256-id tile)
+constexpr int A2_BYTES = 128 * ROW_BYTES;  // 16 KB
+constexpr int B2_BYTES = 128 * ROW_BYTES;  // 16 KB (half of the 256-id tile)
 constexpr int STAGE2_BYTES = A2_BYTES + B2_BYTES;
 constexpr int SMEM2_BYTES = 1024 + STAGES2 * STAGE2_BYTES + 256;
-constexpr uint32_t kInstrDesc2 = (1u << 4) | (1u << 7) | (1u << 10) | ((256u >> 3) << 17) |
-                                 ((256u >> 4) << 24);  // M = 256 across the pair, N = 256
 
 struct Shared2 {
   uint64_t full[STAGES2];
@@ -450,14 +467,25 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
-__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                              uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(kInstrDesc2), "r"(accumulate)
-      : "memory");
+template <bool kFp8>
+__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t accumulate) {
+  constexpr uint32_t idesc = instr_desc<kFp8>(256, 256);  // M = 256 across the pair
+  if constexpr (kFp8) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
 }
 
 // Arrive once on `bar` in both CTAs of the pair when the MMAs issued so far
@@ -476,6 +504,7 @@ __device__ __forceinline__ void raise_abort2(Shared2 *sh, uint32_t *err) {
   atomicOr(err, SGA_DEVERR_TIMEOUT);
 }
 
+template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     lmhead_argmax_2sm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                              const __grid_constant__ CUtensorMap tmap_b, int M, int num_kb,
@@ -538,9 +567,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
         const uint32_t full_leader = map_to_rank(smem_u32(&sh->full[prod_stage]), 0);
         if (leader) mbar_expect_tx(smem_u32(&sh->full[prod_stage]), 2 * STAGE2_BYTES);
-        tma_load_2d_pair(smem_u32(a_tiles + prod_stage * A2_BYTES), &tmap_a, kb * BK,
+        tma_load_2d_pair(smem_u32(a_tiles + prod_stage * A2_BYTES), &tmap_a, kb * kBk<kFp8>,
                          mp * 256 + static_cast<int>(rank) * 128, full_leader);
-        tma_load_2d_pair(smem_u32(b_tiles + prod_stage * B2_BYTES), &tmap_b, kb * BK,
+        tma_load_2d_pair(smem_u32(b_tiles + prod_stage * B2_BYTES), &tmap_b, kb * kBk<kFp8>,
                          n * 256 + static_cast<int>(rank) * 128, full_leader);
         ++issued;
         if (++prod_stage == STAGES2) {
@@ -571,8 +600,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const uint64_t a_desc = smem_desc_sw128(smem_u32(a_tiles + stage * A2_BYTES));
         const uint64_t b_desc = smem_desc_sw128(smem_u32(b_tiles + stage * B2_BYTES));
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          mma_bf16_pair(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, (kb | kk) != 0);
+        for (int kk = 0; kk < ROW_BYTES / 32; ++kk)
+          mma_pair<kFp8>(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, (kb | kk) != 0);
         mma_commit_pair(smem_u32(&sh->empty[stage]));
         if (++stage == STAGES2) {
           stage = 0;
@@ -685,8 +714,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
 // One warp per row: lanes stride over the row's per-tile partials (contiguous,
 // row-major workspace) and merge them with the (value, id) order.
+// Values of the fp8 variant are raw accumulators of the E4M3 codes until
+// here; the positive row and weight scales (which cannot change the argmax of
+// a row) are applied to the winning value only.
 __global__ void lmhead_finalize_kernel(const sga_stat *__restrict__ ws, int M, int n_tiles,
-                                       int shard_start, sga_stat *__restrict__ out) {
+                                       int shard_start, sga_stat *__restrict__ out,
+                                       const float *__restrict__ row_scale, float w_scale,
+                                       int scaled) {
   pdl_wait();  // the partials of the GEMM kernel are complete and visible
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -704,7 +738,7 @@ __global__ void lmhead_finalize_kernel(const sga_stat *__restrict__ ws, int M, i
   warp_argmax(bv, bi);
   if (lane == 0) {
     sga_stat s;
-    s.v = bv;
+    s.v = scaled ? bv * ((row_scale ? row_scale[r] : 1.0f) * w_scale) : bv;
     s.id = bi == kNoId ? shard_start : bi;
     out[r] = s;
   }
@@ -740,18 +774,22 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor map over a row-major [rows, cols] matrix, box = box_rows x 64
-// columns (128 bytes, swizzled), zero fill outside.
-bool make_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, int box_rows) {
+// 2-D tensor map over a row-major [rows, cols] matrix of bf16 or fp8 (E4M3,
+// stored as bytes); box = box_rows x one 128-byte row (64 bf16 or 128 fp8
+// columns), 128-byte swizzle, zero fill outside.
+bool make_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, int box_rows,
+              bool fp8) {
   auto encode = get_encode_fn();
   if (encode == nullptr) return false;
+  const int elt = fp8 ? 1 : 2;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * elt)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(ROW_BYTES / elt), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
-  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides,
-                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Raise a kernel's dynamic shared-memory limit once per device (slot picks the
@@ -759,7 +797,7 @@ bool make_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, int
 // no function-attribute call.
 cudaError_t set_smem_once(const void *kernel, int bytes, int slot) {
   static std::mutex mu;
-  static bool done[2][64] = {};
+  static bool done[4][64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -774,7 +812,8 @@ cudaError_t set_smem_once(const void *kernel, int bytes, int slot) {
 }
 
 // Number of 2-CTA clusters of the 2-SM kernel that fit on the current device
-// at once (queried once per device).
+// at once (queried once per device and operand type).
+template <bool kFp8>
 int resident_pairs(int num_sms) {
   static std::mutex mu;
   static int cache[64] = {};
@@ -787,13 +826,53 @@ int resident_pairs(int num_sms) {
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = SMEM2_BYTES;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, lmhead_argmax_2sm_kernel, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, lmhead_argmax_2sm_kernel<kFp8>, &cfg) != cudaSuccess) {
       cudaGetLastError();
       n = 0;
     }
     cache[dev] = n > num_sms / 2 ? num_sms / 2 : n;
   }
   return cache[dev];
+}
+
+template <bool kFp8>
+cudaError_t launch_gemm(const void *hidden, int64_t M, int64_t H, const void *weight,
+                        int64_t shard_start, int64_t valid, sga_stat *ws, int n_tiles, int num_sms,
+                        uint32_t *err, cudaStream_t stream) {
+  const int num_kb = static_cast<int>(H / kBk<kFp8>);
+  if (SGA_LMHEAD_2SM && M >= SGA_LMHEAD_2SM_MIN_M && num_sms >= 2) {
+    // 2-SM tiles (256 rows per CTA pair)
+    CUtensorMap map_a, map_b;
+    if (!make_map(&map_a, hidden, M, H, 128, kFp8) || !make_map(&map_b, weight, valid, H, 128, kFp8))
+      return cudaErrorInvalidValue;
+    cudaError_t e = set_smem_once(reinterpret_cast<const void *>(lmhead_argmax_2sm_kernel<kFp8>),
+                                  SMEM2_BYTES, kFp8 ? 2 : 0);
+    if (e != cudaSuccess) return e;
+    const int m_pairs = static_cast<int>((M + 255) / 256);
+    const int total = m_pairs * n_tiles;
+    // A persistent grid must be fully resident: a cluster needs both CTAs in
+    // one GPC, so fewer than num_sms / 2 pairs may fit at once.
+    const int resident = resident_pairs<kFp8>(num_sms);
+    if (resident <= 0) return cudaErrorLaunchOutOfResources;
+    const int pairs = total < resident ? total : resident;
+    lmhead_argmax_2sm_kernel<kFp8><<<2 * pairs, THREADS, SMEM2_BYTES, stream>>>(
+        map_a, map_b, static_cast<int>(M), num_kb, m_pairs, n_tiles, static_cast<int>(valid),
+        static_cast<int>(shard_start), ws, err);
+    return cudaGetLastError();
+  }
+  CUtensorMap map_a, map_b;
+  if (!make_map(&map_a, hidden, M, H, BM, kFp8) || !make_map(&map_b, weight, valid, H, BN, kFp8))
+    return cudaErrorInvalidValue;
+  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(lmhead_argmax_kernel<kFp8>),
+                                SMEM_BYTES, kFp8 ? 3 : 1);
+  if (e != cudaSuccess) return e;
+  const int m_tiles = static_cast<int>((M + BM - 1) / BM);
+  const int total = m_tiles * n_tiles;
+  const int grid = total < num_sms ? total : num_sms;
+  lmhead_argmax_kernel<kFp8><<<grid, THREADS, SMEM_BYTES, stream>>>(
+      map_a, map_b, static_cast<int>(M), num_kb, m_tiles, n_tiles, static_cast<int>(valid),
+      static_cast<int>(shard_start), ws, err);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -812,44 +891,17 @@ size_t lmhead_workspace_bytes(int64_t M, int64_t width) {
 cudaError_t launch_lmhead_argmax(const void *hidden, int64_t M, int64_t H, const void *weight,
                                  int64_t shard_start, int64_t width, int64_t valid,
                                  sga_stat *out, void *workspace, int num_sms, uint32_t *err,
-                                 cudaStream_t stream) {
+                                 cudaStream_t stream, bool fp8, const float *row_scale,
+                                 float w_scale) {
   (void)width;
   sga_stat *ws = static_cast<sga_stat *>(workspace);
-  const int m_tiles = static_cast<int>((M + BM - 1) / BM);
   const int n_tiles = static_cast<int>((valid + BN - 1) / BN);
-  if (n_tiles > 0 && SGA_LMHEAD_2SM && M >= SGA_LMHEAD_2SM_MIN_M && num_sms >= 2) {
-    // 2-SM tiles (256 rows per CTA pair)
-    CUtensorMap map_a, map_b;
-    if (!make_map(&map_a, hidden, M, H, 128) || !make_map(&map_b, weight, valid, H, 128))
-      return cudaErrorInvalidValue;
-    cudaError_t e = set_smem_once(reinterpret_cast<const void *>(lmhead_argmax_2sm_kernel),
-                                  SMEM2_BYTES, 0);
-    if (e != cudaSuccess) return e;
-    const int m_pairs = static_cast<int>((M + 255) / 256);
-    const int total = m_pairs * n_tiles;
-    // A persistent grid must be fully resident: a cluster needs both CTAs in
-    // one GPC, so fewer than num_sms / 2 pairs may fit at once.
-    const int resident = resident_pairs(num_sms);
-    if (resident <= 0) return cudaErrorLaunchOutOfResources;
-    const int pairs = total < resident ? total : resident;
-    lmhead_argmax_2sm_kernel<<<2 * pairs, THREADS, SMEM2_BYTES, stream>>>(
-        map_a, map_b, static_cast<int>(M), static_cast<int>(H / BK), m_pairs, n_tiles,
-        static_cast<int>(valid), static_cast<int>(shard_start), ws, err);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  } else if (n_tiles > 0) {
-    CUtensorMap map_a, map_b;
-    if (!make_map(&map_a, hidden, M, H, BM) || !make_map(&map_b, weight, valid, H, BN))
-      return cudaErrorInvalidValue;
-    cudaError_t e = set_smem_once(reinterpret_cast<const void *>(lmhead_argmax_kernel),
-                                  SMEM_BYTES, 1);
-    if (e != cudaSuccess) return e;
-    const int total = m_tiles * n_tiles;
-    const int grid = total < num_sms ? total : num_sms;
-    lmhead_argmax_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(
-        map_a, map_b, static_cast<int>(M), static_cast<int>(H / BK), m_tiles, n_tiles,
-        static_cast<int>(valid), static_cast<int>(shard_start), ws, err);
-    e = cudaGetLastError();
+  if (n_tiles > 0) {
+    const cudaError_t e =
+        fp8 ? launch_gemm<true>(hidden, M, H, weight, shard_start, valid, ws, n_tiles, num_sms,
+                                err, stream)
+            : launch_gemm<false>(hidden, M, H, weight, shard_start, valid, ws, n_tiles, num_sms,
+                                 err, stream);
     if (e != cudaSuccess) return e;
   }
   // 8 rows per block; programmatic dependent launch lets the blocks become
@@ -864,7 +916,8 @@ cudaError_t launch_lmhead_argmax(const void *hidden, int64_t M, int64_t H, const
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, lmhead_finalize_kernel, static_cast<const sga_stat *>(ws),
-                            static_cast<int>(M), n_tiles, static_cast<int>(shard_start), out);
+                            static_cast<int>(M), n_tiles, static_cast<int>(shard_start), out,
+                            row_scale, w_scale, fp8 ? 1 : 0);
 }
 
 }  // namespace sga

@@ -221,6 +221,32 @@ int sga_lmhead_argmax(const void *hidden, int64_t M, int64_t H, const void *weig
   return launch_status(e);
 }
 
+int sga_lmhead_argmax_fp8(const void *hidden_q, const float *hidden_scale, int64_t M, int64_t H,
+                          const void *weight_q, float weight_scale, int64_t shard_start,
+                          int64_t shard_width, int64_t org_vocab, sga_stat *out_stats,
+                          void *workspace, size_t workspace_bytes, sga_stream stream) {
+  if (M < 0 || M > (int64_t(1) << 20)) return SGA_ERR_SIZE;
+  if (H <= 0 || H % 128 != 0 || H > (int64_t(1) << 20)) return SGA_ERR_SIZE;
+  if (!(weight_scale > 0.0f) || !(weight_scale < 3.4e38f)) return SGA_ERR_SIZE;
+  int st = check_shard(shard_start, shard_width, org_vocab);
+  if (st != SGA_OK) return st;
+  if (M == 0) return SGA_OK;
+  if (hidden_q == nullptr || weight_q == nullptr || out_stats == nullptr || workspace == nullptr)
+    return SGA_ERR_NULL;
+  if (misaligned(hidden_q, 16) || misaligned(weight_q, 16) || misaligned(out_stats, 8) ||
+      misaligned(workspace, 8) || misaligned(hidden_scale, 4))
+    return SGA_ERR_ALIGN;
+  if (workspace_bytes < sga::lmhead_workspace_bytes(M, shard_width)) return SGA_ERR_WORKSPACE;
+  DeviceInfo d;
+  if ((st = current_device(&d)) != SGA_OK) return st;
+  const cudaError_t e = sga::launch_lmhead_argmax(
+      hidden_q, M, H, weight_q, shard_start, shard_width,
+      valid_ids(shard_start, shard_width, org_vocab), out_stats, workspace, d.num_sms, d.err,
+      static_cast<cudaStream_t>(stream), true, hidden_scale, weight_scale);
+  if (e == cudaErrorNotSupported) return SGA_ERR_UNSUPPORTED;
+  return launch_status(e);
+}
+
 // Same work as sga_lmhead_argmax, with the library's fixed scratch array in
 // place of a caller workspace, for callers that cannot allocate device memory.
 int sga_lmhead_argmax_noalloc(const void *hidden, int64_t M, int64_t H,

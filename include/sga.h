@@ -241,6 +241,32 @@ int sga_lmhead_argmax(const void *hidden, int64_t M, int64_t H, const void *weig
                       sga_stream stream);
 
 /*
+ * sga_lmhead_argmax_fp8 -- sga_lmhead_argmax with FP8 (OCP E4M3, "e4m3fn")
+ * operands: hidden states and the weight shard stored as E4M3 codes (one byte
+ * each) with a positive scale per hidden row and one positive weight scale.
+ * logit[r][j] = hidden_scale[r] * weight_scale * sum_k h[r][k] * w[j][k].
+ * Positive scales cannot change which id is the argmax of a row, so the
+ * tensor cores (tcgen05 kind::f8f6f4, fp32 accumulation) work on the raw
+ * codes and only the reported value is scaled.
+ * Page: as sga_lmhead_argmax (vLLM PR #62604, Purpose; PR #39419, Changes);
+ * FP8 models are the pages' workloads (vLLM PR #34049, Test Plan:
+ * Llama 4 Maverick FP8), an fp8 LM head is this library's extension.
+ *
+ *   hidden_q      device uint8 [M, H] E4M3 codes, 16-byte aligned.
+ *   hidden_scale  device fp32 [M] (nullable: all 1), 4-byte aligned; each
+ *                 scale must be positive and finite (not checked).
+ *   H             a positive multiple of 128.
+ *   weight_q      device uint8 [shard_width, H] E4M3 codes, 16-byte aligned.
+ *   weight_scale  host value, positive and finite (SGA_ERR_SIZE otherwise).
+ *   workspace     as sga_lmhead_argmax (same size function).
+ * The reported value is fp32(acc) * (hidden_scale[r] * weight_scale).
+ */
+int sga_lmhead_argmax_fp8(const void *hidden_q, const float *hidden_scale, int64_t M, int64_t H,
+                          const void *weight_q, float weight_scale, int64_t shard_start,
+                          int64_t shard_width, int64_t org_vocab, sga_stat *out_stats,
+                          void *workspace, size_t workspace_bytes, sga_stream stream);
+
+/*
  * sga_lmhead_argmax_noalloc -- sga_lmhead_argmax for callers that must not
  * allocate device memory.  The pages have no counterpart to this entry point.
  *

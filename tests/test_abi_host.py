@@ -120,3 +120,14 @@ def test_local_argmax_shards_validation(sga_lib):
     assert f(FAKE, 1, 4, 100, 0, None, None, 100, FAKE, None) == -2
     assert f(FAKE, 1, 4, 100, 65, None, None, 100, FAKE, None) == -2
     assert f(FAKE, 1, 4, 100, 2, None, None, 100, FAKE, None) == -1
+
+
+def test_fp8_validation(sga_lib):
+    f = sga_lib.lib().sga_lmhead_argmax_fp8
+    fake = FAKE
+    ws = 1 << 20
+    assert f(fake, None, 4, 192, fake, 1.0, 0, 64, 64, fake, fake, ws, None) == -2   # H % 128
+    assert f(fake, None, 4, 128, fake, 0.0, 0, 64, 64, fake, fake, ws, None) == -2   # scale
+    assert f(fake, None, 4, 128, fake, -1.0, 0, 64, 64, fake, fake, ws, None) == -2
+    assert f(fake, ctypes.c_void_p(0x10002), 4, 128, fake, 1.0, 0, 64, 64, fake, fake, ws,
+             None) == -6
