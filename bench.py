@@ -611,9 +611,10 @@ def run_ours_lmhead(args, fp8=False):
                      "kernel": "lmhead_argmax_2sm_kernel<fp8>" if fp8 else "lmhead_argmax_2sm_kernel",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
-                     "traffic": None if fp8 else ncu_traffic(
-                         "lmhead_fused.md", ["greedy_spec_decode_gb300/csrc/lmhead.cu",
-                                             "greedy_spec_decode_gb300/csrc/common.cuh"]),
+                     "traffic": ncu_traffic(
+                         "lmhead_fused_fp8.md" if fp8 else "lmhead_fused.md",
+                         ["greedy_spec_decode_gb300/csrc/lmhead.cu",
+                          "greedy_spec_decode_gb300/csrc/common.cuh"]),
                      "traffic_unit": "DRAM bytes per launch of the GEMM kernel",
                      "peak_source": ((f"{pk_src} bf16_tflops_sustained (cuBLAS bf16, timed in a "
                                       f"long loop)") if pk_src == "measured" else "fallback")

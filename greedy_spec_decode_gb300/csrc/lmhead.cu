@@ -728,12 +728,25 @@ __global__ void lmhead_finalize_kernel(const sga_stat *__restrict__ ws, int M, i
   float bv = __int_as_float(0xff800000);
   int32_t bi = kNoId;
   const sga_stat *row = ws + static_cast<size_t>(r) * n_tiles;
-  for (int n = lane; n < n_tiles; n += 32) {
-    const sga_stat c = row[n];
-    if (pair_beats(c.v, c.id, bv, bi)) {
-      bv = c.v;
-      bi = c.id;
+  constexpr int kInFlight = 4;  // loads issued before the first compare
+  for (int n0 = lane; n0 < n_tiles; n0 += 32 * kInFlight) {
+    sga_stat c[kInFlight];
+#pragma unroll
+    for (int u = 0; u < kInFlight; ++u) {
+      const int n = n0 + 32 * u;
+      if (n < n_tiles) {
+        c[u] = row[n];
+      } else {
+        c[u].v = __int_as_float(0xff800000);
+        c[u].id = kNoId;
+      }
     }
+#pragma unroll
+    for (int u = 0; u < kInFlight; ++u)
+      if (pair_beats(c[u].v, c[u].id, bv, bi)) {
+        bv = c[u].v;
+        bi = c[u].id;
+      }
   }
   warp_argmax(bv, bi);
   if (lane == 0) {
