@@ -24,8 +24,9 @@ marshals numpy arrays into it.  Sources, by page title and section:
 Pins (``tests/test_oracle_pins.py``, CPU only): an independent set-based brute
 force, ``torch.argmax`` as a third opinion on unpadded rows, planted ties /
 NaNs / -inf rows with known answers (``tests/golden/``), hand-computed
-acceptance cases, shard-count invariance, and for the LM-head logits a numpy
-fp64 matmul and exact one-hot weights.
+acceptance cases, shard-count invariance, a grouped brute force of the
+block-granular statistics, and for the LM-head logits a numpy fp64 matmul and
+exact one-hot weights.
 """
 import ctypes
 
@@ -52,6 +53,8 @@ def configure(L):
         "oracle_argmax_f64": ([vp, i64, i64, i64, i64, vp, vp, vp], None),
         "oracle_e4m3_value": ([ctypes.c_uint8], ctypes.c_double),
         "oracle_lmhead_logits_fp8": ([vp, vp, i64, vp, ctypes.c_double, i64, vp, i64, vp], None),
+        "oracle_block_count": ([i64, i64, i64], i64),
+        "oracle_block_stats": ([vp, cint, i64, i64, i64, i64, i64, i64, i64, cint, vp, vp], i64),
         "oracle_num_threads": ([], cint),
         "oracle_set_num_threads": ([cint], None),
     }
@@ -129,6 +132,46 @@ def gathered_stats(x, shards, org_vocab):
     if x.shape[0] == 0:
         return np.zeros(0, STAT)
     return np.concatenate([shard_argmax(x, o, w, org_vocab) for o, w in shards])
+
+
+def block_count(shard_start, shard_width, block):
+    """Number of fixed global blocks of `block` ids that meet the shard."""
+    return int(lib().oracle_block_count(int(shard_start), int(shard_width), int(block)))
+
+
+def block_stats(x, shard_start, shard_width, org_vocab, draft_block, bonus_block=None,
+                cu_num_draft=None):
+    """Block-granular stats of one shard: [n_pieces * rows] entries, piece-major.
+    Draft rows use draft_block, the bonus row of each request (given by
+    cu_num_draft; None = every row is a draft row) uses bonus_block."""
+    ld = _row_stride(x)
+    rows = x.shape[0]
+    if shard_start < 0 or shard_width <= 0 or shard_start + shard_width > x.shape[1]:
+        raise ValueError("shard outside the row")
+    bonus_block = draft_block if bonus_block is None else bonus_block
+    n = block_count(shard_start, shard_width, min(draft_block, bonus_block))
+    out = np.zeros(n * rows, STAT)
+    cu = None if cu_num_draft is None else np.ascontiguousarray(cu_num_draft, np.int32)
+    if rows:
+        base = x[:, shard_start:]
+        got = lib().oracle_block_stats(
+            ctypes.c_void_p(base.ctypes.data), _dtype_code(x), rows, ld, shard_start,
+            shard_width, int(org_vocab), int(draft_block), int(bonus_block),
+            0 if cu is None else cu.shape[0] - 1, None if cu is None else _ptr(cu), _ptr(out))
+        if got != n:
+            raise ValueError(f"oracle_block_stats status {got}")
+    return out
+
+
+def gathered_block_stats(x, shards, org_vocab, draft_block, bonus_block=None, cu_num_draft=None):
+    """Block stats of every shard concatenated in shard order; returns
+    (stats, total pieces per row), ready for shard_reduce / greedy_verify
+    with num_shards = total pieces."""
+    parts = [block_stats(x, o, w, org_vocab, draft_block, bonus_block, cu_num_draft)
+             for o, w in shards]
+    rows = x.shape[0]
+    total = sum(p.shape[0] for p in parts) // rows if rows else 0
+    return (np.concatenate(parts) if rows else np.zeros(0, STAT)), total
 
 
 def shard_reduce(stats, num_shards, rows):

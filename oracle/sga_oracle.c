@@ -335,3 +335,70 @@ void oracle_lmhead_logits_fp8(const uint8_t *hidden, const float *hidden_scale, 
     }
   }
 }
+
+/* Number of fixed global blocks [b * block, (b + 1) * block) that meet the
+ * shard [shard_start, shard_start + shard_width). */
+int64_t oracle_block_count(int64_t shard_start, int64_t shard_width, int64_t block) {
+  return (shard_start + shard_width - 1) / block - shard_start / block + 1;
+}
+
+/* Block-granular statistics of one shard ([P4] item 1: each rank reduces its
+ * shard to per-block (max, id) statistics; the blocks keep the global
+ * boundaries of the unsharded kernels, 8192 ids for draft positions and 1024
+ * for the bonus position, also where a block straddles a shard edge).
+ *
+ * Row r uses block size B = draft_block, except the bonus row of a request
+ * (row b_i + K_i with b_i = cu_num_draft[i] + i), which uses bonus_block;
+ * cu_num_draft may be NULL, and then every row uses draft_block.  With
+ * b0 = floor(shard_start / B), piece p of row r is the argmax (scan_row, the
+ * same rule as a whole shard) over global ids
+ *   [max(shard_start, (b0 + p) * B), min(shard_start + shard_width, (b0 + p + 1) * B)).
+ * Every row has n_pieces = oracle_block_count(shard_start, shard_width,
+ * min(draft_block, bonus_block)) slots, written to out[p * rows + r]; the
+ * slots past the row's own piece count (rows with the larger block have
+ * fewer pieces) hold value -inf with the shard's last id, which never wins
+ * the reduction because a real piece precedes it.
+ * Returns n_pieces, or -1 if a block size is not positive or cu_num_draft
+ * does not describe `rows` rows. */
+int64_t oracle_block_stats(const void *logits, int dtype, int64_t rows, int64_t ld,
+                           int64_t shard_start, int64_t shard_width, int64_t org_vocab,
+                           int64_t draft_block, int64_t bonus_block, int num_reqs,
+                           const int32_t *cu_num_draft, oracle_stat *out) {
+  if (draft_block <= 0 || bonus_block <= 0) return -1;
+  const int64_t small = draft_block < bonus_block ? draft_block : bonus_block;
+  const int64_t n_pieces = oracle_block_count(shard_start, shard_width, small);
+  const int64_t shard_end = shard_start + shard_width;
+  char *is_bonus = (char *)calloc((size_t)(rows > 0 ? rows : 1), 1);
+  if (!is_bonus) return -1;
+  if (cu_num_draft) {
+    if ((int64_t)cu_num_draft[num_reqs] + num_reqs != rows) {
+      free(is_bonus);
+      return -1;
+    }
+    for (int i = 0; i < num_reqs; ++i) is_bonus[(int64_t)cu_num_draft[i + 1] + i] = 1;
+  }
+  int64_t r;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (r = 0; r < rows; ++r) {
+    const char *row = (const char *)logits + r * ld * elt_size(dtype);
+    const int64_t B = is_bonus[r] ? bonus_block : draft_block;
+    const int64_t b0 = shard_start / B;
+    const int64_t own = oracle_block_count(shard_start, shard_width, B);
+    for (int64_t p = 0; p < n_pieces; ++p) {
+      oracle_stat st;
+      if (p < own) {
+        int64_t lo = (b0 + p) * B, hi = (b0 + p + 1) * B;
+        if (lo < shard_start) lo = shard_start;
+        if (hi > shard_end) hi = shard_end;
+        st.id = scan_row(row + (lo - shard_start) * elt_size(dtype), dtype, lo, hi - lo,
+                         org_vocab, &st.v);
+      } else {
+        st.v = -INFINITY;
+        st.id = (int32_t)(shard_end - 1);
+      }
+      out[p * rows + r] = st;
+    }
+  }
+  free(is_bonus);
+  return n_pieces;
+}

@@ -6,7 +6,8 @@ local instead of a global id, a transposed stats layout, acceptance that keeps
 counting after a mismatch, a missing bonus-row offset, a wrong count, a dropped
 dot-product term, a wrong bf16 widening, a runner-up equal to the winner, the
 bonus taken from the wrong row, a wrong E4M3 exponent bias, the fp8 scales
-dropped), builds it with gcc, points the oracle wrapper
+dropped, block boundaries taken from the shard start instead of global ids,
+the bonus row's block size ignored or given to the wrong row), builds it with gcc, points the oracle wrapper
 at it, and runs the pin tests of tests/test_oracle_pins.py: at least one pin
 must fail for every mutant.  The committed oracle source is never modified.
 """
@@ -42,6 +43,12 @@ MUTANTS = {
     "e4m3_bias_off_by_one": ("v = ldexp(1.0 + (double)m / 8.0, e - 7);",
                              "v = ldexp(1.0 + (double)m / 8.0, e - 8);"),
     "fp8_scale_dropped": ("out[j] = scale * acc;", "out[j] = acc;"),
+    "blocks_relative_to_shard": ("int64_t lo = (b0 + p) * B, hi = (b0 + p + 1) * B;",
+                                 "int64_t lo = shard_start + p * B, hi = shard_start + (p + 1) * B;"),
+    "bonus_row_uses_draft_block": ("const int64_t B = is_bonus[r] ? bonus_block : draft_block;",
+                                   "const int64_t B = draft_block;"),
+    "bonus_row_is_first_row": ("is_bonus[(int64_t)cu_num_draft[i + 1] + i] = 1;",
+                               "is_bonus[(int64_t)cu_num_draft[i] + i] = 1;"),
 }
 
 PIN_CALLS = [
@@ -61,6 +68,8 @@ PIN_CALLS = [
     pins.test_lmhead_one_hot_weight_is_exact_column_pick,
     pins.test_e4m3_decode_matches_torch_float8_for_every_code,
     pins.test_lmhead_fp8_logits_match_numpy_with_scales,
+    lambda: pins.test_block_stats_match_grouped_brute_force("bf16"),
+    pins.test_block_pieces_follow_global_boundaries_across_shard_edges,
 ]
 
 

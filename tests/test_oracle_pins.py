@@ -317,3 +317,91 @@ def test_e4m3_quantizer_of_the_generators_matches_torch():
     x = np.clip(x, -448, 448)
     ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     assert (wl.f32_to_e4m3(x) == ref).all()
+
+
+def brute_block_stats(xf, shard, org_vocab, row_blocks):
+    """Independent reading of block-granular stats: group the shard's ids by
+    their global block id // B (B of that row), in ascending block order,
+    and take the set-based argmax of each group.  Returns, per row, the
+    list of (id, value) of its pieces."""
+    o, w = shard
+    res = []
+    for r, B in enumerate(row_blocks):
+        groups = {}
+        for i in range(o, o + w):
+            groups.setdefault(i // B, []).append(i)
+        res.append([brute_argmax_row(xf[r, ids[0]:ids[-1] + 1], ids[0], org_vocab)
+                    for _, ids in sorted(groups.items())])
+    return res
+
+
+def row_blocks_of(rows, cu, draft_block, bonus_block):
+    blocks = [draft_block] * rows
+    if cu is not None:
+        for i in range(len(cu) - 1):
+            blocks[cu[i + 1] + i] = bonus_block
+    return blocks
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_block_stats_match_grouped_brute_force(dtype):
+    rng = np.random.default_rng(21)
+    for trial in range(12):
+        n = int(rng.integers(1, 5))
+        ks = rng.integers(0, 4, n)
+        cu = np.concatenate([[0], np.cumsum(ks)]).astype(np.int32)
+        rows = int(cu[-1]) + n
+        vocab = int(rng.integers(20, 90))
+        x = wl.discrete_logits(300 + trial, rows, vocab, dtype, p_nan=0.02)
+        xf = as_f32(x)
+        shards = wl.random_shards(trial, vocab, int(rng.integers(1, 5)))
+        draft_block, bonus_block = [(8, 2), (4, 16), (16, 16), (1, 4), (32, 8), (128, 1)][trial % 6]
+        use_cu = trial % 3 != 0
+        blocks = row_blocks_of(rows, cu if use_cu else None, draft_block, bonus_block)
+        for org in (vocab, vocab - 7, shards[-1][0] + 1):
+            for o, w in shards:
+                st = oracle.block_stats(x, o, w, org, draft_block, bonus_block,
+                                        cu if use_cu else None)
+                n_pieces = oracle.block_count(o, w, min(draft_block, bonus_block))
+                assert st.shape[0] == n_pieces * rows
+                exp = brute_block_stats(xf, (o, w), org, blocks)
+                for r in range(rows):
+                    for p in range(n_pieces):
+                        got = st[p * rows + r]
+                        if p < len(exp[r]):
+                            assert got["id"] == exp[r][p][0], (trial, o, w, r, p)
+                            assert bits32(got["v"]) == bits32(exp[r][p][1])
+                        else:
+                            assert got["id"] == o + w - 1 and got["v"] == -np.inf
+
+
+def test_block_stats_reduce_to_the_full_argmax_and_to_shard_stats():
+    # the reduction over all pieces of all shards is the unsharded argmax for
+    # every block size; one block wider than the vocab gives the shard stats
+    x = wl.discrete_logits(7, 40, 700, "bf16", p_nan=0.003, p_inf=0.01)
+    cu = np.array([0, 3, 3, 10, 25, 35], np.int32)          # 35 drafts + 5 bonus rows
+    for shards in (wl.even_shards(700, 3), wl.random_shards(4, 700, 5), [(0, 700)]):
+        for org in (700, 613):
+            _, full_ids = oracle.full_argmax(x, org)
+            for db, bb in ((8192, 1024), (64, 16), (16, 64), (1, 1), (256, 256)):
+                st, n = oracle.gathered_block_stats(x, shards, org, db, bb, cu)
+                assert n == sum(oracle.block_count(o, w, min(db, bb)) for o, w in shards)
+                _, ids = oracle.shard_reduce(st, n, 40)
+                assert (ids == full_ids).all(), (db, bb, org)
+            st, n = oracle.gathered_block_stats(x, shards, org, 1 << 20)
+            assert n == len(shards)
+            sh = oracle.gathered_stats(x, shards, org)
+            assert (st["id"] == sh["id"]).all() and (bits32(st["v"]) == bits32(sh["v"])).all()
+
+
+def test_block_pieces_follow_global_boundaries_across_shard_edges():
+    # shard [5, 15) with 4-id blocks: pieces [5,8), [8,12), [12,15); the
+    # second shard [15, 21) starts inside block [12,16), which it shares
+    vals = np.arange(21, dtype=np.float32)[::-1].copy()   # strictly decreasing
+    x = vals[None, :]
+    assert oracle.block_count(5, 10, 4) == 3 and oracle.block_count(15, 6, 4) == 3
+    assert list(oracle.block_stats(x, 5, 10, 21, 4)["id"]) == [5, 8, 12]
+    assert list(oracle.block_stats(x, 15, 6, 21, 4)["id"]) == [15, 16, 20]
+    assert list(oracle.block_stats(x, 15, 6, 18, 4)["id"]) == [15, 16, 20]
+    st = oracle.block_stats(x, 15, 6, 18, 4)
+    assert st["v"][0] == 5.0 and st["v"][1] == 4.0 and st["v"][2] == -np.inf
