@@ -139,6 +139,12 @@ def block_count(shard_start, shard_width, block):
     return int(lib().oracle_block_count(int(shard_start), int(shard_width), int(block)))
 
 
+def block_slots(shard_start, shard_width, draft_block, bonus_block):
+    """Stats slots per row of one shard: the larger of the two block counts."""
+    return max(block_count(shard_start, shard_width, draft_block),
+               block_count(shard_start, shard_width, bonus_block))
+
+
 def block_stats(x, shard_start, shard_width, org_vocab, draft_block, bonus_block=None,
                 cu_num_draft=None):
     """Block-granular stats of one shard: [n_pieces * rows] entries, piece-major.
@@ -149,7 +155,7 @@ def block_stats(x, shard_start, shard_width, org_vocab, draft_block, bonus_block
     if shard_start < 0 or shard_width <= 0 or shard_start + shard_width > x.shape[1]:
         raise ValueError("shard outside the row")
     bonus_block = draft_block if bonus_block is None else bonus_block
-    n = block_count(shard_start, shard_width, min(draft_block, bonus_block))
+    n = block_slots(shard_start, shard_width, draft_block, bonus_block)
     out = np.zeros(n * rows, STAT)
     cu = None if cu_num_draft is None else np.ascontiguousarray(cu_num_draft, np.int32)
     if rows:

@@ -353,11 +353,12 @@ int64_t oracle_block_count(int64_t shard_start, int64_t shard_width, int64_t blo
  * b0 = floor(shard_start / B), piece p of row r is the argmax (scan_row, the
  * same rule as a whole shard) over global ids
  *   [max(shard_start, (b0 + p) * B), min(shard_start + shard_width, (b0 + p + 1) * B)).
- * Every row has n_pieces = oracle_block_count(shard_start, shard_width,
- * min(draft_block, bonus_block)) slots, written to out[p * rows + r]; the
- * slots past the row's own piece count (rows with the larger block have
- * fewer pieces) hold value -inf with the shard's last id, which never wins
- * the reduction because a real piece precedes it.
+ * Every row has n_pieces slots, the larger of the two block counts
+ * oracle_block_count(shard_start, shard_width, B), written to
+ * out[p * rows + r]; the slots past the row's own piece count hold value
+ * -inf with the shard's last id, which never wins the reduction because a
+ * real piece precedes it.  (When one size divides the other the smaller
+ * block has the larger count; 3 and 2 over ids [2, 4) show that it need not.)
  * Returns n_pieces, or -1 if a block size is not positive or cu_num_draft
  * does not describe `rows` rows. */
 int64_t oracle_block_stats(const void *logits, int dtype, int64_t rows, int64_t ld,
@@ -365,8 +366,9 @@ int64_t oracle_block_stats(const void *logits, int dtype, int64_t rows, int64_t 
                            int64_t draft_block, int64_t bonus_block, int num_reqs,
                            const int32_t *cu_num_draft, oracle_stat *out) {
   if (draft_block <= 0 || bonus_block <= 0) return -1;
-  const int64_t small = draft_block < bonus_block ? draft_block : bonus_block;
-  const int64_t n_pieces = oracle_block_count(shard_start, shard_width, small);
+  const int64_t n_draft = oracle_block_count(shard_start, shard_width, draft_block);
+  const int64_t n_bonus = oracle_block_count(shard_start, shard_width, bonus_block);
+  const int64_t n_pieces = n_draft > n_bonus ? n_draft : n_bonus;
   const int64_t shard_end = shard_start + shard_width;
   char *is_bonus = (char *)calloc((size_t)(rows > 0 ? rows : 1), 1);
   if (!is_bonus) return -1;

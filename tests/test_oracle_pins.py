@@ -346,7 +346,7 @@ def row_blocks_of(rows, cu, draft_block, bonus_block):
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_block_stats_match_grouped_brute_force(dtype):
     rng = np.random.default_rng(21)
-    for trial in range(12):
+    for trial in range(16):
         n = int(rng.integers(1, 5))
         ks = rng.integers(0, 4, n)
         cu = np.concatenate([[0], np.cumsum(ks)]).astype(np.int32)
@@ -355,14 +355,16 @@ def test_block_stats_match_grouped_brute_force(dtype):
         x = wl.discrete_logits(300 + trial, rows, vocab, dtype, p_nan=0.02)
         xf = as_f32(x)
         shards = wl.random_shards(trial, vocab, int(rng.integers(1, 5)))
-        draft_block, bonus_block = [(8, 2), (4, 16), (16, 16), (1, 4), (32, 8), (128, 1)][trial % 6]
+        draft_block, bonus_block = [(8, 2), (4, 16), (16, 16), (1, 4), (32, 8), (128, 1),
+                                    (3, 2), (5, 7)][trial % 8]
         use_cu = trial % 3 != 0
         blocks = row_blocks_of(rows, cu if use_cu else None, draft_block, bonus_block)
         for org in (vocab, vocab - 7, shards[-1][0] + 1):
             for o, w in shards:
                 st = oracle.block_stats(x, o, w, org, draft_block, bonus_block,
                                         cu if use_cu else None)
-                n_pieces = oracle.block_count(o, w, min(draft_block, bonus_block))
+                n_pieces = max(len({i // B for i in range(o, o + w)})
+                               for B in (draft_block, bonus_block))
                 assert st.shape[0] == n_pieces * rows
                 exp = brute_block_stats(xf, (o, w), org, blocks)
                 for r in range(rows):
@@ -383,9 +385,10 @@ def test_block_stats_reduce_to_the_full_argmax_and_to_shard_stats():
     for shards in (wl.even_shards(700, 3), wl.random_shards(4, 700, 5), [(0, 700)]):
         for org in (700, 613):
             _, full_ids = oracle.full_argmax(x, org)
-            for db, bb in ((8192, 1024), (64, 16), (16, 64), (1, 1), (256, 256)):
+            for db, bb in ((8192, 1024), (64, 16), (16, 64), (1, 1), (256, 256), (24, 7)):
                 st, n = oracle.gathered_block_stats(x, shards, org, db, bb, cu)
-                assert n == sum(oracle.block_count(o, w, min(db, bb)) for o, w in shards)
+                assert n == sum(max(oracle.block_count(o, w, db), oracle.block_count(o, w, bb))
+                                for o, w in shards)
                 _, ids = oracle.shard_reduce(st, n, 40)
                 assert (ids == full_ids).all(), (db, bb, org)
             st, n = oracle.gathered_block_stats(x, shards, org, 1 << 20)
@@ -400,6 +403,8 @@ def test_block_pieces_follow_global_boundaries_across_shard_edges():
     vals = np.arange(21, dtype=np.float32)[::-1].copy()   # strictly decreasing
     x = vals[None, :]
     assert oracle.block_count(5, 10, 4) == 3 and oracle.block_count(15, 6, 4) == 3
+    assert oracle.block_count(2, 2, 3) == 2 and oracle.block_count(2, 2, 2) == 1
+    assert oracle.block_slots(2, 2, 2, 3) == 2
     assert list(oracle.block_stats(x, 5, 10, 21, 4)["id"]) == [5, 8, 12]
     assert list(oracle.block_stats(x, 15, 6, 21, 4)["id"]) == [15, 16, 20]
     assert list(oracle.block_stats(x, 15, 6, 18, 4)["id"]) == [15, 16, 20]
