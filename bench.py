@@ -45,8 +45,8 @@ def parse_args():
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["large_verify", "lmhead", "lmhead_fp8",
-                                          "draft_top_tokens", "greedy_verify"],
+    p.add_argument("--workload", choices=["large_verify", "large_verify_blocks", "lmhead",
+                                          "lmhead_fp8", "draft_top_tokens", "greedy_verify"],
                    default="large_verify")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -196,7 +196,7 @@ def max_over_ranks(value, world, device=None):
 class VerifyPath:
     """Device buffers and one step of the large-verify path."""
 
-    def __init__(self, c, torch, sga):
+    def __init__(self, c, torch, sga, blocks=None):
         self.torch, self.sga = torch, sga
         self.rows = c["logits"].shape[0]
         self.shards = c["shards"]
@@ -205,13 +205,19 @@ class VerifyPath:
         self.cu_host = c["cu_num_draft"]
         self.n = self.cu_host.size - 1
         self.x = torch.from_numpy(c["logits"].view(np.int16)).view(torch.bfloat16).cuda()
-        self.stats = sga.new_stats(len(self.shards) * self.rows)
+        # blocks = (draft_block, bonus_block): block-granular stats, one
+        # sga_local_argmax_blocks launch per shard; else one stat per shard
+        self.blocks = blocks
+        self.slots = ([sga.sga_block_slots(o, w, *blocks) for o, w in self.shards] if blocks
+                      else [1] * len(self.shards))
+        self.n_stats = sum(self.slots)
+        self.stats = sga.new_stats(self.n_stats * self.rows)
         self.cu = torch.from_numpy(self.cu_host).cuda()
         # drafts: copy the target's greedy token where the plan says so; the
         # target tokens come from one untimed pass of the device path
         t = torch.empty(self.rows, dtype=torch.int32, device="cuda")
         self.run_argmax()
-        sga.sga_shard_reduce(self.stats, len(self.shards), self.rows, t)
+        sga.sga_shard_reduce(self.stats, self.n_stats, self.rows, t)
         self.drafts_host = wl.compose_drafts(t.cpu().numpy(), self.cu_host, c["flags"], c["rand_ids"])
         self.drafts = torch.from_numpy(self.drafts_host).cuda()
         i32 = dict(dtype=torch.int32, device="cuda")
@@ -219,29 +225,40 @@ class VerifyPath:
         self.num_sampled = torch.empty(self.n, **i32)
         self.num_rejected = torch.empty(self.n, **i32)
         self.bonus = torch.empty(self.n, **i32)
-        self.launches_per_step = 2
+        self.launches_per_step = 1 + (len(self.shards) if blocks else 1)
         elt = 2
-        self.argmax_bytes = [self.rows * (w * elt + 8) for _, w in self.shards]
-        self.step_bytes = (sum(self.argmax_bytes) + 8 * len(self.shards) * self.rows
+        self.argmax_bytes = [self.rows * (w * elt + 8 * n) for (_, w), n in zip(self.shards, self.slots)]
+        self.step_bytes = (sum(self.argmax_bytes) + 8 * self.n_stats * self.rows
                            + 4 * int(self.cu_host[-1]) + 4 * (self.n + 1)
                            + 4 * self.n * (self.k + 1) + 12 * self.n)
 
     def run_argmax(self, events=None):
-        """All shards of this GPU in one launch (sga_local_argmax_shards)."""
+        """All shards of this GPU in one launch (sga_local_argmax_shards), or
+        with block stats one sga_local_argmax_blocks launch per shard."""
         if events is not None:
             events[0].record()
-        self.sga.sga_local_argmax_shards(self.x, self.shards, self.org, self.stats)
+        if self.blocks:
+            self.run_argmax_per_shard()
+        else:
+            self.sga.sga_local_argmax_shards(self.x, self.shards, self.org, self.stats)
         if events is not None:
             events[1].record()
 
     def run_argmax_per_shard(self):
         """One launch per shard, as separate tensor-parallel ranks would."""
-        for s, (o, w) in enumerate(self.shards):
-            self.sga.sga_local_argmax(self.x[:, o:o + w], o, w, self.org,
-                                      self.stats[s * self.rows:(s + 1) * self.rows])
+        off = 0
+        for (o, w), n in zip(self.shards, self.slots):
+            out = self.stats[off * self.rows:(off + n) * self.rows]
+            if self.blocks:
+                self.sga.sga_local_argmax_blocks(self.x[:, o:o + w], o, w, self.org,
+                                                 self.blocks[0], out, bonus_block=self.blocks[1],
+                                                 cu_num_draft=self.cu)
+            else:
+                self.sga.sga_local_argmax(self.x[:, o:o + w], o, w, self.org, out)
+            off += n
 
     def run_verify(self):
-        self.sga.sga_greedy_verify(self.stats, len(self.shards), self.cu, self.drafts, self.k,
+        self.sga.sga_greedy_verify(self.stats, self.n_stats, self.cu, self.drafts, self.k,
                                    self.sampled, self.num_sampled, self.num_rejected, self.bonus)
 
     def step(self, events=None):
@@ -416,7 +433,10 @@ def run_reference(args, c_builder):
     return 0
 
 
-def run_ours_verify(args):
+BLOCK_SIZES = (8192, 1024)   # draft / bonus block of the per-block statistics
+
+
+def run_ours_verify(args, blocks=None):
     import torch
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
@@ -430,7 +450,9 @@ def run_ours_verify(args):
     c = wl.large_verify(rows_limit=args.rows)
     if args.rows is not None:
         c["name"] += f" (first {c['logits'].shape[0]} rows)"
-    path = VerifyPath(c, torch, sga)
+    if blocks:
+        c["name"] += f", block stats {blocks[0]}/{blocks[1]} (draft/bonus)"
+    path = VerifyPath(c, torch, sga, blocks)
     total_ms, argmax_ms, verify_ms, clocks = time_device_steps(path, args.steps, args.warmup,
                                                                torch, world, rank)
     total_ms = max_over_ranks(total_ms, world, "cuda")
@@ -442,9 +464,13 @@ def run_ours_verify(args):
     argmax_bytes = sum(path.argmax_bytes)
     achieved = argmax_bytes / (argmax_ms * 1e-3) / 1e9
     per_shard_ms = time_per_shard_steps(path, max(20, min(500, args.steps // 4)), torch)
-    traffic = ncu_traffic("local_argmax_large_verify.md",
-                          ["greedy_spec_decode_gb300/csrc/argmax.cu",
+    kernel_src = "blocks.cu" if blocks else "argmax.cu"
+    traffic = ncu_traffic("block_argmax_large_verify.md" if blocks
+                          else "local_argmax_large_verify.md",
+                          ["greedy_spec_decode_gb300/csrc/" + kernel_src,
+                           "greedy_spec_decode_gb300/csrc/scan.cuh",
                            "greedy_spec_decode_gb300/csrc/common.cuh"])  # device code only
+    # (the block-stats profile records the DRAM bytes of one step's launches, one per shard)
     e2e_ms, h2d, d2h = time_e2e(path, c, args.e2e_steps, torch)
     e2e_ms = max_over_ranks(e2e_ms, world, "cuda")
 
@@ -461,11 +487,13 @@ def run_ours_verify(args):
         "data": "synthetic",
         "config": {"workload": c["name"], "rows": path.rows, "vocab": int(c["logits"].shape[1]),
                    "shards": [w for _, w in path.shards], "requests": path.n, "k": path.k,
+                   "stats_per_row": path.n_stats,
                    "l2": f"inputs ({c['logits'].nbytes / 1e9:.2f} GB) larger than L2 (129 MB); no flush",
                    "parallelism": f"{world} independent replica(s), emulated TP{len(path.shards)} per GPU"},
         "step_gbs": path.step_bytes / (step_ms * 1e-3) / 1e9,
         "step_frac_of_hbm": path.step_bytes / (step_ms * 1e-3) / 1e9 / hbm,
-        "kernel_us": {"local_argmax_all_shards": round(argmax_ms * 1e3, 2),
+        "kernel_us": {("block_argmax_all_shards" if blocks else "local_argmax_all_shards"):
+                      round(argmax_ms * 1e3, 2),
                       "greedy_verify": round(verify_ms * 1e3, 2),
                       "note": f"CUDA events on every {EVENT_STRIDE}th timed step; the other "
                               "steps run back to back, where the verify launch overlaps "
@@ -473,7 +501,9 @@ def run_ours_verify(args):
         "per_shard_launches": {"ms_per_step": per_shard_ms,
                                "rows_per_s": world * path.rows / (per_shard_ms * 1e-3),
                                "note": "same step with one sga_local_argmax launch per shard"},
-        "roofline": {"bound": "hbm", "kernel": "local_argmax_kernel<bf16> (all shards, one launch)",
+        "roofline": {"bound": "hbm",
+                     "kernel": ("block_argmax_kernel<bf16> (one launch per shard, summed)" if blocks
+                                else "local_argmax_kernel<bf16> (all shards, one launch)"),
                      "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": traffic,
                      "peak_source": f"{pk_src} hbm_gbs (MEASURED_PEAKS.json copy bandwidth)"
@@ -740,6 +770,8 @@ def main():
         return run_ours_small(args, wl.draft_top_tokens)
     if args.workload == "greedy_verify":
         return run_ours_small(args, wl.greedy_verify_small)
+    if args.workload == "large_verify_blocks":
+        return run_ours_verify(args, BLOCK_SIZES)
     return run_ours_verify(args)
 
 

@@ -27,7 +27,7 @@ LIB_PATH = os.path.join(_PKG, "_build", "libsga.so")
 SGA_F32, SGA_BF16 = 0, 1
 SGA_MAX_K = 15
 SGA_MAX_VOCAB = 1 << 24
-SGA_DEVERR_K_RANGE, SGA_DEVERR_D2T_RANGE, SGA_DEVERR_TIMEOUT = 1, 2, 4
+SGA_DEVERR_K_RANGE, SGA_DEVERR_D2T_RANGE, SGA_DEVERR_TIMEOUT, SGA_DEVERR_LAYOUT = 1, 2, 4, 8
 
 _lib = None
 
@@ -53,6 +53,9 @@ def lib():
             "sga_status_string": ([i32], ctypes.c_char_p),
             "sga_local_argmax": ([vp, i32, i64, i64, i64, i64, i64, vp, vp], i32),
             "sga_local_argmax_shards": ([vp, i32, i64, i64, i32, vp, vp, i64, vp, vp], i32),
+            "sga_block_slots": ([i64, i64, i64, i64], i64),
+            "sga_local_argmax_blocks": ([vp, i32, i64, i64, i64, i64, i64, i64, i64, i32, vp,
+                                         vp, vp], i32),
             "sga_shard_reduce": ([vp, i32, i64, vp, vp, vp, i64, vp], i32),
             "sga_greedy_verify": ([vp, i32, i32, vp, vp, i32, vp, vp, vp, vp, vp, vp], i32),
             "sga_lmhead_argmax_workspace": ([i64, i64], sz),
@@ -144,6 +147,35 @@ def sga_local_argmax_shards(logits, shards, org_vocab, out_stats, stream=None):
     ld = logits.stride(0) if rows > 1 else max(logits.stride(0), logits.size(1))
     _check("sga_local_argmax_shards", lib().sga_local_argmax_shards(
         _ptr(logits), _dtype_code(logits), rows, ld, n, starts, widths, int(org_vocab),
+        _ptr(out_stats), _stream(stream)))
+    return out_stats
+
+
+def sga_block_slots(shard_start, shard_width, draft_block, bonus_block=None):
+    """Stats per row that sga_local_argmax_blocks writes for one shard."""
+    bonus_block = draft_block if bonus_block is None else bonus_block
+    n = int(lib().sga_block_slots(int(shard_start), int(shard_width), int(draft_block),
+                                  int(bonus_block)))
+    _check("sga_block_slots", n if n < 0 else 0)
+    return n
+
+
+def sga_local_argmax_blocks(logits, shard_start, shard_width, org_vocab, draft_block,
+                            out_stats, bonus_block=None, cu_num_draft=None, stream=None):
+    """Block-granular stats of one shard: for every row, the argmax of each
+    fixed global block of ids meeting the shard.  `logits` as for
+    sga_local_argmax; out_stats receives sga_block_slots(...) * rows stats,
+    piece-major.  With cu_num_draft (int32 CUDA tensor [N + 1]) the bonus row
+    of each request uses bonus_block."""
+    if logits.dim() != 2 or (logits.size(1) > 1 and logits.stride(1) != 1):
+        raise ValueError("logits must be 2-D with unit stride along the vocab")
+    bonus_block = draft_block if bonus_block is None else bonus_block
+    rows = logits.size(0)
+    ld = logits.stride(0) if rows > 1 else max(logits.stride(0), shard_width)
+    num_reqs = 0 if cu_num_draft is None else cu_num_draft.numel() - 1
+    _check("sga_local_argmax_blocks", lib().sga_local_argmax_blocks(
+        _ptr(logits), _dtype_code(logits), rows, ld, int(shard_start), int(shard_width),
+        int(org_vocab), int(draft_block), int(bonus_block), int(num_reqs), _ptr(cu_num_draft),
         _ptr(out_stats), _stream(stream)))
     return out_stats
 

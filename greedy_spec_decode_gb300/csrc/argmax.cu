@@ -27,6 +27,7 @@
 #include <cooperative_groups.h>
 
 #include "common.cuh"
+#include "scan.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -56,56 +57,6 @@ struct ShardTable {
   int32_t col[kMaxShardsPerLaunch];    // column of that id relative to `logits`
   int32_t valid[kMaxShardsPerLaunch];  // non-padding ids of the shard
 };
-
-template <bool kBf16>
-__device__ __forceinline__ float load_elem(const char *p, int j) {
-  if (kBf16) {
-    const unsigned short b = __ldg(reinterpret_cast<const unsigned short *>(p) + j);
-    return __uint_as_float(static_cast<uint32_t>(b) << 16);
-  } else {
-    return __ldg(reinterpret_cast<const float *>(p) + j);
-  }
-}
-
-// NaN-propagating maximum of the elements of one 16-byte vector.
-template <bool kBf16>
-__device__ __forceinline__ float vec_max(const uint4 a) {
-  if (kBf16) {
-    const uint32_t m = max_nan_bf16x2(max_nan_bf16x2(a.x, a.y), max_nan_bf16x2(a.z, a.w));
-    return max_nan(bf16_lo(m), bf16_hi(m));
-  } else {
-    return max_nan(max_nan(__uint_as_float(a.x), __uint_as_float(a.y)),
-                   max_nan(__uint_as_float(a.z), __uint_as_float(a.w)));
-  }
-}
-
-// First element of a vector (ids id, id+1, ...) that the scan rule would
-// take over `best`; updates (best, best_id).
-template <bool kBf16>
-__device__ __forceinline__ void scan_vec(const uint4 a, int32_t id, float &best, int32_t &best_id) {
-  const uint32_t w[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    if (kBf16) {
-      const float lo = bf16_lo(w[k]);
-      if (scan_better(lo, best)) {
-        best = lo;
-        best_id = id + 2 * k;
-      }
-      const float hi = bf16_hi(w[k]);
-      if (scan_better(hi, best)) {
-        best = hi;
-        best_id = id + 2 * k + 1;
-      }
-    } else {
-      const float x = __uint_as_float(w[k]);
-      if (scan_better(x, best)) {
-        best = x;
-        best_id = id + k;
-      }
-    }
-  }
-}
 
 #ifndef SGA_ARGMAX_BULK
 #define SGA_ARGMAX_BULK 1
@@ -372,11 +323,7 @@ __global__ void shard_reduce_kernel(const sga_stat *__restrict__ stats, int num_
   pdl_wait();
   for (int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; r < rows;
        r += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    sga_stat b = stats[r];
-    for (int s = 1; s < num_shards; ++s) {
-      const sga_stat c = stats[static_cast<int64_t>(s) * rows + r];
-      if (scan_better(c.v, b.v)) b = c;
-    }
+    const sga_stat b = reduce_stats(stats, num_shards, rows, r);
     int32_t id = b.id;
     if (d2t != nullptr) {
       if (id >= 0 && id < d2t_len)

@@ -25,6 +25,16 @@ cudaError_t launch_local_argmax_table(const void *logits, int dtype, int64_t row
                                       const int64_t *cols, const int64_t *valids, sga_stat *out,
                                       int num_sms, uint32_t *err, cudaStream_t stream);
 
+// Block-granular statistics of one shard (blocks.cu).
+int64_t block_count(int64_t shard_start, int64_t shard_width, int64_t block);
+int64_t block_slots(int64_t shard_start, int64_t shard_width, int64_t draft_block,
+                    int64_t bonus_block);
+cudaError_t launch_block_argmax(const void *logits, int dtype, int64_t rows, int64_t ld,
+                                int64_t shard_start, int64_t shard_width, int64_t org_vocab,
+                                int64_t draft_block, int64_t bonus_block, int num_reqs,
+                                const int32_t *cu_num_draft, sga_stat *out, int num_sms,
+                                uint32_t *err, cudaStream_t stream);
+
 cudaError_t launch_shard_reduce(const sga_stat *stats, int num_shards, int64_t rows,
                                 float *out_vals, int32_t *out_ids, const int64_t *d2t,
                                 int64_t d2t_len, uint32_t *err, cudaStream_t stream);

@@ -145,6 +145,42 @@ int sga_local_argmax_shards(const void *logits, int dtype, int64_t rows, int64_t
                                                       static_cast<cudaStream_t>(stream)));
 }
 
+int64_t sga_block_slots(int64_t shard_start, int64_t shard_width, int64_t draft_block,
+                        int64_t bonus_block) {
+  const int st = check_shard(shard_start, shard_width, 1);
+  if (st != SGA_OK) return st;
+  if (draft_block < 1 || draft_block > SGA_MAX_VOCAB || bonus_block < 1 ||
+      bonus_block > SGA_MAX_VOCAB)
+    return SGA_ERR_SIZE;
+  return sga::block_slots(shard_start, shard_width, draft_block, bonus_block);
+}
+
+int sga_local_argmax_blocks(const void *logits, int dtype, int64_t rows, int64_t ld,
+                            int64_t shard_start, int64_t shard_width, int64_t org_vocab,
+                            int64_t draft_block, int64_t bonus_block, int num_reqs,
+                            const int32_t *cu_num_draft, sga_stat *out_stats,
+                            sga_stream stream) {
+  if (dtype != SGA_F32 && dtype != SGA_BF16) return SGA_ERR_DTYPE;
+  int st = check_shard(shard_start, shard_width, org_vocab);
+  if (st != SGA_OK) return st;
+  const int64_t slots = sga_block_slots(shard_start, shard_width, draft_block, bonus_block);
+  if (slots < 0) return static_cast<int>(slots);
+  if (rows < 0 || rows * slots > (int64_t(1) << 28)) return SGA_ERR_SIZE;
+  if (ld < shard_width) return SGA_ERR_SHARD;
+  if (cu_num_draft != nullptr && num_reqs < 1) return SGA_ERR_SIZE;
+  if (rows == 0) return SGA_OK;
+  if (logits == nullptr || out_stats == nullptr) return SGA_ERR_NULL;
+  if (misaligned(logits, dtype == SGA_BF16 ? 2 : 4) || misaligned(out_stats, 8) ||
+      misaligned(cu_num_draft, 4))
+    return SGA_ERR_ALIGN;
+  DeviceInfo d;
+  if ((st = current_device(&d)) != SGA_OK) return st;
+  return launch_status(sga::launch_block_argmax(logits, dtype, rows, ld, shard_start, shard_width,
+                                                org_vocab, draft_block, bonus_block, num_reqs,
+                                                cu_num_draft, out_stats, d.num_sms, d.err,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
 int sga_shard_reduce(const sga_stat *stats, int num_shards, int64_t rows, float *out_vals,
                      int32_t *out_ids, const int64_t *d2t, int64_t d2t_len,
                      sga_stream stream) {

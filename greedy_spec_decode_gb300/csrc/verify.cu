@@ -9,16 +9,23 @@
 // bonus token is the last emitted one.
 //
 // Layout: 16 lanes per request (K <= 15, so K + 1 <= 16 rows), two requests
-// per warp.  Lane j reduces row j of its request over the shards, compares
+// per warp.  Lane j reduces row j of its request over the gathered statistics
+// (one entry per shard, or per block piece of block-granular statistics), compares
 // with draft j, and one ballot gives the first mismatch.  The work is a few
 // bytes per row, so the kernel is latency-bound; it exists to keep the whole
 // verify step in one launch.
 #include "common.cuh"
+#include "scan.cuh"
 
 namespace sga {
 namespace {
 
 constexpr int kThreads = 256;
+// Above this many statistics per row the wide kernel (a warp per row) is used.
+#ifndef SGA_VERIFY_WIDE_ENTRIES
+#define SGA_VERIFY_WIDE_ENTRIES 16
+#endif
+constexpr int kWideEntries = SGA_VERIFY_WIDE_ENTRIES;
 
 __global__ void __launch_bounds__(kThreads)
     greedy_verify_kernel(const sga_stat *__restrict__ stats, int num_shards, int num_reqs,
@@ -47,12 +54,7 @@ __global__ void __launch_bounds__(kThreads)
   bool mismatch = false;
   if (has_row) {
     const int64_t row = static_cast<int64_t>(c) + req + j;
-    sga_stat b = stats[row];
-    for (int s = 1; s < num_shards; ++s) {
-      const sga_stat cand = stats[static_cast<int64_t>(s) * total_rows + row];
-      if (scan_better(cand.v, b.v)) b = cand;
-    }
-    t = b.id;
+    t = reduce_stats(stats, num_shards, total_rows, row).id;
     if (out_target_ids) out_target_ids[row] = t;
     if (j < k) mismatch = draft_tokens[c + j] != t;
   }
@@ -80,6 +82,99 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// Many statistics per row (block-granular statistics: hundreds per row): one
+// CTA per request, warp j reduces row j.  Lane l scans entries l, l + 32, ...
+// in ascending order with the scan rule, then the warp merges the lanes'
+// winners on (value, entry position): NaN first, larger value, then the
+// EARLIER position, which is exactly the sequential scan over all entries
+// (the first NaN, else the first maximum).  Lanes 0..15 of warp 0 then finish
+// the request as in the narrow kernel.
+constexpr int kWideWarps = 16;
+
+__global__ void __launch_bounds__(kWideWarps * 32)
+    greedy_verify_wide_kernel(const sga_stat *__restrict__ stats, int num_entries, int num_reqs,
+                              const int32_t *__restrict__ cu_num_draft,
+                              const int32_t *__restrict__ draft_tokens, int max_k,
+                              int32_t *__restrict__ out_sampled,
+                              int32_t *__restrict__ out_num_sampled,
+                              int32_t *__restrict__ out_num_rejected,
+                              int32_t *__restrict__ out_bonus, int32_t *__restrict__ out_target_ids,
+                              uint32_t *err) {
+  __shared__ int32_t t_row[kWideWarps];
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int j = threadIdx.x >> 5;  // row within the request
+  const int64_t req = blockIdx.x;
+  const int64_t total_rows = static_cast<int64_t>(cu_num_draft[num_reqs]) + num_reqs;
+  const int32_t c = cu_num_draft[req];
+  const int32_t k = cu_num_draft[req + 1] - c;
+  const bool bad = k < 0 || k > max_k;
+  if (!bad && j <= k) {
+    const int64_t row = static_cast<int64_t>(c) + req + j;
+    float bv = __int_as_float(0xff800000);
+    int32_t bpos = kNoId, bid = 0;
+    int s = lane;
+    for (; s + 7 * 32 < num_entries; s += 8 * 32) {
+      sga_stat e[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) e[u] = stats[static_cast<int64_t>(s + u * 32) * total_rows + row];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (bpos == kNoId || scan_better(e[u].v, bv)) {
+          bv = e[u].v;
+          bpos = s + u * 32;
+          bid = e[u].id;
+        }
+    }
+    for (; s < num_entries; s += 32) {
+      const sga_stat e = stats[static_cast<int64_t>(s) * total_rows + row];
+      if (bpos == kNoId || scan_better(e.v, bv)) {
+        bv = e.v;
+        bpos = s;
+        bid = e.id;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int32_t op = __shfl_xor_sync(0xffffffffu, bpos, off);
+      const int32_t oi = __shfl_xor_sync(0xffffffffu, bid, off);
+      if (op != kNoId && (bpos == kNoId || pair_beats(ov, op, bv, bpos))) {
+        bv = ov;
+        bpos = op;
+        bid = oi;
+      }
+    }
+    if (lane == 0) {
+      t_row[j] = bid;
+      if (out_target_ids) out_target_ids[row] = bid;
+    }
+  }
+  __syncthreads();
+  if (j != 0 || lane >= 16) return;
+  int32_t *sampled_row = out_sampled + req * (max_k + 1);
+  if (bad) {
+    if (lane <= max_k) sampled_row[lane] = -1;
+    if (lane == 0) {
+      out_num_sampled[req] = 0;
+      out_num_rejected[req] = 0;
+      out_bonus[req] = -1;
+      atomicOr(err, SGA_DEVERR_K_RANGE);
+    }
+    return;
+  }
+  const int32_t t = lane <= k ? t_row[lane] : -1;
+  const bool mismatch = lane < k && draft_tokens[c + lane] != t;
+  const uint32_t mine = __ballot_sync(0x0000ffffu, mismatch);
+  const int a = mine ? __ffs(mine) - 1 : k;  // accepted drafts
+  if (lane <= max_k) sampled_row[lane] = lane <= a ? t : -1;
+  if (lane == a) out_bonus[req] = t;
+  if (lane == 0) {
+    out_num_sampled[req] = a + 1;
+    out_num_rejected[req] = k - a;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_greedy_verify(const sga_stat *stats, int num_shards, int num_reqs,
@@ -87,17 +182,23 @@ cudaError_t launch_greedy_verify(const sga_stat *stats, int num_shards, int num_
                                  int max_k, int32_t *out_sampled, int32_t *out_num_sampled,
                                  int32_t *out_num_rejected, int32_t *out_bonus,
                                  int32_t *out_target_ids, uint32_t *err, cudaStream_t stream) {
-  const int64_t threads_needed = static_cast<int64_t>(num_reqs) * 16;
-  const unsigned blocks = static_cast<unsigned>((threads_needed + kThreads - 1) / kThreads);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(blocks);
-  cfg.blockDim = dim3(kThreads);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (num_shards > kWideEntries) {
+    cfg.gridDim = dim3(static_cast<unsigned>(num_reqs));
+    cfg.blockDim = dim3(kWideWarps * 32);
+    return cudaLaunchKernelEx(&cfg, greedy_verify_wide_kernel, stats, num_shards, num_reqs,
+                              cu_num_draft, draft_tokens, max_k, out_sampled, out_num_sampled,
+                              out_num_rejected, out_bonus, out_target_ids, err);
+  }
+  const int64_t threads_needed = static_cast<int64_t>(num_reqs) * 16;
+  cfg.gridDim = dim3(static_cast<unsigned>((threads_needed + kThreads - 1) / kThreads));
+  cfg.blockDim = dim3(kThreads);
   return cudaLaunchKernelEx(&cfg, greedy_verify_kernel, stats, num_shards, num_reqs, cu_num_draft,
                             draft_tokens, max_k, out_sampled, out_num_sampled, out_num_rejected,
                             out_bonus, out_target_ids, err);

@@ -146,6 +146,55 @@ int sga_local_argmax_shards(const void *logits, int dtype, int64_t rows, int64_t
                             sga_stat *out_stats, sga_stream stream);
 
 /*
+ * sga_block_slots -- statistics per row that sga_local_argmax_blocks writes
+ * for one shard: the larger of the numbers of fixed global blocks of
+ * draft_block and of bonus_block ids that meet [shard_start, shard_start +
+ * shard_width).  Returns that count (>= 1), or a negative SGA_ERR_* for an
+ * invalid shard or block size.  Pure host arithmetic, no CUDA call.
+ */
+int64_t sga_block_slots(int64_t shard_start, int64_t shard_width, int64_t draft_block,
+                        int64_t bonus_block);
+
+/*
+ * sga_local_argmax_blocks -- block-granular statistics of one shard: for
+ * every row, the argmax (value, GLOBAL id) of each fixed global block of ids
+ * [b*B, (b+1)*B) that meets the shard, clipped to the shard; a block that
+ * straddles a shard edge gives one piece on each side.
+ * Page: vLLM PR #62604, Purpose item 1 (each rank reduces its shard to
+ * per-block (max, token id) statistics; the blocks keep the unsharded
+ * kernels' global boundaries, 8192 ids for draft positions and 1024 for the
+ * bonus position, also across shard edges, so ties resolve as on the full
+ * logits).
+ *
+ *   logits, dtype, rows, ld, shard_start, shard_width, org_vocab
+ *                 as sga_local_argmax (rows <= 2^28 / slots).
+ *   draft_block   block size B of the draft rows, 1 .. SGA_MAX_VOCAB.
+ *   bonus_block   block size of the bonus rows, 1 .. SGA_MAX_VOCAB.
+ *   num_reqs, cu_num_draft   the request layout of sga_greedy_verify
+ *                 (device int32 [num_reqs + 1]; rows == cu_num_draft[num_reqs]
+ *                 + num_reqs is a precondition).  Row cu_num_draft[i+1] + i
+ *                 is the bonus row of request i.  cu_num_draft may be NULL:
+ *                 then every row is a draft row and num_reqs is ignored.
+ *   out_stats     device, slots * rows entries, 8-byte aligned, with slots =
+ *                 sga_block_slots(shard_start, shard_width, draft_block,
+ *                 bonus_block).  Piece p of row r (ascending ids) goes to
+ *                 out_stats[p*rows + r]; a row with fewer pieces than slots
+ *                 (the rows whose block size gives the smaller count) gets
+ *                 (-inf, shard_start + shard_width - 1) in its remaining
+ *                 slots, which never wins a reduction.  An all-padding piece
+ *                 reports (-inf, its first id).
+ * The stats of all shards, concatenated in shard order, go to
+ * sga_shard_reduce or sga_greedy_verify with num_shards = the sum of the
+ * shards' slots (at most 4096) and give the same ids as per-shard stats.
+ * Errors as sga_local_argmax, plus SGA_ERR_SIZE for a block size out of range.
+ */
+int sga_local_argmax_blocks(const void *logits, int dtype, int64_t rows, int64_t ld,
+                            int64_t shard_start, int64_t shard_width, int64_t org_vocab,
+                            int64_t draft_block, int64_t bonus_block, int num_reqs,
+                            const int32_t *cu_num_draft, sga_stat *out_stats,
+                            sga_stream stream);
+
+/*
  * sga_shard_reduce -- global argmax from the gathered shard statistics,
  * optionally mapped from draft ids to target ids.
  * Page: vLLM PR #34049, Solution step 3 (reduce across ranks to the global
@@ -305,13 +354,16 @@ int sga_lmhead_argmax_noalloc(const void *hidden, int64_t M, int64_t H,
  * of trapping: SGA_DEVERR_K_RANGE (a request's K_i outside [0, max_k]),
  * SGA_DEVERR_D2T_RANGE (a winning id outside the d2t table),
  * SGA_DEVERR_TIMEOUT (a bounded wait inside a pipelined kernel gave up; its
- * outputs are not valid).  sga_device_error synchronises the current device
+ * outputs are not valid), SGA_DEVERR_LAYOUT (sga_local_argmax_blocks: a
+ * request of cu_num_draft names rows outside [0, rows); that request's
+ * statistics are not written).  sga_device_error synchronises the current device
  * and copies the word to *out_word (host pointer); sga_clear_device_error
  * synchronises and zeroes it.  Both return SGA_OK or SGA_ERR_CUDA.
  */
 #define SGA_DEVERR_K_RANGE 1u
 #define SGA_DEVERR_D2T_RANGE 2u
 #define SGA_DEVERR_TIMEOUT 4u
+#define SGA_DEVERR_LAYOUT 8u
 int sga_device_error(uint32_t *out_word);
 int sga_clear_device_error(void);
 

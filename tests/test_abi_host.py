@@ -131,3 +131,38 @@ def test_fp8_validation(sga_lib):
     assert f(fake, None, 4, 128, fake, -1.0, 0, 64, 64, fake, fake, ws, None) == -2
     assert f(fake, ctypes.c_void_p(0x10002), 4, 128, fake, 1.0, 0, 64, 64, fake, fake, ws,
              None) == -6
+
+
+def test_block_slots_and_block_argmax_validation(sga_lib):
+    L = sga_lib.lib()
+    slots = L.sga_block_slots
+    assert slots(0, 67350, 8192, 1024) == 66            # 1024-blocks 0..65
+    assert slots(67350, 67349, 8192, 1024) == 67         # blocks 65..131
+    assert slots(67350, 67349, 8192, 8192) == 9          # blocks 8..16
+    assert slots(2, 2, 2, 3) == 2                        # 3 does not nest in 2
+    assert slots(5, 10, 1 << 20, 1 << 20) == 1
+    assert slots(0, 10, 0, 4) == -2 and slots(0, 10, 4, (1 << 24) + 1) == -2
+    assert slots(-1, 10, 4, 4) == -3 and slots(0, 0, 4, 4) == -3
+    assert sga_lib.sga_block_slots(0, 67350, 8192) == 9
+    with pytest.raises(sga_lib.SgaError):
+        sga_lib.sga_block_slots(0, 10, 0)
+    f = L.sga_local_argmax_blocks
+    ok = dict(logits=FAKE, dtype=1, rows=4, ld=100, start=0, width=100, org=100, db=16, bb=4,
+              n=0, cu=None, out=FAKE)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["logits"], a["dtype"], a["rows"], a["ld"], a["start"], a["width"], a["org"],
+                 a["db"], a["bb"], a["n"], a["cu"], a["out"], None)
+
+    assert call(dtype=2) == -5
+    assert call(db=0) == -2 and call(bb=-4) == -2
+    assert call(rows=-1) == -2
+    assert call(rows=1 << 27) == -2                      # rows * 25 slots > 2^28
+    assert call(width=0) == -3 and call(ld=99) == -3
+    assert call(org=0) == -4
+    assert call(cu=FAKE, n=0) == -2                      # a request layout needs requests
+    assert call(rows=0) == 0
+    assert call(logits=None) == -1 and call(out=None) == -1
+    assert call(dtype=0, logits=BAD_F32) == -6
+    assert call(cu=ctypes.c_void_p(0x10002), n=2) == -6

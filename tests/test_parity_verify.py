@@ -57,8 +57,9 @@ def random_stats(rng, rows, num_shards, vocab):
     return oracle.gathered_stats(x, shards, vocab), x, shards
 
 
-@pytest.mark.parametrize("num_shards", [1, 2, 3, 4, 8])
+@pytest.mark.parametrize("num_shards", [1, 2, 3, 4, 8, 16, 17, 40, 257])
 def test_random_variable_k_and_placeholders(sga_lib, num_shards):
+    # up to 16 entries per row: 16 lanes per request; above: a warp per row
     rng = np.random.default_rng(num_shards)
     for trial in range(6):
         n = int(rng.integers(1, 300))
@@ -75,24 +76,26 @@ def test_random_variable_k_and_placeholders(sga_lib, num_shards):
         check_verify(stats_dev, stats_np, num_shards, cu, drafts, max_k)
 
 
-def test_target_ids_optional(sga_lib):
+@pytest.mark.parametrize("num_shards", [2, 20])
+def test_target_ids_optional(sga_lib, num_shards):
     rng = np.random.default_rng(5)
     cu = np.array([0, 3, 6], np.int32)
-    stats_np, _, _ = random_stats(rng, 8, 2, 100)
+    stats_np, _, _ = random_stats(rng, 8, num_shards, 100)
     stats_dev = torch.from_numpy(stats_np.view(np.int32).reshape(-1, 2).copy()).cuda()
-    got = gh.gpu_verify(stats_dev, 2, cu, np.zeros(6, np.int32), 3, with_target_ids=False)
-    exp = oracle.greedy_verify(stats_np, 2, cu, np.zeros(6, np.int32), 3)
+    got = gh.gpu_verify(stats_dev, num_shards, cu, np.zeros(6, np.int32), 3, with_target_ids=False)
+    exp = oracle.greedy_verify(stats_np, num_shards, cu, np.zeros(6, np.int32), 3)
     assert (got["sampled"] == exp["sampled"]).all()
     assert (got["target_ids"] == -99).all()   # untouched
 
 
-def test_k_above_max_k_sets_error_word(sga_lib):
+@pytest.mark.parametrize("num_shards", [1, 33])
+def test_k_above_max_k_sets_error_word(sga_lib, num_shards):
     sga_lib.sga_clear_device_error()
     rng = np.random.default_rng(6)
     cu = np.array([0, 2, 6, 7], np.int32)   # request 1 has K = 4 > max_k = 3
-    stats_np, _, _ = random_stats(rng, 10, 1, 50)
+    stats_np, _, _ = random_stats(rng, 10, num_shards, 50)
     stats_dev = torch.from_numpy(stats_np.view(np.int32).reshape(-1, 2).copy()).cuda()
-    got = gh.gpu_verify(stats_dev, 1, cu, np.zeros(7, np.int32), 3)
+    got = gh.gpu_verify(stats_dev, num_shards, cu, np.zeros(7, np.int32), 3)
     assert sga_lib.sga_device_error() & sga_lib.SGA_DEVERR_K_RANGE
     assert got["num_sampled"][1] == 0 and got["bonus"][1] == -1 and (got["sampled"][1] == -1).all()
     assert got["num_sampled"][0] >= 1 and got["num_sampled"][2] >= 1
