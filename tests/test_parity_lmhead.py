@@ -93,10 +93,46 @@ def test_small_shapes(sga_lib, M, H, vocab, num_shards):
         check_rows(np.arange(M), hidden, weight, shards, org, st, v, i)
 
 
-def test_all_padding_shard_and_exact_one_hot(sga_lib):
+@pytest.mark.parametrize("M", [1, 2, 15, 16, 17, 31, 32, 33, 48, 63, 64, 65])
+def test_decode_sizes_around_kernel_boundaries(sga_lib, M):
+    # M <= 64 runs the swapped-operand decode kernel with N = 16, 32 or 64
+    # hidden columns; 65 is the first size of the 1-SM kernel.  A ragged
+    # vocab (not a multiple of 128 or 256), 3 uneven shards, and padding.
+    H, vocab = 256, 4099
+    hidden = wl.normal_matrix(900 + M, M, H, 1.0)
+    weight = wl.normal_matrix(901 + M, vocab, H, 1.0 / np.sqrt(H))
+    shards = wl.random_shards(M, vocab, 3)
+    for org in (vocab, shards[1][0] + 5):
+        st, v, i = run_gpu(hidden, weight, shards, org)
+        check_rows(np.arange(M), hidden, weight, shards, org, st, v, i)
+
+
+@pytest.mark.parametrize("M,H", [(8, 192), (40, 64), (3, 320)])
+def test_decode_sizes_odd_number_of_k_blocks(sga_lib, M, H):
+    # H / 64 odd: the last pipeline stage of a two-K-block ring holds one block
+    vocab = 1500
+    hidden = wl.normal_matrix(40 + M, M, H, 1.0)
+    weight = wl.normal_matrix(41 + M, vocab, H, 1.0 / np.sqrt(H))
+    shards = wl.even_shards(vocab, 2)
+    st, v, i = run_gpu(hidden, weight, shards, vocab)
+    check_rows(np.arange(M), hidden, weight, shards, vocab, st, v, i)
+
+
+def test_decode_size_vocab_narrower_than_a_tile(sga_lib):
+    # one shard of 100 ids: a single 256-id tile, one CTA, 156 ids of zero fill
+    M, H, vocab = 9, 128, 100
+    hidden = wl.normal_matrix(31, M, H, 1.0)
+    weight = wl.normal_matrix(32, vocab, H, 1.0 / np.sqrt(H))
+    st, v, i = run_gpu(hidden, weight, [(0, vocab)], vocab)
+    check_rows(np.arange(M), hidden, weight, [(0, vocab)], vocab, st, v, i)
+
+
+@pytest.mark.parametrize("M", [130, 40, 20, 5])
+def test_all_padding_shard_and_exact_one_hot(sga_lib, M):
     # one-hot weights: logit[r][j] = hidden[r][perm[j]] exactly, so ties and
-    # values are exact and the id must follow torch.argmax order
-    M, H, vocab = 130, 128, 600
+    # values are exact and the id must follow torch.argmax order (M <= 64:
+    # decode kernel, where ties are resolved across lanes, warps and CTAs)
+    H, vocab = 128, 600
     hidden = wl.normal_matrix(7, M, H, 1.0)
     perm = np.random.default_rng(1).integers(0, H, vocab)
     weight = np.zeros((vocab, H), np.uint16)

@@ -78,6 +78,8 @@ def make(M, H, vocab, seed):
 @pytest.mark.parametrize("M,H,vocab,num_shards", [
     (1, 128, 300, 1), (100, 256, 1000, 2), (128, 512, 5000, 3), (300, 256, 2311, 4),
     (513, 1024, 4099, 2), (16, 4096, 20000, 2),
+    # decode kernel with 16, 32 and 64 hidden columns
+    (7, 256, 3001, 3), (33, 512, 3001, 2), (64, 256, 1000, 3), (5, 384, 2000, 2),
 ])
 def test_small_shapes(sga_lib, M, H, vocab, num_shards):
     hq, hs, wq, w_scale = make(M, H, vocab, M + H + vocab)
@@ -87,8 +89,9 @@ def test_small_shapes(sga_lib, M, H, vocab, num_shards):
         check(np.arange(M), hq, hs, wq, w_scale, shards, org, st, v, i)
 
 
-def test_no_row_scales_and_nan_code(sga_lib):
-    M, H, vocab = 200, 256, 700
+@pytest.mark.parametrize("M", [200, 40, 12])
+def test_no_row_scales_and_nan_code(sga_lib, M):
+    H, vocab = 256, 700
     hq, _, wq, w_scale = make(M, H, vocab, 9)
     wq = wq.copy()
     wq[333, 17] = 0x7F                                 # E4M3 NaN in weight row 333
