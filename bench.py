@@ -531,6 +531,27 @@ LMHEAD_METRIC_FP8 = "fused fp8 LM-head + argmax rows/s and TFLOP/s (frac of fp8 
 FP8_TO_BF16_NOMINAL = 4.5 / 2.25   # dense tensor peaks, PFLOP/s per GPU
 
 
+DECODE_MAX_M = 64   # the library's decode-size LM-head kernel covers M <= 64
+
+
+def decode_roofline(weight_bytes, kern_ms, num_shards, fp8):
+    """HBM roofline of the decode-size LM-head kernel: the weight is read once
+    per step (one launch per shard)."""
+    pk, pk_src = peaks()
+    hbm = float(pk.get("hbm_gbs", FALLBACK_HBM_GBS))
+    achieved = weight_bytes / (kern_ms * 1e-3) / 1e9
+    traffic = ncu_traffic("lmhead_decode.md", ["greedy_spec_decode_gb300/csrc/lmhead.cu",
+                                               "greedy_spec_decode_gb300/csrc/common.cuh"])
+    return {"bound": "hbm",
+            "kernel": "lmhead_argmax_decode_kernel<%s>" % ("fp8" if fp8 else "bf16"),
+            "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+            "traffic": None if (traffic is None or fp8) else traffic,
+            "traffic_unit": "DRAM bytes per launch (one shard), bf16 M = 16 capture",
+            "peak_source": f"{pk_src} hbm_gbs (MEASURED_PEAKS.json copy bandwidth)"
+            if pk_src == "measured" else "fallback 6.8 TB/s",
+            "bytes_per_step": weight_bytes, "launches_per_step": num_shards}
+
+
 def run_ours_lmhead(args, fp8=False):
     """Fused LM-head + argmax: 512 rows, hidden 4096, vocab 151936 in 2 shards;
     one step = sga_lmhead_argmax (or its fp8 variant) per shard +
@@ -604,6 +625,10 @@ def run_ours_lmhead(args, fp8=False):
         burst *= FP8_TO_BF16_NOMINAL
     achieved = flops / (kern_ms * 1e-3) / 1e12
     assert sga.sga_device_error() == 0, "device error word set during the bench"
+    # M <= 64 runs the decode-size kernel: a weight stream bound by HBM, not
+    # by the tensor cores (2 M flops per weight element)
+    decode = M <= DECODE_MAX_M
+    weight_bytes = weight.numel() * weight.element_size()
 
     # end to end: hidden states in from pinned host memory, ids back
     hid_h = (torch.from_numpy(c["hidden"]) if fp8 else
@@ -637,7 +662,8 @@ def run_ours_lmhead(args, fp8=False):
         "weight_gbs": weight.numel() * weight.element_size() / (kern_ms * 1e-3) / 1e9,
         "kernel_us": {"lmhead_argmax_per_step": round(kern_ms * 1e3, 2),
                       "reduce_and_gaps": round((step_ms - kern_ms) * 1e3, 2)},
-        "roofline": {"bound": "tensor",
+        "roofline": decode_roofline(weight_bytes, kern_ms, S, fp8) if decode else
+                    {"bound": "tensor",
                      "kernel": "lmhead_argmax_2sm_kernel<fp8>" if fp8 else "lmhead_argmax_2sm_kernel",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,

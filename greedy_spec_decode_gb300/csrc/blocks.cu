@@ -21,13 +21,13 @@
 // draft rows and its bonus row, read from two entries of cu_num_draft, so no
 // warp ever searches for the kind of its row) or, without cu_num_draft, 16
 // draft rows.  The group's real pieces (K_i x draft count + bonus count) are
-// dealt round-robin to the parts x 8 warps of the group; a warp streams its
+// dealt round-robin to the parts x 4 warps of the group; a warp streams its
 // piece with 16-byte loads, kUnroll in flight per lane, keeps the best
 // vector in registers (the steps of the per-shard kernel), merges across
 // the warp and stores one stat.  The empty slots (all but a few of a draft
 // row's slots when the bonus block is the smaller one) are plain stores,
 // spread over every thread of the group.  Parts are chosen so that the grid
-// fills the GPU about four CTAs deep.  A piece is at most one block (8192 ids
+// is one wave of resident CTAs.  A piece is at most one block (8192 ids
 // = 16 KB of bf16): too short for the per-shard kernel's bulk-copy ring.
 #include "common.cuh"
 #include "scan.cuh"
