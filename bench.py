@@ -52,8 +52,13 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--graph", action="store_true",
+                   help="lmhead workloads: replay each step from a CUDA graph and time the "
+                        "whole step (no per-launch events)")
     p.add_argument("--lmhead-rows", type=int, default=512,
                    help="rows (hidden states) of the fused LM-head workload")
+    p.add_argument("--lmhead-shards", type=int, default=2,
+                   help="vocab shards (emulated TP ranks) of the fused LM-head workload")
     p.add_argument("--lmhead-vocab", type=int, default=151936,
                    help="vocab of the fused LM-head workload (smaller for profiling)")
     p.add_argument("--rows", type=int, default=None,
@@ -567,12 +572,14 @@ def run_ours_lmhead(args, fp8=False):
     import greedy_spec_decode_gb300 as sga
 
     if fp8:
-        c = wl.fused_lmhead_fp8(m=args.lmhead_rows, vocab=args.lmhead_vocab)
+        c = wl.fused_lmhead_fp8(m=args.lmhead_rows, vocab=args.lmhead_vocab,
+                                num_shards=args.lmhead_shards)
         hidden = torch.from_numpy(c["hidden"]).cuda()
         weight = torch.from_numpy(c["weight"]).cuda()
         hscale = torch.from_numpy(c["hidden_scale"]).cuda()
     else:
-        c = wl.fused_lmhead(m=args.lmhead_rows, vocab=args.lmhead_vocab)
+        c = wl.fused_lmhead(m=args.lmhead_rows, vocab=args.lmhead_vocab,
+                            num_shards=args.lmhead_shards)
         hidden = torch.from_numpy(c["hidden"].view(np.int16)).view(torch.bfloat16).cuda()
         weight = torch.from_numpy(c["weight"].view(np.int16)).view(torch.bfloat16).cuda()
     M, H = hidden.shape
@@ -601,6 +608,16 @@ def run_ours_lmhead(args, fp8=False):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    graph = None
+    if args.graph:
+        # the whole step replayed from one CUDA graph, as a serving engine
+        # replays a decode step: no host submission gaps between launches
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
     barrier(world)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * S)] for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -608,14 +625,21 @@ def run_ours_lmhead(args, fp8=False):
     time.sleep(0.3)
     start.record()
     for i in range(args.steps):
-        step(ev[i])
+        if graph is not None:
+            graph.replay()
+        else:
+            step(ev[i])
     end.record()
     torch.cuda.synchronize()
     clocks = sampler.stop()
     barrier(world)
     total_ms = max_over_ranks(start.elapsed_time(end), world, "cuda")
     step_ms = total_ms / args.steps
-    kern_ms = sum(sum(e[2 * s].elapsed_time(e[2 * s + 1]) for s in range(S)) for e in ev) / args.steps
+    if graph is not None:
+        kern_ms = step_ms   # the step as a whole (LM-head launches + finalize + reduce)
+    else:
+        kern_ms = sum(sum(e[2 * s].elapsed_time(e[2 * s + 1]) for s in range(S))
+                      for e in ev) / args.steps
     flops = 2.0 * M * H * sum(w for _, w in shards)
     pk, pk_src = peaks()
     peak = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops", FALLBACK_BF16_TFLOPS)))
@@ -680,6 +704,8 @@ def run_ours_lmhead(args, fp8=False):
         "e2e": {"value": world * M / (e2e_ms * 1e-3), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": M * 4,
                 "ms_per_step": e2e_ms},
+        "timing": ("whole step replayed from a CUDA graph" if graph is not None else
+                   "CUDA events around each LM-head call (GEMM + finalize)"),
         "gpu_launches": args.steps * (2 * S + 1),
         "clocks": clocks,
     }

@@ -258,6 +258,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = sh->tmem_base;
+  // launched with programmatic stream serialisation: everything above (barrier
+  // set-up, TMEM allocation) overlaps the previous kernel's tail; inputs and
+  // the workspace are touched only after that kernel has completed
+  pdl_wait();
   const int total = m_tiles * n_tiles;
 
   int prod_stage = 0;
@@ -444,6 +448,7 @@ constexpr int dec_chunks = kN <= 16 ? SGA_LMHEAD_DEC_CHUNKS_N16 : SGA_LMHEAD_DEC
 template <int kN>
 constexpr int dec_halves = dec_chunks<kN> >= 2 ? 1 : 2;  // 128-id halves per tile
 constexpr int DEC_SUB_BYTES = 128 * ROW_BYTES;            // one 128-row x 128-byte box
+constexpr int kDecMaxParts = 256;  // CTAs (partials per row) of one decode launch, at most
 template <int kN>
 constexpr int dec_a_bytes = dec_chunks<kN> * dec_halves<kN> * DEC_SUB_BYTES;
 template <int kN>
@@ -614,6 +619,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = sh->tmem_base;
+  // launched with programmatic stream serialisation: everything above (barrier
+  // set-up, TMEM allocation) overlaps the previous kernel's tail; inputs and
+  // the workspace are touched only after that kernel has completed
+  pdl_wait();
 
   int prod_stage = 0;
   uint32_t prod_phase = 0;
@@ -949,6 +958,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
   tc_fence_after();
   const uint32_t tmem_base = sh->tmem_base;
+  // launched with programmatic stream serialisation: everything above (barrier
+  // set-up, TMEM allocation) overlaps the previous kernel's tail; inputs and
+  // the workspace are touched only after that kernel has completed
+  pdl_wait();
   const int total = m_pairs * n_tiles;
 
   int prod_stage = 0;
@@ -1121,6 +1134,7 @@ __global__ void lmhead_finalize_kernel(const sga_stat *__restrict__ ws, int M, i
                                        const float *__restrict__ row_scale, float w_scale,
                                        int scaled) {
   pdl_wait();  // the partials of the GEMM kernel are complete and visible
+  pdl_launch_dependents();  // the next kernel may start its prologue
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= M) return;
@@ -1247,6 +1261,24 @@ int resident_pairs(int num_sms) {
   return cache[dev];
 }
 
+// Launch a GEMM kernel (THREADS threads per CTA) with programmatic stream
+// serialisation; the kernel calls griddepcontrol.wait after its prologue.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), int grid, int smem, cudaStream_t stream,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 template <bool kFp8, int kN>
 cudaError_t launch_decode(const void *hidden, int64_t M, int64_t H, const void *weight,
                           int64_t shard_start, int64_t valid, sga_stat *ws, int n_tiles,
@@ -1258,16 +1290,17 @@ cudaError_t launch_decode(const void *hidden, int64_t M, int64_t H, const void *
   const int slot = 4 + (kFp8 ? 3 : 0) + (kN == 16 ? 0 : kN == 32 ? 1 : 2);
   cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), dec_smem_bytes<kN>, slot);
   if (e != cudaSuccess) return e;
-  // grid <= n_tiles (256-id tiles) keeps the partials within an M x n_tiles
-  // workspace even when the kernel's own tiles are 128 ids
-  const int grid = n_tiles < num_sms ? n_tiles : num_sms;
+  // one CTA per SM, at most one per tile; the workspace holds
+  // min(ceil(width / 128), kDecMaxParts) partials per row for M <= 64
+  (void)n_tiles;
   const int tile_ids = 128 * dec_halves<kN>;
   const int dec_tiles = static_cast<int>((valid + tile_ids - 1) / tile_ids);
-  kern<<<grid, THREADS, dec_smem_bytes<kN>, stream>>>(
-      map_w, map_h, static_cast<int>(M), static_cast<int>(H / kBk<kFp8>), dec_tiles,
-      static_cast<int>(valid), static_cast<int>(shard_start), ws, err);
+  int grid = dec_tiles < num_sms ? dec_tiles : num_sms;
+  if (grid > kDecMaxParts) grid = kDecMaxParts;
   *ws_stride = grid;
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dec_smem_bytes<kN>, stream, map_w, map_h, static_cast<int>(M),
+                    static_cast<int>(H / kBk<kFp8>), dec_tiles, static_cast<int>(valid),
+                    static_cast<int>(shard_start), ws, err);
 }
 
 // Partial statistics go to ws[row * (*ws_stride) + part]; *ws_stride <=
@@ -1303,10 +1336,9 @@ cudaError_t launch_gemm(const void *hidden, int64_t M, int64_t H, const void *we
     const int resident = resident_pairs<kFp8>(num_sms);
     if (resident <= 0) return cudaErrorLaunchOutOfResources;
     const int pairs = total < resident ? total : resident;
-    lmhead_argmax_2sm_kernel<kFp8><<<2 * pairs, THREADS, SMEM2_BYTES, stream>>>(
-        map_a, map_b, static_cast<int>(M), num_kb, m_pairs, n_tiles, static_cast<int>(valid),
-        static_cast<int>(shard_start), ws, err);
-    return cudaGetLastError();
+    return launch_pdl(lmhead_argmax_2sm_kernel<kFp8>, 2 * pairs, SMEM2_BYTES, stream, map_a,
+                      map_b, static_cast<int>(M), num_kb, m_pairs, n_tiles,
+                      static_cast<int>(valid), static_cast<int>(shard_start), ws, err);
   }
   CUtensorMap map_a, map_b;
   if (!make_map(&map_a, hidden, M, H, BM, kFp8) || !make_map(&map_b, weight, valid, H, BN, kFp8))
@@ -1317,10 +1349,9 @@ cudaError_t launch_gemm(const void *hidden, int64_t M, int64_t H, const void *we
   const int m_tiles = static_cast<int>((M + BM - 1) / BM);
   const int total = m_tiles * n_tiles;
   const int grid = total < num_sms ? total : num_sms;
-  lmhead_argmax_kernel<kFp8><<<grid, THREADS, SMEM_BYTES, stream>>>(
-      map_a, map_b, static_cast<int>(M), num_kb, m_tiles, n_tiles, static_cast<int>(valid),
-      static_cast<int>(shard_start), ws, err);
-  return cudaGetLastError();
+  return launch_pdl(lmhead_argmax_kernel<kFp8>, grid, SMEM_BYTES, stream, map_a, map_b,
+                    static_cast<int>(M), num_kb, m_tiles, n_tiles, static_cast<int>(valid),
+                    static_cast<int>(shard_start), ws, err);
 }
 
 }  // namespace
@@ -1331,9 +1362,17 @@ cudaError_t launch_selftest_timeout(unsigned long long limit_ns, uint32_t *err,
   return cudaGetLastError();
 }
 
+// Partials per row: one per 256-id tile, and for decode sizes at least one per
+// CTA of the decode kernel (up to kDecMaxParts), so that narrow shards still
+// spread over every SM.  For M <= 64 the extra is at most 128 KB.
 size_t lmhead_workspace_bytes(int64_t M, int64_t width) {
-  const int64_t n_tiles = (width + BN - 1) / BN;
-  return static_cast<size_t>(n_tiles * M) * sizeof(sga_stat);
+  int64_t parts = (width + BN - 1) / BN;
+  if (M <= SGA_LMHEAD_DECODE_MAX_M) {
+    int64_t dec = (width + 127) / 128;
+    if (dec > kDecMaxParts) dec = kDecMaxParts;
+    if (dec > parts) parts = dec;
+  }
+  return static_cast<size_t>(parts * M) * sizeof(sga_stat);
 }
 
 cudaError_t launch_lmhead_argmax(const void *hidden, int64_t M, int64_t H, const void *weight,
