@@ -124,6 +124,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
+// Bring one box of a tensor into L2 (no shared-memory destination, no
+// completion to wait for).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -437,6 +446,12 @@ __global__ void __launch_bounds__(THREADS, 1)
 //   N = 32, 64:       1 chunk 203-208 / 117-122 us, 2 chunks 196-200 /
 //                     110-115, 4 chunks 201-206 / 115-119 (only 2 stages)
 // Longer contiguous runs per weight row pay more than extra bytes in flight.
+#ifndef SGA_LMHEAD_DEC_PREFETCH
+// L2 prefetch of the first stages before the PDL wait.  Measured (graph
+// replay, 8 shards of 18992 ids): bf16 M = 1 223.7 -> 219.7 us per step, fp8
+// 137.6 -> 133.2 us; 2 shards of 75968 ids unchanged.
+#define SGA_LMHEAD_DEC_PREFETCH 1
+#endif
 #ifndef SGA_LMHEAD_DEC_CHUNKS_N16
 #define SGA_LMHEAD_DEC_CHUNKS_N16 4
 #endif
@@ -593,6 +608,17 @@ __global__ void __launch_bounds__(THREADS, 1)
   const volatile int *abort_flag = &sh->abort;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+
+  if (SGA_LMHEAD_DEC_PREFETCH && threadIdx.x == 64 && blockIdx.x < n_tiles) {
+    // Warm L2 with what the ring loads first (this CTA's first tile, one
+    // ring's worth of K blocks) while the previous kernel drains.  A prefetch
+    // only moves lines into L2, which stays coherent with any later write, so
+    // it may precede griddepcontrol.wait.
+    const int n = blockIdx.x;
+    for (int kb = 0; kb < num_kb && kb < kStages * kChunks; ++kb)
+      for (int h = 0; h < kHalves; ++h)
+        tma_prefetch_2d(&tmap_w, kb * kBk<kFp8>, n * kTileIds + h * 128);
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
