@@ -26,6 +26,12 @@ static int host_checks(void) {
   if (sga_status_string(SGA_ERR_SHARD) == 0 || strlen(sga_status_string(SGA_ERR_SHARD)) == 0)
     bad |= 16;
   if (sizeof(sga_stat) != 8) bad |= 32;
+  /* block-granular statistics: slot count is host arithmetic; a zero block
+   * size is rejected before any CUDA call */
+  if (sga_block_slots(67350, 67349, 8192, 1024) != 67) bad |= 64;
+  if (sga_local_argmax_blocks((const void *)0x10000, SGA_BF16, 4, 100, 0, 100, 100, 0, 16, 0, 0,
+                              (sga_stat *)0x10000, 0) != SGA_ERR_SIZE)
+    bad |= 64;
   return bad;
 }
 
