@@ -155,3 +155,39 @@ def test_fused_lmhead_workload_sampled_rows(sga_lib):
     checked, excluded = check_rows(rows, c["hidden"], c["weight"], c["shards"],
                                    c["org_vocab"], st, v, i)
     assert checked >= len(rows) - 3, (checked, excluded)
+
+
+@pytest.mark.parametrize("M_req,K,H,vocab,num_shards", [(6, 3, 256, 5000, 3), (40, 1, 128, 3001, 2)])
+def test_lmhead_stats_feed_greedy_verify(sga_lib, M_req, K, H, vocab, num_shards):
+    # the whole target side from hidden states: fused LM-head argmax per shard
+    # (stats gathered shard-major) -> fused greedy verify.  Each row gets a
+    # planted winner (its weight row is the row's own hidden vector, so its
+    # logit |h|^2 ~ H beats every other by a wide margin); the expected
+    # tokens are then exact and the verify outputs must match the oracle's
+    import greedy_spec_decode_gb300 as sga
+    rows = M_req * (K + 1)
+    rng = np.random.default_rng(rows + vocab)
+    hidden = wl.normal_matrix(rows + 1, rows, H, 1.0)
+    weight = wl.normal_matrix(rows + 2, vocab, H, 1.0 / np.sqrt(H))
+    planted = rng.choice(vocab, rows, replace=False).astype(np.int32)
+    weight[planted] = hidden
+    shards = wl.random_shards(rows, vocab, num_shards)
+    st, _, ids = run_gpu(hidden, weight, shards, vocab)
+    logits = oracle.lmhead_logits(hidden, weight, np.arange(rows))
+    top1, top2, exp_ids = oracle.argmax_f64(logits, 0, vocab)
+    assert (top1 - top2 > 1.0).all() and (exp_ids == planted).all()
+    assert (ids == planted).all()
+    cu = np.arange(M_req + 1, dtype=np.int32) * K
+    flags = rng.random(M_req * K) < 0.7
+    drafts = wl.compose_drafts(planted, cu, flags, rng.integers(0, vocab, M_req * K).astype(np.int32))
+    stats_dev = torch.from_numpy(st.view(np.int32).reshape(-1, 2).copy()).cuda()
+    got = gh.gpu_verify(stats_dev, num_shards, cu, drafts, K)
+    oracle_stats = np.zeros(num_shards * rows, oracle.STAT)
+    for s, (o, w) in enumerate(shards):
+        s1, _, sid = oracle.argmax_f64(logits[:, o:o + w], o, vocab)
+        oracle_stats["v"][s * rows:(s + 1) * rows] = s1
+        oracle_stats["id"][s * rows:(s + 1) * rows] = sid
+    ref = oracle.greedy_verify(oracle_stats, num_shards, cu, drafts, K)
+    for key in ("sampled", "num_sampled", "num_rejected", "bonus", "target_ids"):
+        assert (got[key] == ref[key]).all(), key
+    assert sga.sga_device_error() == 0
