@@ -38,7 +38,7 @@ def _worker(rank, world, port, out_dir):
     got = bench.max_over_ranks(1.5 + rank, world, "cpu")
 
     class Args:
-        steps, warmup, gpus = 2, 1, world
+        steps, warmup, gpus, workload = 2, 1, world, "large_verify"
     buf = io.StringIO()
     with redirect_stdout(buf):
         rc = bench.run_reference(Args, lambda: wl.large_verify(rows_limit=48))
