@@ -51,8 +51,12 @@ constexpr int kBk = kFp8 ? 128 : 64;
 #define SGA_LMHEAD_2SM_MIN_M 129
 #endif
 #ifndef SGA_LMHEAD_DECODE_MAX_M
-#define SGA_LMHEAD_DECODE_MAX_M 64  // swapped-operand decode kernel for M <= this (0: off)
+// Swapped-operand decode kernel for M <= this (0: off; at most 64).  Measured:
+// an N = 128 variant for M = 65..128 was slower than the 1-SM kernel (graph
+// replay, 2 shards: M = 128 bf16 210 vs 201 us, fp8 122 vs 114 us).
+#define SGA_LMHEAD_DECODE_MAX_M 64
 #endif
+static_assert(SGA_LMHEAD_DECODE_MAX_M <= 64, "the decode kernel holds at most 64 hidden rows");
 constexpr int STAGES = SGA_LMHEAD_STAGES;
 constexpr int A_BYTES = BM * ROW_BYTES;   // 16 KB
 constexpr int B_BYTES = BN * ROW_BYTES;   // 32 KB
@@ -755,15 +759,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int32_t id = live ? shard_start + local : kNoId;
         const uint32_t taddr =
             tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + (acc * kHalves + h) * kN;
-        uint32_t r[kN];
-        tmem_ld_cols<kN>(taddr, r);
-        tmem_ld_wait();
 #pragma unroll
         for (int g = 0; g < kSlots; ++g) {
+          uint32_t r[kG];  // one group of columns at a time
+          tmem_ld_cols<kG>(taddr + g * kG, r);
+          tmem_ld_wait();
           float x[kG];
 #pragma unroll
           for (int k = 0; k < kG; ++k)
-            x[k] = live ? __uint_as_float(r[g * kG + k]) : __int_as_float(0xff800000);
+            x[k] = live ? __uint_as_float(r[k]) : __int_as_float(0xff800000);
           float v;
           int32_t i;
           rows_argmax<kG>(x, id, lane, v, i);
@@ -1249,7 +1253,7 @@ bool make_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, int
 // no function-attribute call.
 cudaError_t set_smem_once(const void *kernel, int bytes, int slot) {
   static std::mutex mu;
-  static bool done[10][64] = {};
+  static bool done[12][64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -1313,7 +1317,7 @@ cudaError_t launch_decode(const void *hidden, int64_t M, int64_t H, const void *
   if (!make_map(&map_w, weight, valid, H, 128, kFp8) || !make_map(&map_h, hidden, M, H, kN, kFp8))
     return cudaErrorInvalidValue;
   auto kern = lmhead_argmax_decode_kernel<kFp8, kN>;
-  const int slot = 4 + (kFp8 ? 3 : 0) + (kN == 16 ? 0 : kN == 32 ? 1 : 2);
+  const int slot = 4 + (kFp8 ? 4 : 0) + (kN == 16 ? 0 : kN == 32 ? 1 : kN == 64 ? 2 : 3);
   cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), dec_smem_bytes<kN>, slot);
   if (e != cudaSuccess) return e;
   // one CTA per SM, at most one per tile; the workspace holds
