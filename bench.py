@@ -384,14 +384,14 @@ def cpu_baseline(c, target_seconds):
     drafts = oracle_drafts(oracle, x, shards, org, cu, c["flags"], c["rand_ids"])
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle_verify_step(oracle, x, shards, org, cu, drafts, k)
+        out = oracle_verify_step(oracle, x, shards, org, cu, drafts, k)
         reps += 1
         el = time.perf_counter() - t0
         if el >= target_seconds or reps >= 500:
             break
     rows = x.shape[0]
     return {"value": rows * reps / el, "unit": "rows/s", "cores": oracle.num_threads(),
-            "kind": "oracle",
+            "kind": "oracle", "_drafts": drafts, "_outputs": out,
             "sample": f"the whole workload ({rows} rows x {x.shape[1]} bf16 logits, "
                       f"{len(shards)} shard argmaxes + verify of {cu.size - 1} requests) "
                       f"repeated {reps} times in {el:.1f} s"}
@@ -527,7 +527,19 @@ def run_ours_verify(args, blocks=None):
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(c, args.cpu_seconds)
+        base = cpu_baseline(c, args.cpu_seconds)
+        # the baseline leg ran the oracle on the whole workload: recheck the
+        # timed device outputs against it, bit for bit
+        exp, exp_drafts = base.pop("_outputs"), base.pop("_drafts")
+        got = {"sampled": path.sampled, "num_sampled": path.num_sampled,
+               "num_rejected": path.num_rejected, "bonus": path.bonus}
+        same = bool((exp_drafts == path.drafts_host).all()) and all(
+            bool((v.cpu().numpy() == exp[key]).all()) for key, v in got.items())
+        if not same:
+            raise SystemExit("timed outputs differ from the oracle: no number is reported")
+        line["parity"] = ("timed outputs (sampled, num_sampled, num_rejected, bonus) and the "
+                          "drafts bit-exact with the oracle of the cpu_baseline leg")
+        line["cpu_baseline"] = base
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
