@@ -555,6 +555,42 @@ LMHEAD_METRIC_FP8 = "fused fp8 LM-head + argmax rows/s and TFLOP/s (frac of fp8 
 FP8_TO_BF16_NOMINAL = 4.5 / 2.25   # dense tensor peaks, PFLOP/s per GPU
 
 
+def lmhead_cpu_baseline(c, fp8, gpu_ids, target_seconds):
+    """The oracle's fp64 LM-head logits + argmax on a bounded sample of rows
+    (whole vocabulary, every shard), timed; the same rows of the device path's
+    ids are checked against it within the LM-head tolerance (ids equal where
+    the top-1 / top-2 gap exceeds 1e-2, else a near-winner)."""
+    import oracle
+    M = c["hidden"].shape[0]
+    org = c["org_vocab"]
+    rows_done, checked, t0 = 0, 0, time.perf_counter()
+    while rows_done < M:
+        sel = np.arange(rows_done, min(M, rows_done + 2), dtype=np.int64)
+        if fp8:
+            logits = oracle.lmhead_logits_fp8(c["hidden"], c["hidden_scale"], c["weight"],
+                                              c["weight_scale"], sel)
+        else:
+            logits = oracle.lmhead_logits(c["hidden"], c["weight"], sel)
+        top1, top2, exp = oracle.argmax_f64(logits, 0, org)
+        for q, r in enumerate(sel):
+            g = int(gpu_ids[r])
+            ok = g == exp[q] if top1[q] - top2[q] > 1e-2 else logits[q, g] >= top1[q] - 1e-2
+            if not ok:
+                raise SystemExit(f"LM-head row {r}: device id {g}, oracle {exp[q]}: no number is "
+                                 "reported")
+            checked += 1
+        rows_done += sel.size
+        if time.perf_counter() - t0 >= target_seconds:
+            break
+    el = time.perf_counter() - t0
+    base = {"value": rows_done / el, "unit": "rows/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"the first {rows_done} of {M} rows, fp64 logits over all "
+                      f"{c['weight'].shape[0]} ids ({el:.1f} s)"}
+    return base, (f"ids of {checked} sampled rows within the LM-head tolerance of the oracle "
+                  "of the cpu_baseline leg")
+
+
 DECODE_MAX_M = 64   # the library's decode-size LM-head kernel covers M <= 64
 
 
@@ -728,6 +764,9 @@ def run_ours_lmhead(args, fp8=False):
         "gpu_launches": args.steps * (2 * S + 1),
         "clocks": clocks,
     }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"], line["parity"] = lmhead_cpu_baseline(
+            c, fp8, ids.cpu().numpy(), args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
