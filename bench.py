@@ -775,6 +775,47 @@ def run_ours_lmhead(args, fp8=False):
     return 0
 
 
+def small_cpu_baseline(c, stats, outs, drafts, target_seconds):
+    """The oracle on the whole small workload, repeated for about
+    target_seconds and timed; the device path's statistics and results are
+    checked against it bit for bit (no number on a mismatch)."""
+    import oracle
+    x, shards, org = c["logits"], c["shards"], c["org_vocab"]
+    S, rows = len(shards), c["logits"].shape[0]
+    verify = drafts is not None
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        st = oracle.gathered_stats(x, shards, org)
+        if verify:
+            exp = oracle.greedy_verify(st, S, c["cu_num_draft"], drafts, c["k"])
+        else:
+            _, exp_ids = oracle.shard_reduce(st, S, rows)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= target_seconds or reps >= 2000:
+            break
+    got_st = stats.cpu().numpy().view(oracle.STAT).reshape(-1)
+    same = bool((got_st["id"] == st["id"]).all()
+                and (got_st["v"].view(np.uint32) == st["v"].view(np.uint32)).all())
+    if verify:
+        names = ("sampled", "num_sampled", "num_rejected", "bonus")
+        same = same and all(bool((o.cpu().numpy() == exp[k]).all()) for k, o in zip(names, outs))
+        # the drafts copy the device path's own argmax: they must be the oracle's
+        _, t = oracle.shard_reduce(st, S, rows)
+        same = same and bool((wl.compose_drafts(t, c["cu_num_draft"], c["flags"],
+                                                c["rand_ids"]) == drafts).all())
+    else:
+        same = same and bool((outs.cpu().numpy() == exp_ids).all())
+    if not same:
+        raise SystemExit("timed outputs differ from the oracle: no number is reported")
+    base = {"value": rows * reps / el, "unit": "rows/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"the whole workload ({rows} rows, {S} shards) repeated {reps} times "
+                      f"in {el:.1f} s"}
+    return base, ("timed statistics and results bit-exact with the oracle of the "
+                  "cpu_baseline leg")
+
+
 def run_ours_small(args, builder):
     """L2-resident workloads (draft get_top_tokens, small greedy verify): one
     step = the one-launch shard argmax + the reduce (no drafts) or the fused
@@ -859,6 +900,35 @@ def run_ours_small(args, builder):
         "gpu_launches": args.steps * 2,
         "clocks": clocks,
     }
+    # end to end through the same calls with host buffers: logits (and the
+    # drafts) in from pinned memory, the step's results back
+    logits_h = torch.from_numpy(x_np.view(np.int16) if x_np.dtype == np.uint16 else x_np).pin_memory()
+    x_raw = x.view(torch.int16) if x_np.dtype == np.uint16 else x
+    outs_d = outs if verify else [ids]
+    outs_h = [torch.empty(t_.shape, dtype=t_.dtype).pin_memory() for t_ in outs_d]
+    drafts_h = torch.from_numpy(drafts.cpu().numpy()).pin_memory() if verify else None
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(1, args.e2e_steps)
+    e0.record()
+    for _ in range(e2e_steps):
+        x_raw.copy_(logits_h, non_blocking=True)
+        if verify:
+            drafts.copy_(drafts_h, non_blocking=True)
+        step()
+        for h_, d_ in zip(outs_h, outs_d):
+            h_.copy_(d_, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, "cuda")
+    line["e2e"] = {"value": world * rows / (e2e_ms * 1e-3), "unit": "rows/s",
+                   "h2d_bytes_per_step": logits_h.numel() * logits_h.element_size()
+                   + (drafts_h.numel() * 4 if verify else 0),
+                   "d2h_bytes_per_step": sum(h_.numel() * 4 for h_ in outs_h),
+                   "ms_per_step": e2e_ms}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"], line["parity"] = small_cpu_baseline(
+            c, stats, outs if verify else ids, drafts.cpu().numpy() if verify else None,
+            args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
