@@ -230,7 +230,7 @@ class VerifyPath:
         self.num_sampled = torch.empty(self.n, **i32)
         self.num_rejected = torch.empty(self.n, **i32)
         self.bonus = torch.empty(self.n, **i32)
-        self.launches_per_step = 1 + (len(self.shards) if blocks else 1)
+        self.launches_per_step = 2
         elt = 2
         self.argmax_bytes = [self.rows * (w * elt + 8 * n) for (_, w), n in zip(self.shards, self.slots)]
         self.step_bytes = (sum(self.argmax_bytes) + 8 * self.n_stats * self.rows
@@ -238,12 +238,14 @@ class VerifyPath:
                            + 4 * self.n * (self.k + 1) + 12 * self.n)
 
     def run_argmax(self, events=None):
-        """All shards of this GPU in one launch (sga_local_argmax_shards), or
-        with block stats one sga_local_argmax_blocks launch per shard."""
+        """All shards of this GPU in one launch (sga_local_argmax_shards, or
+        sga_local_argmax_blocks_shards for block statistics)."""
         if events is not None:
             events[0].record()
         if self.blocks:
-            self.run_argmax_per_shard()
+            self.sga.sga_local_argmax_blocks_shards(
+                self.x, self.shards, self.org, self.blocks[0], self.stats,
+                bonus_block=self.blocks[1], cu_num_draft=self.cu)
         else:
             self.sga.sga_local_argmax_shards(self.x, self.shards, self.org, self.stats)
         if events is not None:
@@ -482,7 +484,7 @@ def run_ours_verify(args, blocks=None):
                           ["greedy_spec_decode_gb300/csrc/" + kernel_src,
                            "greedy_spec_decode_gb300/csrc/scan.cuh",
                            "greedy_spec_decode_gb300/csrc/common.cuh"])  # device code only
-    # (the block-stats profile records the DRAM bytes of one step's launches, one per shard)
+    # (the block-stats profile records the DRAM bytes of the one-launch step)
     e2e_ms, h2d, d2h = time_e2e(path, c, args.e2e_steps, torch)
     e2e_ms = max_over_ranks(e2e_ms, world, "cuda")
 
@@ -512,9 +514,10 @@ def run_ours_verify(args, blocks=None):
                               "the argmax tail (programmatic dependent launch)"},
         "per_shard_launches": {"ms_per_step": per_shard_ms,
                                "rows_per_s": world * path.rows / (per_shard_ms * 1e-3),
-                               "note": "same step with one sga_local_argmax launch per shard"},
+                               "note": "same step with one launch per shard (sga_local_argmax"
+                                       + ("_blocks" if blocks else "") + ")"},
         "roofline": {"bound": "hbm",
-                     "kernel": ("block_argmax_kernel<bf16> (one launch per shard, summed)" if blocks
+                     "kernel": ("block_argmax_kernel<bf16> (all shards, one launch)" if blocks
                                 else "local_argmax_kernel<bf16> (all shards, one launch)"),
                      "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": traffic,

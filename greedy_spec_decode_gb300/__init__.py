@@ -56,6 +56,8 @@ def lib():
             "sga_block_slots": ([i64, i64, i64, i64], i64),
             "sga_local_argmax_blocks": ([vp, i32, i64, i64, i64, i64, i64, i64, i64, i32, vp,
                                          vp, vp], i32),
+            "sga_local_argmax_blocks_shards": ([vp, i32, i64, i64, i32, vp, vp, i64, i64, i64,
+                                                i32, vp, vp, vp], i32),
             "sga_shard_reduce": ([vp, i32, i64, vp, vp, vp, i64, vp], i32),
             "sga_greedy_verify": ([vp, i32, i32, vp, vp, i32, vp, vp, vp, vp, vp, vp], i32),
             "sga_lmhead_argmax_workspace": ([i64, i64], sz),
@@ -176,6 +178,28 @@ def sga_local_argmax_blocks(logits, shard_start, shard_width, org_vocab, draft_b
     _check("sga_local_argmax_blocks", lib().sga_local_argmax_blocks(
         _ptr(logits), _dtype_code(logits), rows, ld, int(shard_start), int(shard_width),
         int(org_vocab), int(draft_block), int(bonus_block), int(num_reqs), _ptr(cu_num_draft),
+        _ptr(out_stats), _stream(stream)))
+    return out_stats
+
+
+def sga_local_argmax_blocks_shards(logits, shards, org_vocab, draft_block, out_stats,
+                                   bonus_block=None, cu_num_draft=None, stream=None):
+    """Block-granular stats of several shards in one launch.  `logits` is a
+    2-D CUDA tensor whose column 0 is global id shards[0][0]; shards =
+    [(start, width), ...] ascending; out_stats receives the shards' slots
+    concatenated in shard order (see sga_block_slots), piece-major."""
+    if logits.dim() != 2 or (logits.size(1) > 1 and logits.stride(1) != 1):
+        raise ValueError("logits must be 2-D with unit stride along the vocab")
+    bonus_block = draft_block if bonus_block is None else bonus_block
+    n = len(shards)
+    starts = (ctypes.c_int64 * n)(*[int(o) for o, _ in shards])
+    widths = (ctypes.c_int64 * n)(*[int(w) for _, w in shards])
+    rows = logits.size(0)
+    ld = logits.stride(0) if rows > 1 else max(logits.stride(0), logits.size(1))
+    num_reqs = 0 if cu_num_draft is None else cu_num_draft.numel() - 1
+    _check("sga_local_argmax_blocks_shards", lib().sga_local_argmax_blocks_shards(
+        _ptr(logits), _dtype_code(logits), rows, ld, n, starts, widths, int(org_vocab),
+        int(draft_block), int(bonus_block), int(num_reqs), _ptr(cu_num_draft),
         _ptr(out_stats), _stream(stream)))
     return out_stats
 

@@ -57,6 +57,18 @@ constexpr int kWarpsPerCta = SGA_BLOCKS_WARPS;
 constexpr int kUnroll = SGA_BLOCKS_UNROLL;
 constexpr int kGroupRows = 16;   // rows per group without a request layout
 
+// The shards of one launch: shard s covers global ids [start, start + width),
+// held at column col of `logits`, and owns the slots slot0 .. slot0 + slots - 1
+// of every row in the gathered statistics.
+struct BlockShardTable {
+  int n;
+  int32_t start[kMaxBlockShards];
+  int32_t col[kMaxBlockShards];
+  int32_t width[kMaxBlockShards];
+  int32_t slot0[kMaxBlockShards];
+  int32_t slots[kMaxBlockShards];
+};
+
 // Argmax (value, global id) of the non-padding ids [lo, hi) of row r, the
 // shard's column 0 being global id shard_start; computed by the whole warp,
 // every lane returns the result.  hi <= lo: no element, (-inf, lo).
@@ -126,16 +138,21 @@ __device__ __forceinline__ sga_stat piece_argmax(const char *__restrict__ row, i
   return st;
 }
 
-// grid.x = groups x parts; CTA b: group b / parts, part b % parts.  Ids and
-// block sizes are below 2^24 + 1 and a group's pieces below 2^31, so the
-// per-piece arithmetic is 32-bit.
+// grid.x = groups x parts; CTA b: group b / parts, part b % parts.  The
+// shards of the table are processed in one launch: a group's real pieces are
+// numbered shard by shard (then row, then piece), so consecutive items still
+// stream consecutive memory.  Ids and block sizes are below 2^24 + 1 and a
+// group's pieces below 2^31, so the per-piece arithmetic is 32-bit.
 template <bool kBf16>
 __global__ void __launch_bounds__(kWarpsPerCta * 32)
     block_argmax_kernel(const char *__restrict__ logits, int64_t ld_bytes, int64_t rows,
-                        int32_t shard_start, int32_t shard_width, int32_t org_vocab,
-                        int32_t draft_block, int32_t bonus_block, int32_t n_slots, int parts,
+                        const __grid_constant__ BlockShardTable tab, int32_t org_vocab,
+                        int32_t draft_block, int32_t bonus_block, int parts,
                         const int32_t *__restrict__ cu, sga_stat *__restrict__ out,
                         uint32_t *err) {
+  constexpr int kElt = kBf16 ? 2 : 4;
+  __shared__ int32_t cnt_d[kMaxBlockShards], cnt_b[kMaxBlockShards];
+  __shared__ int32_t item0[kMaxBlockShards + 1], empty0[kMaxBlockShards + 1];
   pdl_wait();
   const int g = static_cast<int>(blockIdx.x / parts);
   const int part = static_cast<int>(blockIdx.x % parts);
@@ -150,55 +167,83 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
     n_bonus = 1;
     if (c1 < c0 || c0 < 0 || first + n_draft >= rows) {
       if (part == 0 && threadIdx.x == 0) atomicOr(err, SGA_DEVERR_LAYOUT);
-      return;
+      return;  // CTA-uniform: before any barrier
     }
   } else {
     first = static_cast<int64_t>(g) * kGroupRows;
     n_draft = static_cast<int>(min(static_cast<int64_t>(kGroupRows), rows - first));
     n_bonus = 0;
   }
-  const int32_t end = shard_start + shard_width;
-  const int32_t b0_d = shard_start / draft_block, b0_b = shard_start / bonus_block;
-  const int32_t cnt_d = (end - 1) / draft_block - b0_d + 1;
-  const int32_t cnt_b = (end - 1) / bonus_block - b0_b + 1;
+  // per shard: block counts, and where its pieces and empty slots start in
+  // the group's numbering
+  if (threadIdx.x == 0) {
+    int32_t items = 0, empties = 0;
+    for (int s = 0; s < tab.n; ++s) {
+      const int32_t st = tab.start[s], en = st + tab.width[s];
+      const int32_t cd = (en - 1) / draft_block - st / draft_block + 1;
+      const int32_t cb = (en - 1) / bonus_block - st / bonus_block + 1;
+      cnt_d[s] = cd;
+      cnt_b[s] = cb;
+      item0[s] = items;
+      empty0[s] = empties;
+      items += n_draft * cd + n_bonus * cb;
+      empties += n_draft * (tab.slots[s] - cd) + n_bonus * (tab.slots[s] - cb);
+    }
+    item0[tab.n] = items;
+    empty0[tab.n] = empties;
+  }
+  __syncthreads();
 
   // real pieces, dealt round-robin to the group's warps
-  const int32_t n_draft_items = n_draft * cnt_d;
-  const int32_t n_items = n_draft_items + n_bonus * cnt_b;
+  const int n_items = item0[tab.n];
   const int workers = parts * kWarpsPerCta;
+  int s = 0;  // each warp's items increase, so its shard index only advances
   for (int32_t t = part * kWarpsPerCta + (threadIdx.x >> 5); t < n_items; t += workers) {
-    int32_t rr, p, b, B;
-    if (t < n_draft_items) {
-      rr = t / cnt_d;
-      p = t - rr * cnt_d;
-      b = b0_d + p;
+    while (t >= item0[s + 1]) ++s;
+    const int32_t u = t - item0[s];
+    const int32_t sd = n_draft * cnt_d[s];
+    int32_t rr, p, B;
+    if (u < sd) {
+      rr = u / cnt_d[s];
+      p = u - rr * cnt_d[s];
       B = draft_block;
     } else {
       rr = n_draft;
-      p = t - n_draft_items;
-      b = b0_b + p;
+      p = u - sd;
       B = bonus_block;
     }
-    const int32_t lo = max(shard_start, b * B);
-    const int32_t hi = min(min(end, b * B + B), org_vocab);
+    const int32_t st = tab.start[s], en = st + tab.width[s];
+    const int32_t b = st / B + p;
+    const int32_t lo = max(st, b * B);
+    const int32_t hi = min(min(en, b * B + B), org_vocab);
     const int64_t r = first + rr;
-    const sga_stat st = piece_argmax<kBf16>(logits + r * ld_bytes, shard_start, lo, hi, lane);
-    if (lane == 0) out[static_cast<int64_t>(p) * rows + r] = st;
+    const sga_stat stat = piece_argmax<kBf16>(
+        logits + r * ld_bytes + static_cast<int64_t>(tab.col[s]) * kElt, st, lo, hi, lane);
+    if (lane == 0) out[static_cast<int64_t>(tab.slot0[s] + p) * rows + r] = stat;
   }
   pdl_launch_dependents();
 
-  // empty slots: (-inf, end - 1), consecutive threads on consecutive rows
-  sga_stat empty;
-  empty.v = __int_as_float(0xff800000);
-  empty.id = end - 1;
-  const int32_t n_empty_draft = n_draft * (n_slots - cnt_d);
-  const int32_t n_empty = n_empty_draft + n_bonus * (n_slots - cnt_b);
+  // empty slots: (-inf, the shard's last id), consecutive threads on
+  // consecutive rows
+  const int n_empty = empty0[tab.n];
+  s = 0;
   for (int32_t t = part * static_cast<int32_t>(blockDim.x) + threadIdx.x; t < n_empty;
        t += parts * static_cast<int32_t>(blockDim.x)) {
-    if (t < n_empty_draft)
-      out[static_cast<int64_t>(cnt_d + t / n_draft) * rows + first + t % n_draft] = empty;
-    else
-      out[static_cast<int64_t>(cnt_b + t - n_empty_draft) * rows + first + n_draft] = empty;
+    while (t >= empty0[s + 1]) ++s;
+    const int32_t u = t - empty0[s];
+    const int32_t ed = n_draft * (tab.slots[s] - cnt_d[s]);
+    sga_stat empty;
+    empty.v = __int_as_float(0xff800000);
+    empty.id = tab.start[s] + tab.width[s] - 1;
+    int64_t slot, r;
+    if (u < ed) {
+      slot = cnt_d[s] + u / n_draft;
+      r = first + u % n_draft;
+    } else {
+      slot = cnt_b[s] + (u - ed);
+      r = first + n_draft;
+    }
+    out[(tab.slot0[s] + slot) * rows + r] = empty;
   }
 }
 
@@ -233,13 +278,24 @@ int64_t block_slots(int64_t shard_start, int64_t shard_width, int64_t draft_bloc
   return a > b ? a : b;
 }
 
-cudaError_t launch_block_argmax(const void *logits, int dtype, int64_t rows, int64_t ld,
-                                int64_t shard_start, int64_t shard_width, int64_t org_vocab,
-                                int64_t draft_block, int64_t bonus_block, int num_reqs,
-                                const int32_t *cu_num_draft, sga_stat *out, int num_sms,
-                                uint32_t *err, cudaStream_t stream) {
+cudaError_t launch_block_argmax_table(const void *logits, int dtype, int64_t rows, int64_t ld,
+                                      int num_shards, const int64_t *starts, const int64_t *cols,
+                                      const int64_t *widths, int64_t org_vocab,
+                                      int64_t draft_block, int64_t bonus_block, int num_reqs,
+                                      const int32_t *cu_num_draft, sga_stat *out, int num_sms,
+                                      uint32_t *err, cudaStream_t stream) {
   const bool bf16 = dtype == SGA_BF16;
-  const int n_slots = static_cast<int>(block_slots(shard_start, shard_width, draft_block, bonus_block));
+  BlockShardTable tab = {};
+  tab.n = num_shards;
+  int32_t slot = 0;
+  for (int s = 0; s < num_shards; ++s) {
+    tab.start[s] = static_cast<int32_t>(starts[s]);
+    tab.col[s] = static_cast<int32_t>(cols[s]);
+    tab.width[s] = static_cast<int32_t>(widths[s]);
+    tab.slot0[s] = slot;
+    tab.slots[s] = static_cast<int32_t>(block_slots(starts[s], widths[s], draft_block, bonus_block));
+    slot += tab.slots[s];
+  }
   const int64_t groups = cu_num_draft != nullptr ? num_reqs : (rows + kGroupRows - 1) / kGroupRows;
   // one wave: as many parts per group as the resident CTAs allow (the work of
   // a group splits evenly over its parts, so a partial second wave would
@@ -261,12 +317,22 @@ cudaError_t launch_block_argmax(const void *logits, int dtype, int64_t rows, int
   const int elt = bf16 ? 2 : 4;
   const char *base = static_cast<const char *>(logits);
   auto kern = bf16 ? block_argmax_kernel<true> : block_argmax_kernel<false>;
-  return cudaLaunchKernelEx(&cfg, kern, base, ld * elt, rows, static_cast<int32_t>(shard_start),
-                            static_cast<int32_t>(shard_width),
-                            static_cast<int32_t>(org_vocab < SGA_MAX_VOCAB ? org_vocab : SGA_MAX_VOCAB),
-                            static_cast<int32_t>(draft_block), static_cast<int32_t>(bonus_block),
-                            static_cast<int32_t>(n_slots), static_cast<int>(parts), cu_num_draft,
-                            out, err);
+  return cudaLaunchKernelEx(
+      &cfg, kern, base, ld * elt, rows, tab,
+      static_cast<int32_t>(org_vocab < SGA_MAX_VOCAB ? org_vocab : SGA_MAX_VOCAB),
+      static_cast<int32_t>(draft_block), static_cast<int32_t>(bonus_block),
+      static_cast<int>(parts), cu_num_draft, out, err);
+}
+
+cudaError_t launch_block_argmax(const void *logits, int dtype, int64_t rows, int64_t ld,
+                                int64_t shard_start, int64_t shard_width, int64_t org_vocab,
+                                int64_t draft_block, int64_t bonus_block, int num_reqs,
+                                const int32_t *cu_num_draft, sga_stat *out, int num_sms,
+                                uint32_t *err, cudaStream_t stream) {
+  const int64_t col = 0;
+  return launch_block_argmax_table(logits, dtype, rows, ld, 1, &shard_start, &col, &shard_width,
+                                   org_vocab, draft_block, bonus_block, num_reqs, cu_num_draft,
+                                   out, num_sms, err, stream);
 }
 
 }  // namespace sga

@@ -29,6 +29,16 @@ cudaError_t launch_local_argmax_table(const void *logits, int dtype, int64_t row
 int64_t block_count(int64_t shard_start, int64_t shard_width, int64_t block);
 int64_t block_slots(int64_t shard_start, int64_t shard_width, int64_t draft_block,
                     int64_t bonus_block);
+constexpr int kMaxBlockShards = 64;
+// Several shards of one logits buffer in one launch: shard s covers global
+// ids [starts[s], starts[s] + widths[s]) held at column cols[s] of `logits`;
+// its slots follow the previous shards' slots in the gathered statistics.
+cudaError_t launch_block_argmax_table(const void *logits, int dtype, int64_t rows, int64_t ld,
+                                      int num_shards, const int64_t *starts, const int64_t *cols,
+                                      const int64_t *widths, int64_t org_vocab,
+                                      int64_t draft_block, int64_t bonus_block, int num_reqs,
+                                      const int32_t *cu_num_draft, sga_stat *out, int num_sms,
+                                      uint32_t *err, cudaStream_t stream);
 cudaError_t launch_block_argmax(const void *logits, int dtype, int64_t rows, int64_t ld,
                                 int64_t shard_start, int64_t shard_width, int64_t org_vocab,
                                 int64_t draft_block, int64_t bonus_block, int num_reqs,

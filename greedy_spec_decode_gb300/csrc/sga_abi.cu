@@ -181,6 +181,43 @@ int sga_local_argmax_blocks(const void *logits, int dtype, int64_t rows, int64_t
                                                 static_cast<cudaStream_t>(stream)));
 }
 
+int sga_local_argmax_blocks_shards(const void *logits, int dtype, int64_t rows, int64_t ld,
+                                   int num_shards, const int64_t *shard_starts,
+                                   const int64_t *shard_widths, int64_t org_vocab,
+                                   int64_t draft_block, int64_t bonus_block, int num_reqs,
+                                   const int32_t *cu_num_draft, sga_stat *out_stats,
+                                   sga_stream stream) {
+  if (dtype != SGA_F32 && dtype != SGA_BF16) return SGA_ERR_DTYPE;
+  if (num_shards < 1 || num_shards > sga::kMaxBlockShards) return SGA_ERR_SIZE;
+  if (shard_starts == nullptr || shard_widths == nullptr) return SGA_ERR_NULL;
+  int64_t cols[sga::kMaxBlockShards];
+  int64_t slots = 0;
+  for (int s = 0; s < num_shards; ++s) {
+    int st = check_shard(shard_starts[s], shard_widths[s], org_vocab);
+    if (st != SGA_OK) return st;
+    if (s > 0 && shard_starts[s] < shard_starts[s - 1] + shard_widths[s - 1]) return SGA_ERR_SHARD;
+    const int64_t n = sga_block_slots(shard_starts[s], shard_widths[s], draft_block, bonus_block);
+    if (n < 0) return static_cast<int>(n);
+    slots += n;
+    cols[s] = shard_starts[s] - shard_starts[0];
+  }
+  if (cols[num_shards - 1] + shard_widths[num_shards - 1] > ld) return SGA_ERR_SHARD;
+  if (rows < 0 || rows * slots > (int64_t(1) << 28)) return SGA_ERR_SIZE;
+  if (cu_num_draft != nullptr && num_reqs < 1) return SGA_ERR_SIZE;
+  if (rows == 0) return SGA_OK;
+  if (logits == nullptr || out_stats == nullptr) return SGA_ERR_NULL;
+  if (misaligned(logits, dtype == SGA_BF16 ? 2 : 4) || misaligned(out_stats, 8) ||
+      misaligned(cu_num_draft, 4))
+    return SGA_ERR_ALIGN;
+  DeviceInfo d;
+  const int st = current_device(&d);
+  if (st != SGA_OK) return st;
+  return launch_status(sga::launch_block_argmax_table(
+      logits, dtype, rows, ld, num_shards, shard_starts, cols, shard_widths, org_vocab,
+      draft_block, bonus_block, num_reqs, cu_num_draft, out_stats, d.num_sms, d.err,
+      static_cast<cudaStream_t>(stream)));
+}
+
 int sga_shard_reduce(const sga_stat *stats, int num_shards, int64_t rows, float *out_vals,
                      int32_t *out_ids, const int64_t *d2t, int64_t d2t_len,
                      sga_stream stream) {

@@ -195,6 +195,33 @@ int sga_local_argmax_blocks(const void *logits, int dtype, int64_t rows, int64_t
                             sga_stream stream);
 
 /*
+ * sga_local_argmax_blocks_shards -- sga_local_argmax_blocks for several
+ * shards of one logits buffer in a single launch (one GPU holding the vocab
+ * slices of several tensor-parallel ranks), as sga_local_argmax_shards is
+ * for per-shard statistics.  Shard s's slots follow shard s-1's: with
+ * slots_s = sga_block_slots(starts[s], widths[s], draft_block, bonus_block),
+ * piece p of row r of shard s goes to out_stats[(slots_0 + ... + slots_{s-1}
+ * + p) * rows + r], exactly what concatenating the per-shard calls' outputs
+ * in shard order gives.
+ * Page: as sga_local_argmax_blocks (vLLM PR #62604, Purpose item 1).
+ *
+ *   logits        device; element (r, 0) holds global id shard_starts[0] of
+ *                 row r; global id g sits at column g - shard_starts[0].
+ *   num_shards    1 .. 64.
+ *   shard_starts, shard_widths   HOST arrays, shards ascending and
+ *                 non-overlapping; the last shard ends at or before column ld.
+ *   rows          0 .. 2^28 / (total slots).
+ *   out_stats     device, (total slots) * rows entries, 8-byte aligned.
+ * Other arguments and the errors as sga_local_argmax_blocks.
+ */
+int sga_local_argmax_blocks_shards(const void *logits, int dtype, int64_t rows, int64_t ld,
+                                   int num_shards, const int64_t *shard_starts,
+                                   const int64_t *shard_widths, int64_t org_vocab,
+                                   int64_t draft_block, int64_t bonus_block, int num_reqs,
+                                   const int32_t *cu_num_draft, sga_stat *out_stats,
+                                   sga_stream stream);
+
+/*
  * sga_shard_reduce -- global argmax from the gathered shard statistics,
  * optionally mapped from draft ids to target ids.
  * Page: vLLM PR #34049, Solution step 3 (reduce across ranks to the global

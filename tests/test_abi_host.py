@@ -166,3 +166,27 @@ def test_block_slots_and_block_argmax_validation(sga_lib):
     assert call(logits=None) == -1 and call(out=None) == -1
     assert call(dtype=0, logits=BAD_F32) == -6
     assert call(cu=ctypes.c_void_p(0x10002), n=2) == -6
+
+
+def test_block_shards_validation(sga_lib):
+    f = sga_lib.lib().sga_local_argmax_blocks_shards
+
+    def call(starts, widths, rows=4, ld=100, org=100, dtype=1, db=16, bb=4, n=0, cu=None,
+             logits=FAKE, out=FAKE):
+        k = len(starts)
+        st = (ctypes.c_int64 * k)(*starts)
+        wd = (ctypes.c_int64 * k)(*widths)
+        return f(logits, dtype, rows, ld, k, st, wd, org, db, bb, n, cu, out, None)
+
+    assert call([0, 40], [50, 50]) == -3          # overlap
+    assert call([0, 50], [50, 60]) == -3          # past ld
+    assert call([0, 50], [50, 0]) == -3           # empty shard
+    assert call([0], [100], dtype=3) == -5
+    assert call([0], [100], db=0) == -2
+    assert call([0, 50], [50, 50], rows=1 << 25) == -2   # rows x slots > 2^28
+    assert call([0], [100], cu=FAKE, n=0) == -2
+    assert call([0], [100], rows=0) == 0
+    assert call([0], [100], logits=None) == -1
+    assert f(FAKE, 1, 4, 100, 0, None, None, 100, 16, 4, 0, None, FAKE, None) == -2
+    assert f(FAKE, 1, 4, 100, 65, None, None, 100, 16, 4, 0, None, FAKE, None) == -2
+    assert f(FAKE, 1, 4, 100, 2, None, None, 100, 16, 4, 0, None, FAKE, None) == -1

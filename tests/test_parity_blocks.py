@@ -34,6 +34,18 @@ def gpu_block_stats(x_dev, shards, org, draft_block, bonus_block, cu_np):
     return stats, sum(slots)
 
 
+def gpu_block_stats_one_launch(x_dev, shards, org, draft_block, bonus_block, cu_np):
+    """All shards' block stats with one sga_local_argmax_blocks_shards launch."""
+    rows = x_dev.size(0)
+    n = sum(sga.sga_block_slots(o, w, draft_block, bonus_block) for o, w in shards)
+    stats = sga.new_stats(n * rows)
+    stats.fill_(-12345)
+    cu_d = None if cu_np is None else torch.from_numpy(np.asarray(cu_np, np.int32)).cuda()
+    sga.sga_local_argmax_blocks_shards(x_dev[:, shards[0][0]:], shards, org, draft_block, stats,
+                                       bonus_block=bonus_block, cu_num_draft=cu_d)
+    return stats, n
+
+
 def random_layout(rng, max_k, n):
     ks = rng.integers(0, max_k + 1, n)
     return np.concatenate([[0], np.cumsum(ks)]).astype(np.int32)
@@ -62,6 +74,9 @@ def test_block_stats_bit_exact(sga_lib, dtype, vocab, num_shards, blocks):
             exp, n_exp = oracle.gathered_block_stats(x, shards, org, db, bb, c)
             assert n == n_exp
             gh.assert_stats_equal(gh.stats_to_numpy(stats), exp)
+            one, n_one = gpu_block_stats_one_launch(x_dev, shards, org, db, bb, c)
+            assert n_one == n_exp
+            gh.assert_stats_equal(gh.stats_to_numpy(one), exp)
             _, ids = gh.gpu_reduce(stats, n, rows)
             assert (ids == oracle.full_argmax(x, org)[1]).all()
 
@@ -170,3 +185,25 @@ def test_request_layout_past_the_rows_sets_error_word(sga_lib):
     gh.assert_stats_equal(got, exp)
     sga_lib.sga_clear_device_error()
     assert sga_lib.sga_device_error() == 0
+
+
+def test_one_launch_large_verify_and_subset_of_shards(sga_lib):
+    # the large-verify shards in one launch (sampled requests against the
+    # oracle, the verify against per-shard launches), and a GPU holding shards
+    # 1 and 3 of 4 (a gap between them)
+    c = wl.large_verify(rows_limit=640)
+    x, shards, org, cu = c["logits"], c["shards"], c["org_vocab"], c["cu_num_draft"]
+    x_dev = gh.to_device(x)
+    one, n = gpu_block_stats_one_launch(x_dev, shards, org, 8192, 1024, cu)
+    per, n_per = gpu_block_stats(x_dev, shards, org, 8192, 1024, cu)
+    assert n == n_per == 200
+    gh.assert_stats_equal(gh.stats_to_numpy(one), gh.stats_to_numpy(per))
+    exp, _ = oracle.gathered_block_stats(x[:16], shards, org, 8192, 1024, cu[:2] - cu[0])
+    gh.assert_stats_equal(gh.stats_to_numpy(one).reshape(n, -1)[:, :16].reshape(-1), exp)
+    y = wl.discrete_logits(77, 9, 4000, "bf16", p_nan=1e-3)
+    quarters = wl.even_shards(4000, 4)
+    held = [quarters[1], quarters[3]]
+    got, m = gpu_block_stats_one_launch(gh.to_device(y), held, 3990, 256, 64, None)
+    exp, m_exp = oracle.gathered_block_stats(y, held, 3990, 256, 64)
+    assert m == m_exp
+    gh.assert_stats_equal(gh.stats_to_numpy(got), exp)
