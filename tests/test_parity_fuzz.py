@@ -1,5 +1,7 @@
 """Randomised parity sweep (fixed seeds) of the one-launch shard argmax, the
-reduce and the fused verify, and of the fused LM head, against the oracle.
+reduce and the fused verify, of block-granular statistics (both entry points)
+feeding the verify, and of the fused LM head (bf16 and fp8), against the
+oracle.
 
 Every case draws its own shape: rows, vocabulary, number and widths of shards,
 dtype, row-stride padding, org_vocab (padding), value distribution (normal or
@@ -80,3 +82,60 @@ def test_random_lmhead(sga_lib, seed):
     st, v, i = lm.run_gpu(hidden, weight, shards, org)
     rows = np.arange(M) if M <= 300 else np.arange(0, M, 3)
     lm.check_rows(rows, hidden, weight, shards, org, st, v, i)
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_random_block_stats(sga_lib, seed):
+    # block-granular statistics with random vocab, shards, block sizes (nested
+    # or not), request layouts with 0..K drafts, padding and row strides; both
+    # entry points (per shard and one launch), then the wide or narrow verify
+    import test_parity_blocks as tb
+    rng = np.random.default_rng(3000 + seed)
+    vocab = int(rng.choice([97, 1000, 4099, 20000, 50257]))
+    num_shards = int(rng.integers(1, min(6, vocab) + 1))
+    dtype = "bf16" if rng.random() < 0.6 else "f32"
+    n = int(rng.integers(1, 20))
+    max_k = int(rng.choice([1, 3, 7, 15]))
+    ks = rng.integers(0, max_k + 1, n)
+    cu = np.concatenate([[0], np.cumsum(ks)]).astype(np.int32)
+    rows = int(cu[-1]) + n
+    db = int(rng.choice([1, 7, 64, 1024, 8192]))
+    bb = int(rng.choice([1, 16, 1024, 3000]))
+    if vocab // min(db, bb) * num_shards > 3000:   # keep the slots under the verify's limit
+        db, bb = max(db, 64), max(bb, 64)
+    pad = int(rng.integers(0, 5))
+    org = int(vocab if rng.random() < 0.5 else rng.integers(1, vocab + 1))
+    full = wl.discrete_logits(seed + 50, rows, vocab + pad, dtype, p_nan=0.002, p_inf=0.01)
+    x = np.ascontiguousarray(full[:, :vocab])
+    x_dev = gh.to_device(full)[:, :vocab]
+    shards = wl.random_shards(seed, vocab, num_shards)
+    exp, n_exp = oracle.gathered_block_stats(x, shards, org, db, bb, cu)
+    per, n_per = tb.gpu_block_stats(x_dev, shards, org, db, bb, cu)
+    one, n_one = tb.gpu_block_stats_one_launch(x_dev, shards, org, db, bb, cu)
+    assert n_per == n_one == n_exp
+    gh.assert_stats_equal(gh.stats_to_numpy(per), exp)
+    gh.assert_stats_equal(gh.stats_to_numpy(one), exp)
+    _, t = oracle.shard_reduce(oracle.gathered_stats(x, shards, org), num_shards, rows)
+    drafts = wl.compose_drafts(t, cu, rng.random(int(cu[-1])) < 0.7,
+                               rng.integers(-1, vocab, int(cu[-1])).astype(np.int32))
+    got = gh.gpu_verify(one, n_exp, cu, drafts, max_k)
+    ref = oracle.greedy_verify(exp, n_exp, cu, drafts, max_k)
+    for key in ("sampled", "num_sampled", "num_rejected", "bonus", "target_ids"):
+        assert (got[key] == ref[key]).all(), key
+    assert (ref["target_ids"] == t).all()
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_lmhead_fp8(sga_lib, seed):
+    import test_parity_lmhead_fp8 as f8
+    rng = np.random.default_rng(4000 + seed)
+    M = int(rng.choice([1, 5, 16, 33, 64, 100, 129, 300]))
+    H = int(128 * rng.integers(1, 5))
+    vocab = int(rng.integers(1, 3000))
+    num_shards = int(rng.integers(1, min(4, vocab) + 1))
+    org = int(vocab if rng.random() < 0.5 else rng.integers(1, vocab + 1))
+    hq, hs, wq, w_scale = f8.make(M, H, vocab, 4000 + seed)
+    shards = wl.random_shards(seed, vocab, num_shards)
+    st, v, i = f8.run_gpu(sga_lib, hq, hs, wq, w_scale, shards, org)
+    rows = np.arange(M) if M <= 130 else np.arange(0, M, 3)
+    f8.check(rows, hq, hs, wq, w_scale, shards, org, st, v, i)
