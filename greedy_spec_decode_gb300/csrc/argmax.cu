@@ -61,6 +61,12 @@ struct ShardTable {
 #ifndef SGA_ARGMAX_BULK
 #define SGA_ARGMAX_BULK 1
 #endif
+#ifndef SGA_ARGMAX_PREFETCH
+// L2 prefetch of the first ring stages before the PDL wait.  Measured on the
+// large-verify step: one launch for all shards 231.8 -> 229.9 us, one launch
+// per shard 252.9 -> 244.0 us per step; the small workloads unchanged.
+#define SGA_ARGMAX_PREFETCH 1
+#endif
 #ifndef SGA_ARGMAX_STAGES
 #define SGA_ARGMAX_STAGES 4
 #endif
@@ -121,7 +127,6 @@ __global__ void __launch_bounds__(kThreads + (kBulk ? 32 : 0), kBulk ? 2048 / (k
   __shared__ float cta_v;
   __shared__ int32_t cta_i;
 
-  pdl_wait();  // inputs written by the previous kernel in the stream are visible
   const int chunk = static_cast<int>(blockIdx.x % chunks);
   const int rs = static_cast<int>(blockIdx.x / chunks);
   const int row = rs / tab.n;
@@ -141,6 +146,19 @@ __global__ void __launch_bounds__(kThreads + (kBulk ? 32 : 0), kBulk ? 2048 / (k
   const int tail = valid - head - nvec * kVec;
   const int v0 = static_cast<int>(static_cast<int64_t>(nvec) * chunk / chunks);
   const int v1 = static_cast<int>(static_cast<int64_t>(nvec) * (chunk + 1) / chunks);
+
+  if (kBulk && SGA_ARGMAX_PREFETCH && tid == kThreads && v1 > v0) {
+    // Warm L2 with what the ring loads first while the previous kernel
+    // drains: the addresses come from the parameters alone, and a prefetch
+    // only fills L2, which stays coherent with any later write, so it may
+    // precede the dependency wait.
+    const int n = min(v1 - v0, kStages * kStageVec);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                     reinterpret_cast<const uint4 *>(p + head * kElt) + v0),
+                 "r"(n * 16)
+                 : "memory");
+  }
+  pdl_wait();  // inputs written by the previous kernel in the stream are visible
 
   if (chunk == 0 && tid < head) {
     const float x = load_elem<kBf16>(p, tid);
