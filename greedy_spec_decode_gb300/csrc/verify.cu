@@ -83,15 +83,18 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // Many statistics per row (block-granular statistics: hundreds per row): one
-// CTA per request, warp j reduces row j.  Lane l scans entries l, l + 32, ...
-// in ascending order with the scan rule, then the warp merges the lanes'
-// winners on (value, entry position): NaN first, larger value, then the
+// CTA per request, 512 threads.  Thread (stream k = tid / 16, row j = tid % 16)
+// scans entries k, k + 32, ... of row j in ascending order with the scan rule,
+// so the 16 threads of a half-warp read 16 consecutive rows of one entry
+// (128 contiguous bytes per load).  The 32 streams of a row are then merged in
+// shared memory on (value, entry position): NaN first, larger value, then the
 // EARLIER position, which is exactly the sequential scan over all entries
-// (the first NaN, else the first maximum).  Lanes 0..15 of warp 0 then finish
-// the request as in the narrow kernel.
-constexpr int kWideWarps = 16;
+// (the first NaN, else the first maximum).  Lanes 0..15 of warp 0 finish the
+// request as in the narrow kernel.
+constexpr int kWideThreads = 512;
+constexpr int kStreams = kWideThreads / 16;
 
-__global__ void __launch_bounds__(kWideWarps * 32)
+__global__ void __launch_bounds__(kWideThreads)
     greedy_verify_wide_kernel(const sga_stat *__restrict__ stats, int num_entries, int num_reqs,
                               const int32_t *__restrict__ cu_num_draft,
                               const int32_t *__restrict__ draft_tokens, int max_k,
@@ -100,58 +103,68 @@ __global__ void __launch_bounds__(kWideWarps * 32)
                               int32_t *__restrict__ out_num_rejected,
                               int32_t *__restrict__ out_bonus, int32_t *__restrict__ out_target_ids,
                               uint32_t *err) {
-  __shared__ int32_t t_row[kWideWarps];
+  __shared__ float part_v[kStreams][16];
+  __shared__ int32_t part_pos[kStreams][16];
+  __shared__ int32_t part_id[kStreams][16];
+  __shared__ int32_t t_row[16];
   pdl_wait();
   const int lane = threadIdx.x & 31;
-  const int j = threadIdx.x >> 5;  // row within the request
+  const int j = threadIdx.x & 15;       // row within the request
+  const int stream = threadIdx.x >> 4;  // entries stream, stream + 32, ...
   const int64_t req = blockIdx.x;
   const int64_t total_rows = static_cast<int64_t>(cu_num_draft[num_reqs]) + num_reqs;
   const int32_t c = cu_num_draft[req];
   const int32_t k = cu_num_draft[req + 1] - c;
   const bool bad = k < 0 || k > max_k;
-  if (!bad && j <= k) {
-    const int64_t row = static_cast<int64_t>(c) + req + j;
-    float bv = __int_as_float(0xff800000);
-    int32_t bpos = kNoId, bid = 0;
-    int s = lane;
-    for (; s + 7 * 32 < num_entries; s += 8 * 32) {
-      sga_stat e[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) e[u] = stats[static_cast<int64_t>(s + u * 32) * total_rows + row];
+  const bool has_row = !bad && j <= k;
+  const int64_t row = static_cast<int64_t>(c) + req + j;
+
+  float bv = __int_as_float(0xff800000);
+  int32_t bpos = kNoId, bid = 0;
+  if (has_row) {
+    int e = stream;
+    for (; e + 7 * kStreams < num_entries; e += 8 * kStreams) {
+      sga_stat x[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u)
-        if (bpos == kNoId || scan_better(e[u].v, bv)) {
-          bv = e[u].v;
-          bpos = s + u * 32;
-          bid = e[u].id;
+        x[u] = stats[static_cast<int64_t>(e + u * kStreams) * total_rows + row];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (bpos == kNoId || scan_better(x[u].v, bv)) {
+          bv = x[u].v;
+          bpos = e + u * kStreams;
+          bid = x[u].id;
         }
     }
-    for (; s < num_entries; s += 32) {
-      const sga_stat e = stats[static_cast<int64_t>(s) * total_rows + row];
-      if (bpos == kNoId || scan_better(e.v, bv)) {
-        bv = e.v;
-        bpos = s;
-        bid = e.id;
+    for (; e < num_entries; e += kStreams) {
+      const sga_stat x = stats[static_cast<int64_t>(e) * total_rows + row];
+      if (bpos == kNoId || scan_better(x.v, bv)) {
+        bv = x.v;
+        bpos = e;
+        bid = x.id;
       }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int32_t op = __shfl_xor_sync(0xffffffffu, bpos, off);
-      const int32_t oi = __shfl_xor_sync(0xffffffffu, bid, off);
-      if (op != kNoId && (bpos == kNoId || pair_beats(ov, op, bv, bpos))) {
-        bv = ov;
-        bpos = op;
-        bid = oi;
-      }
-    }
-    if (lane == 0) {
-      t_row[j] = bid;
-      if (out_target_ids) out_target_ids[row] = bid;
     }
   }
+  part_v[stream][j] = bv;
+  part_pos[stream][j] = bpos;
+  part_id[stream][j] = bid;
   __syncthreads();
-  if (j != 0 || lane >= 16) return;
+  if (threadIdx.x < 16 && has_row) {
+    float v = part_v[0][j];
+    int32_t pos = part_pos[0][j], id = part_id[0][j];
+    for (int q = 1; q < kStreams; ++q) {
+      const int32_t qp = part_pos[q][j];
+      if (qp != kNoId && (pos == kNoId || pair_beats(part_v[q][j], qp, v, pos))) {
+        v = part_v[q][j];
+        pos = qp;
+        id = part_id[q][j];
+      }
+    }
+    t_row[j] = id;
+    if (out_target_ids) out_target_ids[row] = id;
+  }
+  __syncthreads();
+  if (threadIdx.x >= 16) return;
   int32_t *sampled_row = out_sampled + req * (max_k + 1);
   if (bad) {
     if (lane <= max_k) sampled_row[lane] = -1;
@@ -191,7 +204,7 @@ cudaError_t launch_greedy_verify(const sga_stat *stats, int num_shards, int num_
   cfg.numAttrs = 1;
   if (num_shards > kWideEntries) {
     cfg.gridDim = dim3(static_cast<unsigned>(num_reqs));
-    cfg.blockDim = dim3(kWideWarps * 32);
+    cfg.blockDim = dim3(kWideThreads);
     return cudaLaunchKernelEx(&cfg, greedy_verify_wide_kernel, stats, num_shards, num_reqs,
                               cu_num_draft, draft_tokens, max_k, out_sampled, out_num_sampled,
                               out_num_rejected, out_bonus, out_target_ids, err);
