@@ -142,19 +142,18 @@ def test_verify_sample_block_stats_match_shard_stats(sga_lib):
 
 def test_large_verify_full_size_block_stats(sga_lib):
     # 4096 rows x 202048 bf16, 3 uneven shards, blocks 8192 / 1024: every
-    # stat of whole sampled requests against the oracle, and the verify from
-    # the block stats against the oracle's verify from per-shard stats
+    # stat of every row against the oracle (per-shard launches and the
+    # one-launch form), and the verify from the block stats against the
+    # oracle's verify from per-shard stats
     c = wl.large_verify()
     x, shards, org, cu = c["logits"], c["shards"], c["org_vocab"], c["cu_num_draft"]
     rows = x.shape[0]
     stats, n = gpu_block_stats(gh.to_device(x), shards, org, 8192, 1024, cu)
-    got_stats = gh.stats_to_numpy(stats).reshape(n, rows)
     slots = [oracle.block_slots(o, w, 8192, 1024) for o, w in shards]
-    for i in (0, 1, 77, 254, 255):                      # whole requests i
-        r0, r1 = int(cu[i]) + i, int(cu[i + 1]) + i + 1
-        sub_cu = np.array([0, cu[i + 1] - cu[i]], np.int32)
-        exp, _ = oracle.gathered_block_stats(x[r0:r1], shards, org, 8192, 1024, sub_cu)
-        gh.assert_stats_equal(got_stats[:, r0:r1].reshape(-1), exp)
+    exp_all, _ = oracle.gathered_block_stats(x, shards, org, 8192, 1024, cu)   # every row
+    gh.assert_stats_equal(gh.stats_to_numpy(stats), exp_all)
+    one, _ = gpu_block_stats_one_launch(gh.to_device(x), shards, org, 8192, 1024, cu)
+    gh.assert_stats_equal(gh.stats_to_numpy(one), exp_all)
     shard_stats = oracle.gathered_stats(x, shards, org)
     _, t = oracle.shard_reduce(shard_stats, 3, rows)
     drafts = wl.compose_drafts(t, cu, c["flags"], c["rand_ids"])
