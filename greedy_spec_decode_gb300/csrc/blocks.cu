@@ -1,5 +1,6 @@
-// blocks.cu -- block-granular statistics of one vocab shard: per row, the
-// (max, id) of every fixed global block of ids that meets the shard.
+// blocks.cu -- block-granular statistics of vocab shards: per row, the
+// (max, id) of every fixed global block of ids that meets a shard; one launch
+// covers one shard or all the shards a GPU holds.
 //
 // vLLM PR #62604, Purpose item 1: each rank reduces its shard to per-block
 // (max, token id) statistics, only those are all-gathered, and one kernel
@@ -14,14 +15,15 @@
 // piece p covers global ids [max(start, (b0+p)B), min(end, (b0+p+1)B)).  Every
 // row gets n_slots stats (the larger of the two block counts); slots past a
 // row's own count hold (-inf, end - 1), which never wins because a real piece
-// precedes it.  Output layout: out[p * rows + r] (piece-major, like the
-// shard-major gathered buffer).
+// precedes it.  Output layout: out[(slot0_s + p) * rows + r] (piece-major,
+// shards in order, like the shard-major gathered buffer).
 //
 // Design: the grid is (row group, part): a row group is one request (its K_i
 // draft rows and its bonus row, read from two entries of cu_num_draft, so no
 // warp ever searches for the kind of its row) or, without cu_num_draft, 16
-// draft rows.  The group's real pieces (K_i x draft count + bonus count) are
-// dealt round-robin to the parts x 4 warps of the group; a warp streams its
+// draft rows.  The group's real pieces (per shard, K_i x draft count + bonus
+// count) are dealt round-robin to the parts x 4 warps of the group; a warp
+// streams its
 // piece with 16-byte loads, kUnroll in flight per lane, keeps the best
 // vector in registers (the steps of the per-shard kernel), merges across
 // the warp and stores one stat.  The empty slots (all but a few of a draft
