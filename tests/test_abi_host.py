@@ -190,3 +190,19 @@ def test_block_shards_validation(sga_lib):
     assert f(FAKE, 1, 4, 100, 0, None, None, 100, 16, 4, 0, None, FAKE, None) == -2
     assert f(FAKE, 1, 4, 100, 65, None, None, 100, 16, 4, 0, None, FAKE, None) == -2
     assert f(FAKE, 1, 4, 100, 2, None, None, 100, 16, 4, 0, None, FAKE, None) == -1
+
+
+def test_valid_call_without_a_gpu_returns_the_cuda_status(sga_lib):
+    # every argument valid, but no device: the status is SGA_ERR_CUDA and
+    # nothing is dereferenced.  Only where no GPU is visible (with one, the
+    # fake pointers would reach a kernel).
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is visible")
+    L = sga_lib.lib()
+    assert L.sga_local_argmax(FAKE, 1, 4, 100, 0, 100, 100, FAKE, None) == -9
+    assert L.sga_shard_reduce(FAKE, 2, 4, None, FAKE, None, 0, None) == -9
+    assert L.sga_lmhead_argmax(FAKE, 4, 64, FAKE, 0, 64, 64, FAKE, FAKE,
+                               L.sga_lmhead_argmax_workspace(4, 64), None) == -9
+    word = ctypes.c_uint32(7)
+    assert L.sga_device_error(ctypes.byref(word)) == -9
