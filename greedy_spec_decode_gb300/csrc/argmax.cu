@@ -355,10 +355,13 @@ __global__ void shard_reduce_kernel(const sga_stat *__restrict__ stats, int num_
 }
 
 // Pieces per (row, shard).  Splitting a row costs two cluster barriers and a
-// shorter-lived CTA (its reduction tail is not streaming), so rows are split
-// only when there are too few (row, shard) pairs to fill one wave of resident
-// CTAs (measured: 96 rows x 4 shards of 50016 bf16 ids take 23.0 us with one
-// wave as the target, 28.2 us with two).
+// shorter-lived CTA (its reduction tail is not streaming), so a row is split
+// (in powers of two) only while the grid stays within half of the resident
+// CTA slots.  Measured on GB300 after an L2 flush (one step, argmax + reduce
+// or verify): 32 rows x 2 shards of 76032 bf16 ids: 1 / 2 / 4 / 8 pieces per
+// row 15.5 / 13.1 / 12.8 / 13.0 us (the rule picks 4); 96 rows x 4 shards of
+// 50016: 19.1 / 20.0 / 23.5 / 23.5 us (the rule picks 1; a one-wave target
+// picked 4).
 #ifndef SGA_ARGMAX_WAVES
 #define SGA_ARGMAX_WAVES 1
 #endif
@@ -373,7 +376,8 @@ int pick_chunks(int64_t rs_count, int64_t max_valid, int elt, int num_sms) {
   }
   const int64_t want_ctas = static_cast<int64_t>(num_sms) * per_sm * SGA_ARGMAX_WAVES;
   int chunks = 1;
-  while (chunks < kMaxChunks && nvec / (2 * chunks) >= kThreads && rs_count * chunks < want_ctas)
+  while (chunks < kMaxChunks && nvec / (2 * chunks) >= kThreads &&
+         rs_count * chunks * 4 <= want_ctas)
     chunks *= 2;
   return chunks;
 }
