@@ -665,7 +665,8 @@ def decode_roofline(weight_bytes, kern_ms, num_shards, fp8):
     pk, pk_src = peaks()
     hbm = float(pk.get("hbm_gbs", FALLBACK_HBM_GBS))
     achieved = weight_bytes / (kern_ms * 1e-3) / 1e9
-    traffic = ncu_traffic("lmhead_decode.md", ["greedy_spec_decode_gb300/csrc/lmhead.cu",
+    traffic = ncu_traffic("lmhead_decode.md", ["greedy_spec_decode_gb300/csrc/lmhead_decode.cu",
+                                               "greedy_spec_decode_gb300/csrc/tcgen05.cuh",
                                                "greedy_spec_decode_gb300/csrc/common.cuh"])
     return {"bound": "hbm",
             "kernel": "lmhead_argmax_decode_kernel<%s>" % ("fp8" if fp8 else "bf16"),
@@ -814,6 +815,7 @@ def run_ours_lmhead(args, fp8=False):
                      "traffic": ncu_traffic(
                          "lmhead_fused_fp8.md" if fp8 else "lmhead_fused.md",
                          ["greedy_spec_decode_gb300/csrc/lmhead.cu",
+                          "greedy_spec_decode_gb300/csrc/tcgen05.cuh",
                           "greedy_spec_decode_gb300/csrc/common.cuh"]),
                      "traffic_unit": "DRAM bytes per launch of the GEMM kernel",
                      "peak_source": ((f"{pk_src} bf16_tflops_sustained (cuBLAS bf16, timed in a "

@@ -66,6 +66,13 @@ cudaError_t launch_lmhead_argmax(const void *hidden, int64_t M, int64_t H, const
                                  const float *row_scale = nullptr, float w_scale = 1.0f);
 
 
+// Decode-size LM head (lmhead_decode.cu), M <= 64: writes one partial per
+// (row, CTA) to ws[row * (*ws_stride) + cta] and sets *ws_stride.
+cudaError_t launch_lmhead_decode(bool fp8, const void *hidden, int64_t M, int64_t H,
+                                 const void *weight, int64_t shard_start, int64_t valid,
+                                 sga_stat *ws, int n_tiles, int num_sms, uint32_t *err,
+                                 cudaStream_t stream, int *ws_stride);
+
 // Bounded-wait self-test (lmhead.cu).
 cudaError_t launch_selftest_timeout(unsigned long long limit_ns, uint32_t *err,
                                     unsigned long long *waited_ns, cudaStream_t stream);

@@ -22,25 +22,18 @@
 // streamed from HBM about once.  A small second kernel reduces each row's
 // per-tile partials (one warp per row, row-major workspace).
 //
+// The decode-size kernel (M <= 64, weight as the MMA's 128-row operand) is in
+// lmhead_decode.cu; the PTX and host helpers both use are in tcgen05.cuh.
+//
 // Every mbarrier wait is bounded in time; on expiry the CTA records
 // SGA_DEVERR_TIMEOUT, stops issuing work, waits (bounded) for its own copies
 // and MMAs in flight, frees its TMEM and exits.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
-#include "common.cuh"
+#include "tcgen05.cuh"
 
 namespace sga {
 namespace {
 
 constexpr int BM = 128;          // rows of hidden per tile (TMEM lanes)
-constexpr int BN = 256;          // vocab ids per tile (TMEM columns)
-constexpr int ROW_BYTES = 128;   // one 128-byte swizzled K-block row of a tile
-// K-block in elements: 64 bf16 or 128 fp8 (E4M3) per 128-byte row
-template <bool kFp8>
-constexpr int kBk = kFp8 ? 128 : 64;
 #ifndef SGA_LMHEAD_STAGES
 #define SGA_LMHEAD_STAGES 4
 #endif
@@ -50,121 +43,14 @@ constexpr int kBk = kFp8 ? 128 : 64;
 #ifndef SGA_LMHEAD_2SM_MIN_M
 #define SGA_LMHEAD_2SM_MIN_M 129
 #endif
-#ifndef SGA_LMHEAD_DECODE_MAX_M
-// Swapped-operand decode kernel for M <= this (0: off; at most 64).  Measured:
-// an N = 128 variant for M = 65..128 was slower than the 1-SM kernel (graph
-// replay, 2 shards: M = 128 bf16 210 vs 201 us, fp8 122 vs 114 us).
-#define SGA_LMHEAD_DECODE_MAX_M 64
-#endif
-static_assert(SGA_LMHEAD_DECODE_MAX_M <= 64, "the decode kernel holds at most 64 hidden rows");
 constexpr int STAGES = SGA_LMHEAD_STAGES;
 constexpr int A_BYTES = BM * ROW_BYTES;   // 16 KB
 constexpr int B_BYTES = BN * ROW_BYTES;   // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int THREADS = 192;           // 6 warps
 constexpr int TMEM_COLS = 2 * BN;      // double-buffered accumulator
 // At least 120 KB so that one CTA (holding all 512 TMEM columns) runs per SM.
 constexpr int SMEM_NEEDED = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 256 /*barriers*/;
 constexpr int SMEM_BYTES = SMEM_NEEDED > 120 * 1024 ? SMEM_NEEDED : 120 * 1024;
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
-
-// ---------------------------------------------------------------- PTX helpers
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned long long global_timer_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Wait for the phase of `parity` to complete, at most limit_ns.  Returns
-// false on expiry (and on an abort raised by another role of this CTA).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          const volatile int *abort_flag,
-                                          unsigned long long limit_ns = kWaitLimitNs) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_timer_ns();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > limit_ns) return false;
-  }
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-
-// Bring one box of a tensor into L2 (no shared-memory destination, no
-// completion to wait for).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y)
-               : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor of a K-major tile stored as 128-byte rows
-// with the 128-byte swizzle (what TMA writes with CU_TENSOR_MAP_SWIZZLE_128B):
-// start address >> 4, leading offset unused (1), stride between 8-row groups
-// 1024 B, descriptor version 1, swizzle mode 2 (128 B).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);
-  d |= static_cast<uint64_t>(1) << 16;
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;
-  d |= static_cast<uint64_t>(1) << 46;
-  d |= static_cast<uint64_t>(2) << 61;
-  return d;
-}
-
-// Instruction descriptor of tcgen05.mma: fp32 accumulator (bits 4-5 = 1),
-// A/B formats (bits 7-9, 10-12: bf16 = 1 for kind::f16, E4M3 = 0 for
-// kind::f8f6f4), both operands K-major, N >> 3 at bit 17, M >> 4 at bit 24.
-template <bool kFp8>
-__host__ __device__ constexpr uint32_t instr_desc(uint32_t m, uint32_t n) {
-  return (1u << 4) | (kFp8 ? 0u : ((1u << 7) | (1u << 10))) | ((n >> 3) << 17) | ((m >> 4) << 24);
-}
 
 // One MMA of a K step (16 bf16 or 32 fp8 = 32 bytes of each row), M = BM,
 // N = BN, issued by one thread of this CTA.
@@ -187,31 +73,6 @@ __device__ __forceinline__ void mma_1sm(uint32_t d_tmem, uint64_t a_desc, uint64
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
   }
-}
-
-// Arrive once on `bar` when every tcgen05.mma issued so far has completed.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-        "=r"(r[31])
-      : "r"(taddr));
-}
-
-__device__ __forceinline__ void tmem_ld_wait() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
 struct Shared {
@@ -420,424 +281,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                  "r"(TMEM_COLS)
-                 : "memory");
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Decode-size variant (M <= 64 hidden rows): the operands swap roles.  The
-// weight tile is the MMA's A operand (M = 128 vocab ids per MMA, two MMAs per
-// 256-id tile) and the hidden rows are its B operand (N = kN = 16, 32 or 64
-// columns).  A stage then holds 32-64 KB of weight and only kN x 128 B of
-// hidden per K chunk (instead of 128 hidden rows, mostly zero fill), and each
-// weight row is read 256-512 contiguous bytes at a time: at these sizes the
-// kernel is a weight stream, paced by the length of its DRAM runs and the
-// bytes in flight.
-// TMEM lane = vocab id, TMEM column = hidden row.  The epilogue reduces each
-// group of 32 (or 16) rows across the 32 lanes of a warp with a butterfly
-// transpose-reduce in the (value, id) order, after which each lane holds one
-// row's winner and keeps that row's running best; the four epilogue warps
-// merge through shared memory at the end and each CTA writes one partial per
-// row to the workspace (row stride = number of CTAs); the finalize kernel
-// merges the CTAs' partials.
-// ---------------------------------------------------------------------------
-// K chunks (128-byte columns of the weight) per stage: 1 -> a stage holds 256
-// weight rows x 128 B (a 256-id tile in two 128-row halves); 2 -> 128 rows x
-// 256 B (a 128-id tile: twice the contiguous bytes per row); 4 -> 128 rows x
-// 512 B.  Measured on GB300 (2 shards of 75968 x 4096, per step, bf16 / fp8):
-//   N = 16 (M <= 16): 1 chunk 199 / 113 us, 2 chunks 201 / 113, 4 chunks
-//                     193 / 108 (3 stages of 72 KB)
-//   N = 32, 64:       1 chunk 203-208 / 117-122 us, 2 chunks 196-200 /
-//                     110-115, 4 chunks 201-206 / 115-119 (only 2 stages)
-// Longer contiguous runs per weight row pay more than extra bytes in flight.
-#ifndef SGA_LMHEAD_DEC_PREFETCH
-// L2 prefetch of the first stages before the PDL wait.  Measured (graph
-// replay, 8 shards of 18992 ids): bf16 M = 1 223.7 -> 219.7 us per step, fp8
-// 137.6 -> 133.2 us; 2 shards of 75968 ids unchanged.
-#define SGA_LMHEAD_DEC_PREFETCH 1
-#endif
-#ifndef SGA_LMHEAD_DEC_CHUNKS_N16
-#define SGA_LMHEAD_DEC_CHUNKS_N16 4
-#endif
-#ifndef SGA_LMHEAD_DEC_CHUNKS
-#define SGA_LMHEAD_DEC_CHUNKS 2
-#endif
-template <int kN>
-constexpr int dec_chunks = kN <= 16 ? SGA_LMHEAD_DEC_CHUNKS_N16 : SGA_LMHEAD_DEC_CHUNKS;
-template <int kN>
-constexpr int dec_halves = dec_chunks<kN> >= 2 ? 1 : 2;  // 128-id halves per tile
-constexpr int DEC_SUB_BYTES = 128 * ROW_BYTES;            // one 128-row x 128-byte box
-constexpr int kDecMaxParts = 256;  // CTAs (partials per row) of one decode launch, at most
-template <int kN>
-constexpr int dec_a_bytes = dec_chunks<kN> * dec_halves<kN> * DEC_SUB_BYTES;
-template <int kN>
-constexpr int dec_stage_bytes = dec_a_bytes<kN> + dec_chunks<kN> * kN * ROW_BYTES;
-template <int kN>
-constexpr int dec_stages = (227 * 1024 - 4096) / dec_stage_bytes<kN>;  // 3, 5, 4
-
-template <int kN>
-struct SharedDec {
-  uint64_t full[dec_stages<kN>];
-  uint64_t empty[dec_stages<kN>];
-  uint64_t tmem_full[2];
-  uint64_t tmem_empty[2];
-  uint64_t drain;
-  uint32_t tmem_base;
-  int abort;
-  float part_v[4][kN];
-  int32_t part_i[4][kN];
-};
-
-template <int kN>
-constexpr int dec_smem_bytes =
-    1024 + dec_stages<kN> * dec_stage_bytes<kN> + static_cast<int>(sizeof(SharedDec<kN>));
-static_assert(dec_smem_bytes<16> <= 227 * 1024 && dec_smem_bytes<32> <= 227 * 1024 &&
-                  dec_smem_bytes<64> <= 227 * 1024,
-              "decode-size LM-head ring exceeds shared memory");
-
-template <int kN>
-__device__ __forceinline__ void raise_abort_dec(SharedDec<kN> *sh, uint32_t *err) {
-  *reinterpret_cast<volatile int *>(&sh->abort) = 1;
-  atomicOr(err, SGA_DEVERR_TIMEOUT);
-}
-
-// One MMA of a K step with M = 128 (weight rows) and N = kN (hidden rows).
-template <bool kFp8, int kN>
-__device__ __forceinline__ void mma_dec(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                        uint32_t accumulate) {
-  constexpr uint32_t idesc = instr_desc<kFp8>(128, kN);
-  if constexpr (kFp8) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  } else {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  }
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-}
-
-// Load kN accumulator columns of this warp's 32 TMEM lanes (x16 loads).
-template <int kN>
-__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[kN]) {
-#pragma unroll
-  for (int c = 0; c < kN / 16; ++c) tmem_ld16(taddr + 16 * c, r + 16 * c);
-}
-
-__device__ __forceinline__ void keep_better(float &v, int32_t &i, float ov, int32_t oi) {
-  if (pair_beats(ov, oi, v, i)) {
-    v = ov;
-    i = oi;
-  }
-}
-
-// Transpose-reduce of G rows (G = 16 or 32) across the 32 lanes of a warp:
-// lane l holds x[k] = the logit of row k at its own vocab id `id`.  Each
-// butterfly step pairs lane l with l ^ s; the lane with bit s set keeps the
-// upper half of its current rows and receives the partner's values of them,
-// the other lane keeps the lower half, and both merge with the (value, id)
-// order.  After 31 merges (instead of 5 shuffle rounds per row), lane l holds
-// the argmax over the warp's 32 ids of row l (G = 32) or row l / 2 (G = 16).
-template <int kCnt, int kS>
-__device__ __forceinline__ void butterfly_step(float *x, int32_t *xi, int lane) {
-  if constexpr (kS >= 1) {
-    if constexpr (kCnt > 1) {
-      constexpr int kHalf = kCnt / 2;
-      const bool upper = (lane & kS) != 0;
-#pragma unroll
-      for (int k = 0; k < kHalf; ++k) {
-        const float sv = upper ? x[k] : x[kHalf + k];
-        const int32_t si = upper ? xi[k] : xi[kHalf + k];
-        float kv = upper ? x[kHalf + k] : x[k];
-        int32_t ki = upper ? xi[kHalf + k] : xi[k];
-        keep_better(kv, ki, __shfl_xor_sync(0xffffffffu, sv, kS),
-                    __shfl_xor_sync(0xffffffffu, si, kS));
-        x[k] = kv;
-        xi[k] = ki;
-      }
-      butterfly_step<kHalf, kS / 2>(x, xi, lane);
-    } else {
-      keep_better(x[0], xi[0], __shfl_xor_sync(0xffffffffu, x[0], kS),
-                  __shfl_xor_sync(0xffffffffu, xi[0], kS));
-      butterfly_step<1, kS / 2>(x, xi, lane);
-    }
-  }
-}
-
-template <int G>
-__device__ __forceinline__ void rows_argmax(float (&x)[G], int32_t id, int lane, float &out_v,
-                                            int32_t &out_i) {
-  int32_t xi[G];
-#pragma unroll
-  for (int k = 0; k < G; ++k) xi[k] = id;
-  butterfly_step<G, 16>(x, xi, lane);
-  out_v = x[0];
-  out_i = xi[0];
-}
-
-template <bool kFp8, int kN>
-__global__ void __launch_bounds__(THREADS, 1)
-    lmhead_argmax_decode_kernel(const __grid_constant__ CUtensorMap tmap_w,
-                                const __grid_constant__ CUtensorMap tmap_h, int M, int num_kb,
-                                int n_tiles, int valid, int shard_start,
-                                sga_stat *__restrict__ ws, uint32_t *err) {
-  constexpr int kStages = dec_stages<kN>;
-  constexpr int kStageBytes = dec_stage_bytes<kN>;
-  constexpr int kChunks = dec_chunks<kN>;
-  constexpr int kHalves = dec_halves<kN>;
-  constexpr int kTileIds = 128 * kHalves;
-  constexpr int kCols = 2 * kHalves * kN;  // halves x two accumulator buffers
-  constexpr int kG = kN < 32 ? kN : 32;  // rows per butterfly group
-  constexpr int kSlots = kN / kG;         // groups (rows held per lane)
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *base = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  SharedDec<kN> *sh = reinterpret_cast<SharedDec<kN> *>(base + kStages * kStageBytes);
-  const volatile int *abort_flag = &sh->abort;
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-
-  if (SGA_LMHEAD_DEC_PREFETCH && threadIdx.x == 64 && blockIdx.x < n_tiles) {
-    // Warm L2 with what the ring loads first (this CTA's first tile, one
-    // ring's worth of K blocks) while the previous kernel drains.  A prefetch
-    // only moves lines into L2, which stays coherent with any later write, so
-    // it may precede griddepcontrol.wait.
-    const int n = blockIdx.x;
-    for (int kb = 0; kb < num_kb && kb < kStages * kChunks; ++kb)
-      for (int h = 0; h < kHalves; ++h)
-        tma_prefetch_2d(&tmap_w, kb * kBk<kFp8>, n * kTileIds + h * 128);
-  }
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&sh->full[s]), 1);
-      mbar_init(smem_u32(&sh->empty[s]), 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&sh->tmem_full[b]), 1);
-      mbar_init(smem_u32(&sh->tmem_empty[b]), 4 * 32);
-    }
-    mbar_init(smem_u32(&sh->drain), 1);
-    sh->abort = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(&sh->tmem_base)),
-                 "r"(kCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = sh->tmem_base;
-  // launched with programmatic stream serialisation: everything above (barrier
-  // set-up, TMEM allocation) overlaps the previous kernel's tail; inputs and
-  // the workspace are touched only after that kernel has completed
-  pdl_wait();
-
-  int prod_stage = 0;
-  uint32_t prod_phase = 0;
-  long long issued = 0;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ producer
-      for (int n = blockIdx.x; n < n_tiles && !*abort_flag; n += gridDim.x) {
-        for (int kb = 0; kb < num_kb; kb += kChunks) {
-          if (!mbar_wait(smem_u32(&sh->empty[prod_stage]), prod_phase ^ 1, abort_flag)) {
-            raise_abort_dec(sh, err);
-            break;
-          }
-          const int chunks = num_kb - kb < kChunks ? num_kb - kb : kChunks;
-          const uint32_t full = smem_u32(&sh->full[prod_stage]);
-          const uint32_t stage_addr = smem_u32(base + prod_stage * kStageBytes);
-          mbar_expect_tx(full, chunks * (kHalves * DEC_SUB_BYTES + kN * ROW_BYTES));
-          for (int c = 0; c < chunks; ++c) {
-            for (int h = 0; h < kHalves; ++h)
-              tma_load_2d(stage_addr + (c * kHalves + h) * DEC_SUB_BYTES, &tmap_w,
-                          (kb + c) * kBk<kFp8>, n * kTileIds + h * 128, full);
-            tma_load_2d(stage_addr + dec_a_bytes<kN> + c * kN * ROW_BYTES, &tmap_h,
-                        (kb + c) * kBk<kFp8>, 0, full);
-          }
-          ++issued;
-          if (++prod_stage == kStages) {
-            prod_stage = 0;
-            prod_phase ^= 1;
-          }
-        }
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ----------------------------------------------------------- MMA issuer
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      for (int n = blockIdx.x; n < n_tiles && !*abort_flag; n += gridDim.x) {
-        if (!mbar_wait(smem_u32(&sh->tmem_empty[acc]), acc_phase ^ 1, abort_flag)) {
-          raise_abort_dec(sh, err);
-          break;
-        }
-        tc_fence_after();
-        bool ok = true;
-        for (int kb = 0; kb < num_kb; kb += kChunks) {
-          if (!mbar_wait(smem_u32(&sh->full[stage]), phase, abort_flag)) {
-            raise_abort_dec(sh, err);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const int chunks = num_kb - kb < kChunks ? num_kb - kb : kChunks;
-          const uint32_t stage_addr = smem_u32(base + stage * kStageBytes);
-          for (int c = 0; c < chunks; ++c) {
-            const uint64_t b_desc = smem_desc_sw128(stage_addr + dec_a_bytes<kN> + c * kN * ROW_BYTES);
-#pragma unroll
-            for (int h = 0; h < kHalves; ++h) {
-              const uint64_t a_desc =
-                  smem_desc_sw128(stage_addr + (c * kHalves + h) * DEC_SUB_BYTES);
-              const uint32_t d_tmem = tmem_base + (acc * kHalves + h) * kN;
-#pragma unroll
-              for (int kk = 0; kk < ROW_BYTES / 32; ++kk)  // 32 bytes = 2 descriptor units
-                mma_dec<kFp8, kN>(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk,
-                                  (kb | c | kk) != 0);
-            }
-          }
-          mma_commit(smem_u32(&sh->empty[stage]));
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
-        if (!ok) break;
-        mma_commit(smem_u32(&sh->tmem_full[acc]));
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1;
-      }
-    }
-  } else {
-    // ------------------------------------------------------------- epilogue
-    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 belong to this warp
-    float rv[kSlots];
-    int32_t ri[kSlots];
-#pragma unroll
-    for (int s = 0; s < kSlots; ++s) {
-      rv[s] = __int_as_float(0xff800000);
-      ri[s] = kNoId;
-    }
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    for (int n = blockIdx.x; n < n_tiles; n += gridDim.x) {
-      bool ok = mbar_wait(smem_u32(&sh->tmem_full[acc]), acc_phase, abort_flag);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) {
-        if (lane == 0) raise_abort_dec(sh, err);
-        break;
-      }
-      tc_fence_after();
-#pragma unroll 1
-      for (int h = 0; h < kHalves; ++h) {
-        const int local = n * kTileIds + h * 128 + quarter * 32 + lane;  // shard-local id
-        const bool live = local < valid;
-        const int32_t id = live ? shard_start + local : kNoId;
-        const uint32_t taddr =
-            tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + (acc * kHalves + h) * kN;
-#pragma unroll
-        for (int g = 0; g < kSlots; ++g) {
-          uint32_t r[kG];  // one group of columns at a time
-          tmem_ld_cols<kG>(taddr + g * kG, r);
-          tmem_ld_wait();
-          float x[kG];
-#pragma unroll
-          for (int k = 0; k < kG; ++k)
-            x[k] = live ? __uint_as_float(r[k]) : __int_as_float(0xff800000);
-          float v;
-          int32_t i;
-          rows_argmax<kG>(x, id, lane, v, i);
-          keep_better(rv[g], ri[g], v, i);
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&sh->tmem_empty[acc]));
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1;
-    }
-#pragma unroll
-    for (int g = 0; g < kSlots; ++g) {
-      // lane l holds row l of the group (kG = 32) or row l / 2 (kG = 16; both
-      // lanes of a pair hold it)
-      if (kG == 32 || (lane & 1) == 0) {
-        const int j = g * kG + (kG == 32 ? lane : lane >> 1);
-        sh->part_v[quarter][j] = rv[g];
-        sh->part_i[quarter][j] = ri[g];
-      }
-    }
-  }
-
-  pdl_launch_dependents();
-  __syncthreads();
-  if (*abort_flag) {
-    // Let this CTA's own copies and MMAs land before its shared memory and
-    // tensor memory are released (bounded as well).
-    const int zero = 0;
-    if (warp == 0 && lane == 0) {
-      const long long outstanding = issued < kStages ? issued : kStages;
-      for (long long i = 1; i <= outstanding; ++i) {
-        int s = prod_stage - static_cast<int>(i);
-        uint32_t ph = prod_phase;
-        if (s < 0) {
-          s += kStages;
-          ph ^= 1;
-        }
-        mbar_wait(smem_u32(&sh->full[s]), ph, &zero);
-      }
-    }
-    if (warp == 1 && lane == 0) {
-      mma_commit(smem_u32(&sh->drain));
-      mbar_wait(smem_u32(&sh->drain), 0, &zero);
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x < M) {
-    // merge the four epilogue warps' bests of row threadIdx.x (any order: the
-    // (value, id) order is total)
-    float v = sh->part_v[0][threadIdx.x];
-    int32_t id = sh->part_i[0][threadIdx.x];
-#pragma unroll
-    for (int q = 1; q < 4; ++q) {
-      const float cv = sh->part_v[q][threadIdx.x];
-      const int32_t ci = sh->part_i[q][threadIdx.x];
-      if (pair_beats(cv, ci, v, id)) {
-        v = cv;
-        id = ci;
-      }
-    }
-    sga_stat st;
-    st.v = v;
-    st.id = id;
-    ws[static_cast<size_t>(threadIdx.x) * gridDim.x + blockIdx.x] = st;
-  }
-  if (warp == 1) {
-    tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "r"(kCols)
                  : "memory");
   }
 }
@@ -1216,57 +659,6 @@ __global__ void selftest_timeout_kernel(unsigned long long limit_ns, uint32_t *e
   if (waited_ns) *waited_ns = global_timer_ns() - t0;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-// 2-D tensor map over a row-major [rows, cols] matrix of bf16 or fp8 (E4M3,
-// stored as bytes); box = box_rows x one 128-byte row (64 bf16 or 128 fp8
-// columns), 128-byte swizzle, zero fill outside.
-bool make_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, int box_rows,
-              bool fp8) {
-  auto encode = get_encode_fn();
-  if (encode == nullptr) return false;
-  const int elt = fp8 ? 1 : 2;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * elt)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(ROW_BYTES / elt), static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[2] = {1, 1};
-  return encode(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// Raise a kernel's dynamic shared-memory limit once per device (slot picks the
-// kernel), so that later calls, including calls inside a stream capture, make
-// no function-attribute call.
-cudaError_t set_smem_once(const void *kernel, int bytes, int slot) {
-  static std::mutex mu;
-  static bool done[12][64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!done[slot][dev]) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e != cudaSuccess) return e;
-    done[slot][dev] = true;
-  }
-  return cudaSuccess;
-}
-
 // Number of 2-CTA clusters of the 2-SM kernel that fit on the current device
 // at once (queried once per device and operand type).
 template <bool kFp8>
@@ -1291,48 +683,6 @@ int resident_pairs(int num_sms) {
   return cache[dev];
 }
 
-// Launch a GEMM kernel (THREADS threads per CTA) with programmatic stream
-// serialisation; the kernel calls griddepcontrol.wait after its prologue.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), int grid, int smem, cudaStream_t stream,
-                       Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, args...);
-}
-
-template <bool kFp8, int kN>
-cudaError_t launch_decode(const void *hidden, int64_t M, int64_t H, const void *weight,
-                          int64_t shard_start, int64_t valid, sga_stat *ws, int n_tiles,
-                          int num_sms, uint32_t *err, cudaStream_t stream, int *ws_stride) {
-  CUtensorMap map_w, map_h;
-  if (!make_map(&map_w, weight, valid, H, 128, kFp8) || !make_map(&map_h, hidden, M, H, kN, kFp8))
-    return cudaErrorInvalidValue;
-  auto kern = lmhead_argmax_decode_kernel<kFp8, kN>;
-  const int slot = 4 + (kFp8 ? 4 : 0) + (kN == 16 ? 0 : kN == 32 ? 1 : kN == 64 ? 2 : 3);
-  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), dec_smem_bytes<kN>, slot);
-  if (e != cudaSuccess) return e;
-  // one CTA per SM, at most one per tile; the workspace holds
-  // min(ceil(width / 128), kDecMaxParts) partials per row for M <= 64
-  (void)n_tiles;
-  const int tile_ids = 128 * dec_halves<kN>;
-  const int dec_tiles = static_cast<int>((valid + tile_ids - 1) / tile_ids);
-  int grid = dec_tiles < num_sms ? dec_tiles : num_sms;
-  if (grid > kDecMaxParts) grid = kDecMaxParts;
-  *ws_stride = grid;
-  return launch_pdl(kern, grid, dec_smem_bytes<kN>, stream, map_w, map_h, static_cast<int>(M),
-                    static_cast<int>(H / kBk<kFp8>), dec_tiles, static_cast<int>(valid),
-                    static_cast<int>(shard_start), ws, err);
-}
-
 // Partial statistics go to ws[row * (*ws_stride) + part]; *ws_stride <=
 // n_tiles, so a workspace of M x n_tiles stats always suffices.
 template <bool kFp8>
@@ -1341,16 +691,9 @@ cudaError_t launch_gemm(const void *hidden, int64_t M, int64_t H, const void *we
                         uint32_t *err, cudaStream_t stream, int *ws_stride) {
   const int num_kb = static_cast<int>(H / kBk<kFp8>);
   *ws_stride = n_tiles;
-  if (M <= SGA_LMHEAD_DECODE_MAX_M) {
-    if (M <= 16)
-      return launch_decode<kFp8, 16>(hidden, M, H, weight, shard_start, valid, ws, n_tiles,
-                                     num_sms, err, stream, ws_stride);
-    if (M <= 32)
-      return launch_decode<kFp8, 32>(hidden, M, H, weight, shard_start, valid, ws, n_tiles,
-                                     num_sms, err, stream, ws_stride);
-    return launch_decode<kFp8, 64>(hidden, M, H, weight, shard_start, valid, ws, n_tiles,
-                                   num_sms, err, stream, ws_stride);
-  }
+  if (M <= SGA_LMHEAD_DECODE_MAX_M)
+    return launch_lmhead_decode(kFp8, hidden, M, H, weight, shard_start, valid, ws, n_tiles,
+                                num_sms, err, stream, ws_stride);
   if (SGA_LMHEAD_2SM && M >= SGA_LMHEAD_2SM_MIN_M && num_sms >= 2) {
     // 2-SM tiles (256 rows per CTA pair)
     CUtensorMap map_a, map_b;

@@ -1,0 +1,477 @@
+// lmhead_decode.cu -- fused LM head + per-shard argmax at decode sizes
+// (M <= 64 hidden rows) on the tcgen05 tensor cores, with the weight as the
+// MMA's 128-row operand.
+//
+// vLLM PR #62604, Purpose (vocab-parallel LM head) and item 2 (fused
+// get_top_tokens); vLLM PR #39419, Changes (lm_head on the hidden states,
+// then the local argmax).  At decode sizes the step is a weight stream, so
+// this kernel is shaped for HBM, not for the tensor pipe.
+#include "tcgen05.cuh"
+
+namespace sga {
+namespace {
+
+// ---------------------------------------------------------------------------
+// Decode-size variant (M <= 64 hidden rows): the operands swap roles.  The
+// weight tile is the MMA's A operand (M = 128 vocab ids per MMA, two MMAs per
+// 256-id tile) and the hidden rows are its B operand (N = kN = 16, 32 or 64
+// columns).  A stage then holds 32-64 KB of weight and only kN x 128 B of
+// hidden per K chunk (instead of 128 hidden rows, mostly zero fill), and each
+// weight row is read 256-512 contiguous bytes at a time: at these sizes the
+// kernel is a weight stream, paced by the length of its DRAM runs and the
+// bytes in flight.
+// TMEM lane = vocab id, TMEM column = hidden row.  The epilogue reduces each
+// group of 32 (or 16) rows across the 32 lanes of a warp with a butterfly
+// transpose-reduce in the (value, id) order, after which each lane holds one
+// row's winner and keeps that row's running best; the four epilogue warps
+// merge through shared memory at the end and each CTA writes one partial per
+// row to the workspace (row stride = number of CTAs); the finalize kernel
+// merges the CTAs' partials.
+// ---------------------------------------------------------------------------
+// K chunks (128-byte columns of the weight) per stage: 1 -> a stage holds 256
+// weight rows x 128 B (a 256-id tile in two 128-row halves); 2 -> 128 rows x
+// 256 B (a 128-id tile: twice the contiguous bytes per row); 4 -> 128 rows x
+// 512 B.  Measured on GB300 (2 shards of 75968 x 4096, per step, bf16 / fp8):
+//   N = 16 (M <= 16): 1 chunk 199 / 113 us, 2 chunks 201 / 113, 4 chunks
+//                     193 / 108 (3 stages of 72 KB)
+//   N = 32, 64:       1 chunk 203-208 / 117-122 us, 2 chunks 196-200 /
+//                     110-115, 4 chunks 201-206 / 115-119 (only 2 stages)
+// Longer contiguous runs per weight row pay more than extra bytes in flight.
+#ifndef SGA_LMHEAD_DEC_PREFETCH
+// L2 prefetch of the first stages before the PDL wait.  Measured (graph
+// replay, 8 shards of 18992 ids): bf16 M = 1 223.7 -> 219.7 us per step, fp8
+// 137.6 -> 133.2 us; 2 shards of 75968 ids unchanged.
+#define SGA_LMHEAD_DEC_PREFETCH 1
+#endif
+#ifndef SGA_LMHEAD_DEC_CHUNKS_N16
+#define SGA_LMHEAD_DEC_CHUNKS_N16 4
+#endif
+#ifndef SGA_LMHEAD_DEC_CHUNKS
+#define SGA_LMHEAD_DEC_CHUNKS 2
+#endif
+template <int kN>
+constexpr int dec_chunks = kN <= 16 ? SGA_LMHEAD_DEC_CHUNKS_N16 : SGA_LMHEAD_DEC_CHUNKS;
+template <int kN>
+constexpr int dec_halves = dec_chunks<kN> >= 2 ? 1 : 2;  // 128-id halves per tile
+constexpr int DEC_SUB_BYTES = 128 * ROW_BYTES;            // one 128-row x 128-byte box
+template <int kN>
+constexpr int dec_a_bytes = dec_chunks<kN> * dec_halves<kN> * DEC_SUB_BYTES;
+template <int kN>
+constexpr int dec_stage_bytes = dec_a_bytes<kN> + dec_chunks<kN> * kN * ROW_BYTES;
+template <int kN>
+constexpr int dec_stages = (227 * 1024 - 4096) / dec_stage_bytes<kN>;  // 3, 5, 4
+
+template <int kN>
+struct SharedDec {
+  uint64_t full[dec_stages<kN>];
+  uint64_t empty[dec_stages<kN>];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  float part_v[4][kN];
+  int32_t part_i[4][kN];
+};
+
+template <int kN>
+constexpr int dec_smem_bytes =
+    1024 + dec_stages<kN> * dec_stage_bytes<kN> + static_cast<int>(sizeof(SharedDec<kN>));
+static_assert(dec_smem_bytes<16> <= 227 * 1024 && dec_smem_bytes<32> <= 227 * 1024 &&
+                  dec_smem_bytes<64> <= 227 * 1024,
+              "decode-size LM-head ring exceeds shared memory");
+
+template <int kN>
+__device__ __forceinline__ void raise_abort_dec(SharedDec<kN> *sh, uint32_t *err) {
+  *reinterpret_cast<volatile int *>(&sh->abort) = 1;
+  atomicOr(err, SGA_DEVERR_TIMEOUT);
+}
+
+// One MMA of a K step with M = 128 (weight rows) and N = kN (hidden rows).
+template <bool kFp8, int kN>
+__device__ __forceinline__ void mma_dec(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t accumulate) {
+  constexpr uint32_t idesc = instr_desc<kFp8>(128, kN);
+  if constexpr (kFp8) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+// Load kN accumulator columns of this warp's 32 TMEM lanes (x16 loads).
+template <int kN>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[kN]) {
+#pragma unroll
+  for (int c = 0; c < kN / 16; ++c) tmem_ld16(taddr + 16 * c, r + 16 * c);
+}
+
+__device__ __forceinline__ void keep_better(float &v, int32_t &i, float ov, int32_t oi) {
+  if (pair_beats(ov, oi, v, i)) {
+    v = ov;
+    i = oi;
+  }
+}
+
+// Transpose-reduce of G rows (G = 16 or 32) across the 32 lanes of a warp:
+// lane l holds x[k] = the logit of row k at its own vocab id `id`.  Each
+// butterfly step pairs lane l with l ^ s; the lane with bit s set keeps the
+// upper half of its current rows and receives the partner's values of them,
+// the other lane keeps the lower half, and both merge with the (value, id)
+// order.  After 31 merges (instead of 5 shuffle rounds per row), lane l holds
+// the argmax over the warp's 32 ids of row l (G = 32) or row l / 2 (G = 16).
+template <int kCnt, int kS>
+__device__ __forceinline__ void butterfly_step(float *x, int32_t *xi, int lane) {
+  if constexpr (kS >= 1) {
+    if constexpr (kCnt > 1) {
+      constexpr int kHalf = kCnt / 2;
+      const bool upper = (lane & kS) != 0;
+#pragma unroll
+      for (int k = 0; k < kHalf; ++k) {
+        const float sv = upper ? x[k] : x[kHalf + k];
+        const int32_t si = upper ? xi[k] : xi[kHalf + k];
+        float kv = upper ? x[kHalf + k] : x[k];
+        int32_t ki = upper ? xi[kHalf + k] : xi[k];
+        keep_better(kv, ki, __shfl_xor_sync(0xffffffffu, sv, kS),
+                    __shfl_xor_sync(0xffffffffu, si, kS));
+        x[k] = kv;
+        xi[k] = ki;
+      }
+      butterfly_step<kHalf, kS / 2>(x, xi, lane);
+    } else {
+      keep_better(x[0], xi[0], __shfl_xor_sync(0xffffffffu, x[0], kS),
+                  __shfl_xor_sync(0xffffffffu, xi[0], kS));
+      butterfly_step<1, kS / 2>(x, xi, lane);
+    }
+  }
+}
+
+template <int G>
+__device__ __forceinline__ void rows_argmax(float (&x)[G], int32_t id, int lane, float &out_v,
+                                            int32_t &out_i) {
+  int32_t xi[G];
+#pragma unroll
+  for (int k = 0; k < G; ++k) xi[k] = id;
+  butterfly_step<G, 16>(x, xi, lane);
+  out_v = x[0];
+  out_i = xi[0];
+}
+
+template <bool kFp8, int kN>
+__global__ void __launch_bounds__(THREADS, 1)
+    lmhead_argmax_decode_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                                const __grid_constant__ CUtensorMap tmap_h, int M, int num_kb,
+                                int n_tiles, int valid, int shard_start,
+                                sga_stat *__restrict__ ws, uint32_t *err) {
+  constexpr int kStages = dec_stages<kN>;
+  constexpr int kStageBytes = dec_stage_bytes<kN>;
+  constexpr int kChunks = dec_chunks<kN>;
+  constexpr int kHalves = dec_halves<kN>;
+  constexpr int kTileIds = 128 * kHalves;
+  constexpr int kCols = 2 * kHalves * kN;  // halves x two accumulator buffers
+  constexpr int kG = kN < 32 ? kN : 32;  // rows per butterfly group
+  constexpr int kSlots = kN / kG;         // groups (rows held per lane)
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *base = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  SharedDec<kN> *sh = reinterpret_cast<SharedDec<kN> *>(base + kStages * kStageBytes);
+  const volatile int *abort_flag = &sh->abort;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (SGA_LMHEAD_DEC_PREFETCH && threadIdx.x == 64 && blockIdx.x < n_tiles) {
+    // Warm L2 with what the ring loads first (this CTA's first tile, one
+    // ring's worth of K blocks) while the previous kernel drains.  A prefetch
+    // only moves lines into L2, which stays coherent with any later write, so
+    // it may precede griddepcontrol.wait.
+    const int n = blockIdx.x;
+    for (int kb = 0; kb < num_kb && kb < kStages * kChunks; ++kb)
+      for (int h = 0; h < kHalves; ++h)
+        tma_prefetch_2d(&tmap_w, kb * kBk<kFp8>, n * kTileIds + h * 128);
+  }
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&sh->full[s]), 1);
+      mbar_init(smem_u32(&sh->empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&sh->tmem_full[b]), 1);
+      mbar_init(smem_u32(&sh->tmem_empty[b]), 4 * 32);
+    }
+    mbar_init(smem_u32(&sh->drain), 1);
+    sh->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&sh->tmem_base)),
+                 "r"(kCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = sh->tmem_base;
+  // launched with programmatic stream serialisation: everything above (barrier
+  // set-up, TMEM allocation) overlaps the previous kernel's tail; inputs and
+  // the workspace are touched only after that kernel has completed
+  pdl_wait();
+
+  int prod_stage = 0;
+  uint32_t prod_phase = 0;
+  long long issued = 0;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      for (int n = blockIdx.x; n < n_tiles && !*abort_flag; n += gridDim.x) {
+        for (int kb = 0; kb < num_kb; kb += kChunks) {
+          if (!mbar_wait(smem_u32(&sh->empty[prod_stage]), prod_phase ^ 1, abort_flag)) {
+            raise_abort_dec(sh, err);
+            break;
+          }
+          const int chunks = num_kb - kb < kChunks ? num_kb - kb : kChunks;
+          const uint32_t full = smem_u32(&sh->full[prod_stage]);
+          const uint32_t stage_addr = smem_u32(base + prod_stage * kStageBytes);
+          mbar_expect_tx(full, chunks * (kHalves * DEC_SUB_BYTES + kN * ROW_BYTES));
+          for (int c = 0; c < chunks; ++c) {
+            for (int h = 0; h < kHalves; ++h)
+              tma_load_2d(stage_addr + (c * kHalves + h) * DEC_SUB_BYTES, &tmap_w,
+                          (kb + c) * kBk<kFp8>, n * kTileIds + h * 128, full);
+            tma_load_2d(stage_addr + dec_a_bytes<kN> + c * kN * ROW_BYTES, &tmap_h,
+                        (kb + c) * kBk<kFp8>, 0, full);
+          }
+          ++issued;
+          if (++prod_stage == kStages) {
+            prod_stage = 0;
+            prod_phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ----------------------------------------------------------- MMA issuer
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      for (int n = blockIdx.x; n < n_tiles && !*abort_flag; n += gridDim.x) {
+        if (!mbar_wait(smem_u32(&sh->tmem_empty[acc]), acc_phase ^ 1, abort_flag)) {
+          raise_abort_dec(sh, err);
+          break;
+        }
+        tc_fence_after();
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; kb += kChunks) {
+          if (!mbar_wait(smem_u32(&sh->full[stage]), phase, abort_flag)) {
+            raise_abort_dec(sh, err);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int chunks = num_kb - kb < kChunks ? num_kb - kb : kChunks;
+          const uint32_t stage_addr = smem_u32(base + stage * kStageBytes);
+          for (int c = 0; c < chunks; ++c) {
+            const uint64_t b_desc = smem_desc_sw128(stage_addr + dec_a_bytes<kN> + c * kN * ROW_BYTES);
+#pragma unroll
+            for (int h = 0; h < kHalves; ++h) {
+              const uint64_t a_desc =
+                  smem_desc_sw128(stage_addr + (c * kHalves + h) * DEC_SUB_BYTES);
+              const uint32_t d_tmem = tmem_base + (acc * kHalves + h) * kN;
+#pragma unroll
+              for (int kk = 0; kk < ROW_BYTES / 32; ++kk)  // 32 bytes = 2 descriptor units
+                mma_dec<kFp8, kN>(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk,
+                                  (kb | c | kk) != 0);
+            }
+          }
+          mma_commit(smem_u32(&sh->empty[stage]));
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&sh->tmem_full[acc]));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 belong to this warp
+    float rv[kSlots];
+    int32_t ri[kSlots];
+#pragma unroll
+    for (int s = 0; s < kSlots; ++s) {
+      rv[s] = __int_as_float(0xff800000);
+      ri[s] = kNoId;
+    }
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int n = blockIdx.x; n < n_tiles; n += gridDim.x) {
+      bool ok = mbar_wait(smem_u32(&sh->tmem_full[acc]), acc_phase, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        if (lane == 0) raise_abort_dec(sh, err);
+        break;
+      }
+      tc_fence_after();
+#pragma unroll 1
+      for (int h = 0; h < kHalves; ++h) {
+        const int local = n * kTileIds + h * 128 + quarter * 32 + lane;  // shard-local id
+        const bool live = local < valid;
+        const int32_t id = live ? shard_start + local : kNoId;
+        const uint32_t taddr =
+            tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + (acc * kHalves + h) * kN;
+#pragma unroll
+        for (int g = 0; g < kSlots; ++g) {
+          uint32_t r[kG];  // one group of columns at a time
+          tmem_ld_cols<kG>(taddr + g * kG, r);
+          tmem_ld_wait();
+          float x[kG];
+#pragma unroll
+          for (int k = 0; k < kG; ++k)
+            x[k] = live ? __uint_as_float(r[k]) : __int_as_float(0xff800000);
+          float v;
+          int32_t i;
+          rows_argmax<kG>(x, id, lane, v, i);
+          keep_better(rv[g], ri[g], v, i);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sh->tmem_empty[acc]));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+#pragma unroll
+    for (int g = 0; g < kSlots; ++g) {
+      // lane l holds row l of the group (kG = 32) or row l / 2 (kG = 16; both
+      // lanes of a pair hold it)
+      if (kG == 32 || (lane & 1) == 0) {
+        const int j = g * kG + (kG == 32 ? lane : lane >> 1);
+        sh->part_v[quarter][j] = rv[g];
+        sh->part_i[quarter][j] = ri[g];
+      }
+    }
+  }
+
+  pdl_launch_dependents();
+  __syncthreads();
+  if (*abort_flag) {
+    // Let this CTA's own copies and MMAs land before its shared memory and
+    // tensor memory are released (bounded as well).
+    const int zero = 0;
+    if (warp == 0 && lane == 0) {
+      const long long outstanding = issued < kStages ? issued : kStages;
+      for (long long i = 1; i <= outstanding; ++i) {
+        int s = prod_stage - static_cast<int>(i);
+        uint32_t ph = prod_phase;
+        if (s < 0) {
+          s += kStages;
+          ph ^= 1;
+        }
+        mbar_wait(smem_u32(&sh->full[s]), ph, &zero);
+      }
+    }
+    if (warp == 1 && lane == 0) {
+      mma_commit(smem_u32(&sh->drain));
+      mbar_wait(smem_u32(&sh->drain), 0, &zero);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < M) {
+    // merge the four epilogue warps' bests of row threadIdx.x (any order: the
+    // (value, id) order is total)
+    float v = sh->part_v[0][threadIdx.x];
+    int32_t id = sh->part_i[0][threadIdx.x];
+#pragma unroll
+    for (int q = 1; q < 4; ++q) {
+      const float cv = sh->part_v[q][threadIdx.x];
+      const int32_t ci = sh->part_i[q][threadIdx.x];
+      if (pair_beats(cv, ci, v, id)) {
+        v = cv;
+        id = ci;
+      }
+    }
+    sga_stat st;
+    st.v = v;
+    st.id = id;
+    ws[static_cast<size_t>(threadIdx.x) * gridDim.x + blockIdx.x] = st;
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(kCols)
+                 : "memory");
+  }
+}
+
+template <bool kFp8, int kN>
+cudaError_t launch_decode(const void *hidden, int64_t M, int64_t H, const void *weight,
+                          int64_t shard_start, int64_t valid, sga_stat *ws, int n_tiles,
+                          int num_sms, uint32_t *err, cudaStream_t stream, int *ws_stride) {
+  CUtensorMap map_w, map_h;
+  if (!make_map(&map_w, weight, valid, H, 128, kFp8) || !make_map(&map_h, hidden, M, H, kN, kFp8))
+    return cudaErrorInvalidValue;
+  auto kern = lmhead_argmax_decode_kernel<kFp8, kN>;
+  const int slot = 4 + (kFp8 ? 4 : 0) + (kN == 16 ? 0 : kN == 32 ? 1 : kN == 64 ? 2 : 3);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), dec_smem_bytes<kN>, slot);
+  if (e != cudaSuccess) return e;
+  // one CTA per SM, at most one per tile; the workspace holds
+  // min(ceil(width / 128), kDecMaxParts) partials per row for M <= 64
+  (void)n_tiles;
+  const int tile_ids = 128 * dec_halves<kN>;
+  const int dec_tiles = static_cast<int>((valid + tile_ids - 1) / tile_ids);
+  int grid = dec_tiles < num_sms ? dec_tiles : num_sms;
+  if (grid > kDecMaxParts) grid = kDecMaxParts;
+  *ws_stride = grid;
+  return launch_pdl(kern, grid, dec_smem_bytes<kN>, stream, map_w, map_h, static_cast<int>(M),
+                    static_cast<int>(H / kBk<kFp8>), dec_tiles, static_cast<int>(valid),
+                    static_cast<int>(shard_start), ws, err);
+}
+
+}  // namespace
+
+cudaError_t launch_lmhead_decode(bool fp8, const void *hidden, int64_t M, int64_t H,
+                                 const void *weight, int64_t shard_start, int64_t valid,
+                                 sga_stat *ws, int n_tiles, int num_sms, uint32_t *err,
+                                 cudaStream_t stream, int *ws_stride) {
+  if (M <= 16)
+    return fp8 ? launch_decode<true, 16>(hidden, M, H, weight, shard_start, valid, ws, n_tiles,
+                                         num_sms, err, stream, ws_stride)
+               : launch_decode<false, 16>(hidden, M, H, weight, shard_start, valid, ws, n_tiles,
+                                          num_sms, err, stream, ws_stride);
+  if (M <= 32)
+    return fp8 ? launch_decode<true, 32>(hidden, M, H, weight, shard_start, valid, ws, n_tiles,
+                                         num_sms, err, stream, ws_stride)
+               : launch_decode<false, 32>(hidden, M, H, weight, shard_start, valid, ws, n_tiles,
+                                          num_sms, err, stream, ws_stride);
+  return fp8 ? launch_decode<true, 64>(hidden, M, H, weight, shard_start, valid, ws, n_tiles,
+                                       num_sms, err, stream, ws_stride)
+             : launch_decode<false, 64>(hidden, M, H, weight, shard_start, valid, ws, n_tiles,
+                                        num_sms, err, stream, ws_stride);
+}
+
+}  // namespace sga
