@@ -18,19 +18,25 @@
 // precedes it.  Output layout: out[(slot0_s + p) * rows + r] (piece-major,
 // shards in order, like the shard-major gathered buffer).
 //
-// Design: the grid is (row group, part): a row group is one request (its K_i
-// draft rows and its bonus row, read from two entries of cu_num_draft, so no
-// warp ever searches for the kind of its row) or, without cu_num_draft, 16
-// draft rows.  The group's real pieces (per shard, K_i x draft count + bonus
-// count) are dealt round-robin to the parts x 4 warps of the group; a warp
-// streams its
-// piece with 16-byte loads, kUnroll in flight per lane, keeps the best
-// vector in registers (the steps of the per-shard kernel), merges across
-// the warp and stores one stat.  The empty slots (all but a few of a draft
-// row's slots when the bonus block is the smaller one) are plain stores,
-// spread over every thread of the group.  Parts are chosen so that the grid
-// is one wave of resident CTAs.  A piece is at most one block (8192 ids
-// = 16 KB of bf16): too short for the per-shard kernel's bulk-copy ring.
+// Design.  The real pieces of the launch are numbered flat: request by
+// request (its K_i draft rows and its bonus row), inside a request shard by
+// shard, then row, then piece, so consecutive numbers are consecutive memory.
+// With D = the draft blocks and Bn = the bonus blocks met by all the shards
+// of the launch, request i's pieces start at number cu[i] * D + i * Bn, a
+// closed form: a warp finds the request of its first piece with one binary
+// search over cu_num_draft and then walks forward.  Every CTA of the grid
+// (one wave of resident CTAs) takes an equal contiguous range of numbers,
+// dealt round-robin to its warps (so a CTA's warps read neighbouring
+// pieces), and the load is balanced whatever the number of requests and
+// their K_i.  A
+// warp scans a piece as the per-shard kernel scans a row: 16-byte vectors
+// with kUnroll streaming loads in flight per lane, the best vector kept in
+// registers and searched once; the element head (to the first 16-byte
+// boundary) and tail are loaded before the vectors so that their latency
+// overlaps; then a merge across the warp and one stat.  The empty slots (all
+// but a few of a draft row's slots when the bonus block is the smaller one)
+// are plain stores, one thread per row.  Without cu_num_draft every row is a
+// request of one draft row and no bonus row.
 #include "common.cuh"
 #include "scan.cuh"
 
@@ -38,30 +44,47 @@ namespace sga {
 namespace {
 
 // Tuning knobs (compile-time): warps per CTA, 16-byte loads in flight per
-// lane, and the resident CTAs per SM the grid is sized for (0: the
-// occupancy calculator's number).  Measured on GB300, large-verify shape
-// (4096 x 202048 bf16, 3 shards, blocks 8192 / 1024, one launch per shard):
-// 4 warps x 16 loads 254.5 us for the three launches (6.50 TB/s); 2 x 16 and
-// 4 x 32 within 1 us of it; 8 x 8 302 us; 16 x 16 283 us; sizing the grid for
-// 2 CTAs per SM instead of the occupancy limit 486 us.  Before the grid was
-// sized to one wave (a partial second wave of a third of the CTAs) 8 x 8
-// took 383 us.
+// lane, the CTAs per SM the registers are budgeted for (the second launch
+// bound: without it the compiler keeps the kernel near 48 registers, too few
+// for the loads in flight), the resident CTAs per SM the grid is sized for
+// (0: the occupancy calculator's number), and how a CTA's range is split
+// (1: round-robin over its warps, 0: a contiguous sub-range per warp).
+// Measured on GB300 with CUDA events around each launch (launches kept
+// apart), large-verify logits (202048 bf16 ids, 3 shards in one launch,
+// blocks 8192 / 1024), 256 requests:
+//   K_i = 15 (4096 rows): 4 warps x 16 loads, 5 CTAs per SM, round-robin
+//     247.8 us (6.68 TB/s); a contiguous sub-range per warp 268.3 us; 8 CTAs
+//     per SM with 8 loads 258-271 us; 10 per SM 268-278 us; 12 per SM with
+//     4 loads 284.7 us; two, four or eight waves of smaller CTAs 274.4,
+//     262.1, 256.0 us; launched without programmatic dependent launch: no
+//     change;
+//   K_i uniform in 0..15 (2271 rows): 172.0 us;
+//   64 requests of K_i = 15 and 192 of K_i = 0 (1216 rows): 118.8 us.
+// The earlier kernel (whole CTAs per request, as many for a request of 0
+// drafts as for one of 15) took 250.2, 189.2 and 162.4 us on these three.
 #ifndef SGA_BLOCKS_WARPS
 #define SGA_BLOCKS_WARPS 4
 #endif
 #ifndef SGA_BLOCKS_UNROLL
 #define SGA_BLOCKS_UNROLL 16
 #endif
+#ifndef SGA_BLOCKS_MIN_CTAS
+#define SGA_BLOCKS_MIN_CTAS 5
+#endif
 #ifndef SGA_BLOCKS_CTAS_PER_SM
 #define SGA_BLOCKS_CTAS_PER_SM 0
 #endif
+#ifndef SGA_BLOCKS_INTERLEAVE
+#define SGA_BLOCKS_INTERLEAVE 1
+#endif
 constexpr int kWarpsPerCta = SGA_BLOCKS_WARPS;
 constexpr int kUnroll = SGA_BLOCKS_UNROLL;
-constexpr int kGroupRows = 16;   // rows per group without a request layout
 
 // The shards of one launch: shard s covers global ids [start, start + width),
-// held at column col of `logits`, and owns the slots slot0 .. slot0 + slots - 1
-// of every row in the gathered statistics.
+// held at column col of `logits`, owns the slots slot0 .. slot0 + slots - 1 of
+// every row in the gathered statistics, and meets cnt_d draft blocks and
+// cnt_b bonus blocks; pre_d / pre_b are the prefix sums of cnt_d / cnt_b over
+// the shards (pre_d[n] = D, pre_b[n] = Bn).
 struct BlockShardTable {
   int n;
   int32_t start[kMaxBlockShards];
@@ -69,38 +92,152 @@ struct BlockShardTable {
   int32_t width[kMaxBlockShards];
   int32_t slot0[kMaxBlockShards];
   int32_t slots[kMaxBlockShards];
+  int32_t cnt_d[kMaxBlockShards];
+  int32_t cnt_b[kMaxBlockShards];
+  int32_t pre_d[kMaxBlockShards + 1];
+  int32_t pre_b[kMaxBlockShards + 1];
 };
 
-// Argmax (value, global id) of the non-padding ids [lo, hi) of row r, the
-// shard's column 0 being global id shard_start; computed by the whole warp,
-// every lane returns the result.  hi <= lo: no element, (-inf, lo).
+// One piece: the non-padding ids [lo, lo + n) of one row inside one block
+// and one shard, at address q in the logits, and where its stat goes.
+struct Piece {
+  const char *q;
+  int32_t lo;
+  int32_t n;
+  int64_t out_idx;
+};
+
+// How a piece splits into an element head up to the first 16-byte boundary,
+// whole 16-byte vectors and an element tail.
 template <bool kBf16>
-__device__ __forceinline__ sga_stat piece_argmax(const char *__restrict__ row, int32_t shard_start,
-                                                 int32_t lo, int32_t hi, int lane) {
+struct Split {
+  int head, nvec, tail;
+  __device__ __forceinline__ explicit Split(const Piece &pc) {
+    constexpr int kElt = kBf16 ? 2 : 4;
+    constexpr int kVec = 16 / kElt;
+    head = static_cast<int>(((16u - (reinterpret_cast<uintptr_t>(pc.q) & 15u)) & 15u) / kElt);
+    if (head > pc.n) head = pc.n;
+    nvec = (pc.n - head) / kVec;
+    tail = pc.n - head - nvec * kVec;
+  }
+};
+
+// One request of the launch: its first row, its k draft rows, whether row
+// first + k is its bonus row, the number of its first piece and its piece
+// count, and whether its rows lie inside [0, rows).  Without cu_num_draft,
+// request g is row g alone, a draft row.
+struct Request {
+  int64_t first;
+  int64_t item0;
+  int32_t k;
+  int32_t bonus;
+  int32_t n_items;
+  bool valid;
+};
+
+__device__ __forceinline__ int64_t clamp_rows(int32_t c, int64_t rows) {
+  return c < 0 ? 0 : (c > rows ? rows : static_cast<int64_t>(c));
+}
+
+// Number of the first piece of request g (cu_num_draft entries clamped to
+// [0, rows], so that a broken layout still gives numbers in range).
+__device__ __forceinline__ int64_t item0_of(int64_t g, const int32_t *__restrict__ cu,
+                                            int64_t rows, int32_t d, int32_t bn) {
+  if (cu == nullptr) return g * d;
+  return clamp_rows(__ldg(cu + g), rows) * d + g * bn;
+}
+
+__device__ __forceinline__ Request request_of(int64_t g, const int32_t *__restrict__ cu,
+                                              int64_t rows, int32_t d, int32_t bn) {
+  Request q;
+  if (cu == nullptr) {
+    q.first = g;
+    q.k = 1;
+    q.bonus = 0;
+    q.item0 = g * d;
+    q.n_items = d;
+    q.valid = true;
+    return q;
+  }
+  const int32_t c0 = __ldg(cu + g), c1 = __ldg(cu + g + 1);
+  q.first = static_cast<int64_t>(c0) + g;
+  q.k = c1 - c0;
+  q.bonus = 1;
+  q.valid = c0 >= 0 && c1 >= c0 && static_cast<int64_t>(c1) + g < rows;
+  q.item0 = clamp_rows(c0, rows) * d + g * bn;
+  q.n_items = q.valid ? q.k * d + bn : 0;
+  return q;
+}
+
+// The request holding piece number t: the largest g in [0, n) whose first
+// piece is at or before t.
+__device__ __forceinline__ int64_t request_at(int64_t t, int64_t n, const int32_t *__restrict__ cu,
+                                              int64_t rows, int32_t d, int32_t bn) {
+  if (cu == nullptr) return t / d;
+  int64_t lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int64_t mid = (lo + hi + 1) >> 1;
+    if (item0_of(mid, cu, rows, d, bn) <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Piece u (0 <= u < q.n_items) of request q.  `s` is the caller's shard
+// cursor inside the request: its pieces only increase, so it only advances.
+template <bool kBf16>
+__device__ __forceinline__ Piece piece_of(int32_t u, int &s, const Request &q,
+                                          const BlockShardTable &tab, int32_t org_vocab,
+                                          int32_t draft_block, int32_t bonus_block,
+                                          const char *logits, int64_t ld_bytes, int64_t rows) {
+  constexpr int kElt = kBf16 ? 2 : 4;
+  while (u >= q.k * tab.pre_d[s + 1] + q.bonus * tab.pre_b[s + 1]) ++s;
+  const int32_t v = u - (q.k * tab.pre_d[s] + q.bonus * tab.pre_b[s]);
+  const int32_t sd = q.k * tab.cnt_d[s];
+  int32_t rr, p, B;
+  if (v < sd) {
+    rr = v / tab.cnt_d[s];
+    p = v - rr * tab.cnt_d[s];
+    B = draft_block;
+  } else {
+    rr = q.k;
+    p = v - sd;
+    B = bonus_block;
+  }
+  const int32_t st = tab.start[s], en = st + tab.width[s];
+  const int32_t b = st / B + p;
+  const int32_t lo = max(st, b * B);
+  const int32_t hi = min(min(en, b * B + B), org_vocab);
+  const int64_t r = q.first + rr;
+  Piece pc;
+  pc.lo = lo;
+  pc.n = hi > lo ? hi - lo : 0;
+  pc.q = logits + r * ld_bytes + static_cast<int64_t>(tab.col[s] + (lo - st)) * kElt;
+  pc.out_idx = static_cast<int64_t>(tab.slot0[s] + p) * rows + r;
+  return pc;
+}
+
+// Argmax (value, global id) of one piece, computed by the whole warp; every
+// lane returns the result.  No element: (-inf, lo).  Per lane the scan order
+// is ascending ids (head element, vectors, tail element), then the merge
+// across the warp takes the full (value, id) order.
+template <bool kBf16>
+__device__ __forceinline__ sga_stat piece_argmax(const Piece &pc, int lane) {
   constexpr int kElt = kBf16 ? 2 : 4;
   constexpr int kVec = 16 / kElt;
-  const int n = hi > lo ? hi - lo : 0;
-  const char *q = row + static_cast<int64_t>(lo - shard_start) * kElt;
-  int head = static_cast<int>(((16u - (reinterpret_cast<uintptr_t>(q) & 15u)) & 15u) / kElt);
-  if (head > n) head = n;
-  const int nvec = (n - head) / kVec;
-  const int tail = n - head - nvec * kVec;
+  const Split<kBf16> sp(pc);
+  // the lane's head and tail elements, loaded first so that their latency
+  // overlaps the vector loads
+  float head_x = __int_as_float(0xff800000), tail_x = __int_as_float(0xff800000);
+  if (lane < sp.head) head_x = load_elem<kBf16>(pc.q, lane);
+  if (lane < sp.tail) tail_x = load_elem<kBf16>(pc.q, sp.head + sp.nvec * kVec + lane);
 
-  float best = __int_as_float(0xff800000);  // -inf
-  int32_t best_id = kNoId;
-  if (lane < head) {
-    const float x = load_elem<kBf16>(q, lane);
-    if (scan_better(x, best)) {
-      best = x;
-      best_id = lo + lane;
-    }
-  }
-  const uint4 *vp = reinterpret_cast<const uint4 *>(q + head * kElt);
+  const uint4 *vp = reinterpret_cast<const uint4 *>(pc.q + sp.head * kElt);
   float vbest = __int_as_float(0xff800000);
   int vbest_idx = -1;
   uint4 vraw = make_uint4(0u, 0u, 0u, 0u);
   int v = lane;
-  for (; v + (kUnroll - 1) * 32 < nvec; v += kUnroll * 32) {
+  for (; v + (kUnroll - 1) * 32 < sp.nvec; v += kUnroll * 32) {
     uint4 a[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) a[u] = ld_stream_v4(vp + v + u * 32);
@@ -115,7 +252,7 @@ __device__ __forceinline__ sga_stat piece_argmax(const char *__restrict__ row, i
     }
   }
 #pragma unroll 4
-  for (; v < nvec; v += 32) {
+  for (; v < sp.nvec; v += 32) {
     const uint4 a = ld_stream_v4(vp + v);
     const float m = vec_max<kBf16>(a);
     if (scan_better(m, vbest)) {
@@ -124,128 +261,120 @@ __device__ __forceinline__ sga_stat piece_argmax(const char *__restrict__ row, i
       vraw = a;
     }
   }
-  if (vbest_idx >= 0) scan_vec<kBf16>(vraw, lo + head + vbest_idx * kVec, best, best_id);
-  if (lane < tail) {
-    const int j = head + nvec * kVec + lane;
-    const float x = load_elem<kBf16>(q, j);
-    if (scan_better(x, best)) {
-      best = x;
-      best_id = lo + j;
-    }
+
+  float best = __int_as_float(0xff800000);
+  int32_t best_id = kNoId;
+  if (lane < sp.head && scan_better(head_x, best)) {
+    best = head_x;
+    best_id = pc.lo + lane;
+  }
+  if (vbest_idx >= 0) scan_vec<kBf16>(vraw, pc.lo + sp.head + vbest_idx * kVec, best, best_id);
+  if (lane < sp.tail && scan_better(tail_x, best)) {
+    best = tail_x;
+    best_id = pc.lo + sp.head + sp.nvec * kVec + lane;
   }
   warp_argmax(best, best_id);
   sga_stat st;
   st.v = best;  // -inf when nothing beat -inf
-  st.id = best_id == kNoId ? lo : best_id;
+  st.id = best_id == kNoId ? pc.lo : best_id;
   return st;
 }
 
-// grid.x = groups x parts; CTA b: group b / parts, part b % parts.  The
-// shards of the table are processed in one launch: a group's real pieces are
-// numbered shard by shard (then row, then piece), so consecutive items still
-// stream consecutive memory.  Ids and block sizes are below 2^24 + 1 and a
-// group's pieces below 2^31, so the per-piece arithmetic is 32-bit.
+// grid.x = C = resident CTAs (at most); CTA c takes the pieces numbered
+// [T c / C, T (c + 1) / C), its warp j every kWarpsPerCta-th of them from
+// the j-th on (or, without interleaving, warp w of W takes [T w / W,
+// T (w + 1) / W)).  num_groups = num_reqs with cu_num_draft, else
+// rows.  Ids and block sizes are below 2^24 + 1 and rows x slots below 2^28,
+// so the arithmetic inside a request is 32-bit.
 template <bool kBf16>
-__global__ void __launch_bounds__(kWarpsPerCta * 32)
+__global__ void __launch_bounds__(kWarpsPerCta * 32, SGA_BLOCKS_MIN_CTAS)
     block_argmax_kernel(const char *__restrict__ logits, int64_t ld_bytes, int64_t rows,
                         const __grid_constant__ BlockShardTable tab, int32_t org_vocab,
-                        int32_t draft_block, int32_t bonus_block, int parts,
+                        int32_t draft_block, int32_t bonus_block, int64_t num_groups,
                         const int32_t *__restrict__ cu, sga_stat *__restrict__ out,
                         uint32_t *err) {
-  constexpr int kElt = kBf16 ? 2 : 4;
-  __shared__ int32_t cnt_d[kMaxBlockShards], cnt_b[kMaxBlockShards];
-  __shared__ int32_t item0[kMaxBlockShards + 1], empty0[kMaxBlockShards + 1];
   pdl_wait();
-  const int g = static_cast<int>(blockIdx.x / parts);
-  const int part = static_cast<int>(blockIdx.x % parts);
   const int lane = threadIdx.x & 31;
-  int64_t first;  // first row of the group
-  int n_draft;    // draft rows first .. first + n_draft - 1
-  int n_bonus;    // 1: row first + n_draft is the group's bonus row
-  if (cu != nullptr) {
-    const int32_t c0 = cu[g], c1 = cu[g + 1];
-    first = static_cast<int64_t>(c0) + g;
-    n_draft = c1 - c0;
-    n_bonus = 1;
-    if (c1 < c0 || c0 < 0 || first + n_draft >= rows) {
-      if (part == 0 && threadIdx.x == 0) atomicOr(err, SGA_DEVERR_LAYOUT);
-      return;  // CTA-uniform: before any barrier
-    }
+  const int32_t d = tab.pre_d[tab.n], bn = cu != nullptr ? tab.pre_b[tab.n] : 0;
+  const int64_t n_pieces =
+      cu != nullptr ? clamp_rows(__ldg(cu + num_groups), rows) * d + num_groups * bn
+                    : rows * d;
+  const int64_t n_warps = static_cast<int64_t>(gridDim.x) * kWarpsPerCta;
+  const int warp = static_cast<int>(threadIdx.x >> 5);
+  // this warp's numbers: t0, t0 + step, ... below t1
+  int64_t t0, t1, step;
+  if (SGA_BLOCKS_INTERLEAVE) {
+    // the CTA's contiguous range, dealt round-robin to its warps
+    t0 = n_pieces * blockIdx.x / gridDim.x + warp;
+    t1 = n_pieces * (blockIdx.x + 1) / gridDim.x;
+    step = kWarpsPerCta;
   } else {
-    first = static_cast<int64_t>(g) * kGroupRows;
-    n_draft = static_cast<int>(min(static_cast<int64_t>(kGroupRows), rows - first));
-    n_bonus = 0;
+    const int64_t w = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + warp;
+    t0 = n_pieces * w / n_warps;
+    t1 = n_pieces * (w + 1) / n_warps;
+    step = 1;
   }
-  // per shard: block counts, and where its pieces and empty slots start in
-  // the group's numbering
-  if (threadIdx.x == 0) {
-    int32_t items = 0, empties = 0;
-    for (int s = 0; s < tab.n; ++s) {
-      const int32_t st = tab.start[s], en = st + tab.width[s];
-      const int32_t cd = (en - 1) / draft_block - st / draft_block + 1;
-      const int32_t cb = (en - 1) / bonus_block - st / bonus_block + 1;
-      cnt_d[s] = cd;
-      cnt_b[s] = cb;
-      item0[s] = items;
-      empty0[s] = empties;
-      items += n_draft * cd + n_bonus * cb;
-      empties += n_draft * (tab.slots[s] - cd) + n_bonus * (tab.slots[s] - cb);
-    }
-    item0[tab.n] = items;
-    empty0[tab.n] = empties;
-  }
-  __syncthreads();
 
-  // real pieces, dealt round-robin to the group's warps
-  const int n_items = item0[tab.n];
-  const int workers = parts * kWarpsPerCta;
-  int s = 0;  // each warp's items increase, so its shard index only advances
-  for (int32_t t = part * kWarpsPerCta + (threadIdx.x >> 5); t < n_items; t += workers) {
-    while (t >= item0[s + 1]) ++s;
-    const int32_t u = t - item0[s];
-    const int32_t sd = n_draft * cnt_d[s];
-    int32_t rr, p, B;
-    if (u < sd) {
-      rr = u / cnt_d[s];
-      p = u - rr * cnt_d[s];
-      B = draft_block;
-    } else {
-      rr = n_draft;
-      p = u - sd;
-      B = bonus_block;
+  if (t0 < t1) {
+    int64_t g = request_at(t0, num_groups, cu, rows, d, bn);
+    Request q = request_of(g, cu, rows, d, bn);
+    int64_t next0 = g + 1 < num_groups ? item0_of(g + 1, cu, rows, d, bn) : INT64_MAX;
+    int s = 0;
+    for (int64_t t = t0; t < t1;) {
+      while (t >= next0) {
+        ++g;
+        q = request_of(g, cu, rows, d, bn);
+        next0 = g + 1 < num_groups ? item0_of(g + 1, cu, rows, d, bn) : INT64_MAX;
+        s = 0;
+      }
+      const int64_t u = t - q.item0;
+      if (u < 0 || u >= q.n_items) {
+        // a request outside the rows (flagged below) or a hole in a broken
+        // layout: nothing to scan up to the next request (this warp's first
+        // number at or after it)
+        if (next0 >= t1) break;
+        t += (next0 - t + step - 1) / step * step;
+        continue;
+      }
+      const Piece pc = piece_of<kBf16>(static_cast<int32_t>(u), s, q, tab, org_vocab, draft_block,
+                                       bonus_block, logits, ld_bytes, rows);
+      const sga_stat stat = piece_argmax<kBf16>(pc, lane);
+      if (lane == 0) out[pc.out_idx] = stat;
+      t += step;
     }
-    const int32_t st = tab.start[s], en = st + tab.width[s];
-    const int32_t b = st / B + p;
-    const int32_t lo = max(st, b * B);
-    const int32_t hi = min(min(en, b * B + B), org_vocab);
-    const int64_t r = first + rr;
-    const sga_stat stat = piece_argmax<kBf16>(
-        logits + r * ld_bytes + static_cast<int64_t>(tab.col[s]) * kElt, st, lo, hi, lane);
-    if (lane == 0) out[static_cast<int64_t>(tab.slot0[s] + p) * rows + r] = stat;
   }
   pdl_launch_dependents();
 
-  // empty slots: (-inf, the shard's last id), consecutive threads on
-  // consecutive rows
-  const int n_empty = empty0[tab.n];
-  s = 0;
-  for (int32_t t = part * static_cast<int32_t>(blockDim.x) + threadIdx.x; t < n_empty;
-       t += parts * static_cast<int32_t>(blockDim.x)) {
-    while (t >= empty0[s + 1]) ++s;
-    const int32_t u = t - empty0[s];
-    const int32_t ed = n_draft * (tab.slots[s] - cnt_d[s]);
-    sga_stat empty;
-    empty.v = __int_as_float(0xff800000);
-    empty.id = tab.start[s] + tab.width[s] - 1;
-    int64_t slot, r;
-    if (u < ed) {
-      slot = cnt_d[s] + u / n_draft;
-      r = first + u % n_draft;
-    } else {
-      slot = cnt_b[s] + (u - ed);
-      r = first + n_draft;
+  const int64_t n_threads = n_warps * 32;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (cu != nullptr) {
+    // every request whose rows leave [0, rows) is flagged, however the walk
+    // above went
+    for (int64_t g = tid; g < num_groups; g += n_threads)
+      if (!request_of(g, cu, rows, d, bn).valid) atomicOr(err, SGA_DEVERR_LAYOUT);
+  }
+  // empty slots: (-inf, the shard's last id), one thread per row,
+  // consecutive threads on consecutive rows
+  for (int64_t r = tid; r < rows; r += n_threads) {
+    bool bonus_row = false;
+    if (cu != nullptr) {
+      int64_t lo = 0, hi = num_groups - 1;  // the request whose rows start at or before r
+      while (lo < hi) {
+        const int64_t mid = (lo + hi + 1) >> 1;
+        if (clamp_rows(__ldg(cu + mid), rows) + mid <= r) lo = mid;
+        else hi = mid - 1;
+      }
+      const Request q = request_of(lo, cu, rows, d, bn);
+      if (!q.valid || r < q.first || r > q.first + q.k) continue;  // no request holds row r
+      bonus_row = r == q.first + q.k;
     }
-    out[(tab.slot0[s] + slot) * rows + r] = empty;
+    for (int sh = 0; sh < tab.n; ++sh) {
+      sga_stat empty;
+      empty.v = __int_as_float(0xff800000);
+      empty.id = tab.start[sh] + tab.width[sh] - 1;
+      for (int p = bonus_row ? tab.cnt_b[sh] : tab.cnt_d[sh]; p < tab.slots[sh]; ++p)
+        out[static_cast<int64_t>(tab.slot0[sh] + p) * rows + r] = empty;
+    }
   }
 }
 
@@ -296,19 +425,27 @@ cudaError_t launch_block_argmax_table(const void *logits, int dtype, int64_t row
     tab.width[s] = static_cast<int32_t>(widths[s]);
     tab.slot0[s] = slot;
     tab.slots[s] = static_cast<int32_t>(block_slots(starts[s], widths[s], draft_block, bonus_block));
+    tab.cnt_d[s] = static_cast<int32_t>(block_count(starts[s], widths[s], draft_block));
+    tab.cnt_b[s] = static_cast<int32_t>(block_count(starts[s], widths[s], bonus_block));
+    tab.pre_d[s + 1] = tab.pre_d[s] + tab.cnt_d[s];
+    tab.pre_b[s + 1] = tab.pre_b[s] + tab.cnt_b[s];
     slot += tab.slots[s];
   }
-  const int64_t groups = cu_num_draft != nullptr ? num_reqs : (rows + kGroupRows - 1) / kGroupRows;
-  // one wave: as many parts per group as the resident CTAs allow (the work of
-  // a group splits evenly over its parts, so a partial second wave would
-  // only add a tail), at least 1, at most 64
-  const int64_t resident =
-      static_cast<int64_t>(num_sms) * (bf16 ? resident_per_sm<true>() : resident_per_sm<false>());
-  int64_t parts = resident / groups;
-  if (parts < 1) parts = 1;
-  if (parts > 64) parts = 64;
+  const bool by_request = cu_num_draft != nullptr;
+  const int64_t groups = by_request ? num_reqs : rows;
+  // pieces of a well-formed layout (rows = cu[num_reqs] + num_reqs); the
+  // kernel takes the count from cu_num_draft itself, this only sizes the grid
+  const int64_t pieces = by_request ? (rows - num_reqs) * tab.pre_d[num_shards] +
+                                          static_cast<int64_t>(num_reqs) * tab.pre_b[num_shards]
+                                    : rows * tab.pre_d[num_shards];
+  // one wave of resident CTAs, fewer when there are fewer pieces than warps
+  const int per_sm = bf16 ? resident_per_sm<true>() : resident_per_sm<false>();
+  int64_t ctas = static_cast<int64_t>(num_sms) * per_sm;
+  const int64_t need = (pieces + kWarpsPerCta - 1) / kWarpsPerCta;
+  if (need < ctas) ctas = need;
+  if (ctas < 1) ctas = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(groups * parts));
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas));
   cfg.blockDim = dim3(kWarpsPerCta * 32);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -322,8 +459,8 @@ cudaError_t launch_block_argmax_table(const void *logits, int dtype, int64_t row
   return cudaLaunchKernelEx(
       &cfg, kern, base, ld * elt, rows, tab,
       static_cast<int32_t>(org_vocab < SGA_MAX_VOCAB ? org_vocab : SGA_MAX_VOCAB),
-      static_cast<int32_t>(draft_block), static_cast<int32_t>(bonus_block),
-      static_cast<int>(parts), cu_num_draft, out, err);
+      static_cast<int32_t>(draft_block), static_cast<int32_t>(bonus_block), groups,
+      cu_num_draft, out, err);
 }
 
 cudaError_t launch_block_argmax(const void *logits, int dtype, int64_t rows, int64_t ld,

@@ -381,9 +381,10 @@ int sga_lmhead_argmax_noalloc(const void *hidden, int64_t M, int64_t H,
  * of trapping: SGA_DEVERR_K_RANGE (a request's K_i outside [0, max_k]),
  * SGA_DEVERR_D2T_RANGE (a winning id outside the d2t table),
  * SGA_DEVERR_TIMEOUT (a bounded wait inside a pipelined kernel gave up; its
- * outputs are not valid), SGA_DEVERR_LAYOUT (sga_local_argmax_blocks: a
- * request of cu_num_draft names rows outside [0, rows); that request's
- * statistics are not written).  sga_device_error synchronises the current device
+ * outputs are not valid), SGA_DEVERR_LAYOUT (sga_local_argmax_blocks[_shards]:
+ * a request of cu_num_draft names rows outside [0, rows) or ends before it
+ * starts; that request's statistics are not written, and with a decreasing
+ * cu_num_draft the other requests' statistics are not valid either).  sga_device_error synchronises the current device
  * and copies the word to *out_word (host pointer); sga_clear_device_error
  * synchronises and zeroes it.  Both return SGA_OK or SGA_ERR_CUDA.
  */

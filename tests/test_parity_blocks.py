@@ -186,6 +186,23 @@ def test_request_layout_past_the_rows_sets_error_word(sga_lib):
     assert sga_lib.sga_device_error() == 0
 
 
+def test_decreasing_request_layout_sets_error_word(sga_lib):
+    # request 1 ends before it starts (cu 5 -> 3): the launch flags the
+    # layout and stays inside the buffers; the error word clears again
+    sga_lib.sga_clear_device_error()
+    x = wl.discrete_logits(13, 12, 900, "f32")
+    cu = np.array([0, 5, 3, 8], np.int32)
+    for n_shards in (1, 2):
+        shards = [(0, 900)] if n_shards == 1 else [(0, 300), (300, 600)]
+        n = sum(sga.sga_block_slots(o, w, 256, 64) for o, w in shards)
+        stats = sga.new_stats(n * 12)
+        sga.sga_local_argmax_blocks_shards(gh.to_device(x), shards, 900, 256, stats,
+                                           bonus_block=64, cu_num_draft=torch.from_numpy(cu).cuda())
+        assert sga_lib.sga_device_error() & sga_lib.SGA_DEVERR_LAYOUT
+        sga_lib.sga_clear_device_error()
+    assert sga_lib.sga_device_error() == 0
+
+
 def test_one_launch_large_verify_and_subset_of_shards(sga_lib):
     # the large-verify shards in one launch (sampled requests against the
     # oracle, the verify against per-shard launches), and a GPU holding shards
