@@ -61,6 +61,9 @@ def parse_args():
                    help="vocab shards (emulated TP ranks) of the fused LM-head workload")
     p.add_argument("--lmhead-vocab", type=int, default=151936,
                    help="vocab of the fused LM-head workload (smaller for profiling)")
+    p.add_argument("--mixed-k", action="store_true",
+                   help="large_verify workloads: 256 requests with K_i uniform in 1..15 "
+                        "instead of K = 15 for all")
     p.add_argument("--rows", type=int, default=None,
                    help="keep only the first rows (whole requests) of the workload; "
                         "for small profiling captures")
@@ -421,10 +424,9 @@ def oracle_verify_step(oracle, x, shards, org, cu, drafts, k, blocks=None):
 
 def oracle_sample(c, n_reqs):
     """The first n_reqs requests of the workload (whole requests)."""
-    k = c["k"]
-    rows = n_reqs * (k + 1)
     cu = c["cu_num_draft"][:n_reqs + 1]
-    return c["logits"][:rows], cu, c["flags"][:n_reqs * k], c["rand_ids"][:n_reqs * k]
+    rows, drafts = int(cu[-1]) + n_reqs, int(cu[-1])
+    return c["logits"][:rows], cu, c["flags"][:drafts], c["rand_ids"][:drafts]
 
 
 def oracle_drafts(oracle, x, shards, org, cu, flags, rand_ids):
@@ -433,14 +435,14 @@ def oracle_drafts(oracle, x, shards, org, cu, flags, rand_ids):
     return wl.compose_drafts(t, cu, flags, rand_ids)
 
 
-def cpu_baseline(c, target_seconds):
+def cpu_baseline(c, target_seconds, blocks=None):
     import oracle
     x, cu = c["logits"], c["cu_num_draft"]
     shards, org, k = c["shards"], c["org_vocab"], c["k"]
     drafts = oracle_drafts(oracle, x, shards, org, cu, c["flags"], c["rand_ids"])
     reps, t0 = 0, time.perf_counter()
     while True:
-        out = oracle_verify_step(oracle, x, shards, org, cu, drafts, k)
+        out = oracle_verify_step(oracle, x, shards, org, cu, drafts, k, blocks)
         reps += 1
         el = time.perf_counter() - t0
         if el >= target_seconds or reps >= 500:
@@ -449,8 +451,10 @@ def cpu_baseline(c, target_seconds):
     return {"value": rows * reps / el, "unit": "rows/s", "cores": oracle.num_threads(),
             "kind": "oracle", "_drafts": drafts, "_outputs": out,
             "sample": f"the whole workload ({rows} rows x {x.shape[1]} bf16 logits, "
-                      f"{len(shards)} shard argmaxes + verify of {cu.size - 1} requests) "
-                      f"repeated {reps} times in {el:.1f} s"}
+                      + (f"block statistics {blocks[0]}/{blocks[1]} of {len(shards)} shards"
+                         if blocks else f"{len(shards)} shard argmaxes")
+                      + f" + verify of {cu.size - 1} requests) repeated {reps} times in "
+                      f"{el:.1f} s"}
 
 
 def run_reference(args, c_builder, blocks=None):
@@ -515,7 +519,7 @@ def run_ours_verify(args, blocks=None):
     barrier(world)
     import greedy_spec_decode_gb300 as sga
 
-    c = wl.large_verify(rows_limit=args.rows)
+    c = (wl.large_verify_mixed_k if args.mixed_k else wl.large_verify)(rows_limit=args.rows)
     if args.rows is not None:
         c["name"] += f" (first {c['logits'].shape[0]} rows)"
     if blocks:
@@ -592,7 +596,7 @@ def run_ours_verify(args, blocks=None):
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        base = cpu_baseline(c, args.cpu_seconds)
+        base = cpu_baseline(c, args.cpu_seconds, blocks)
         # the baseline leg ran the oracle on the whole workload: recheck the
         # timed device outputs against it, bit for bit
         exp, exp_drafts = base.pop("_outputs"), base.pop("_drafts")
@@ -1009,7 +1013,7 @@ def main():
     if args.impl == "reference":
         # the oracle's arm is defined for the verify workloads; any other
         # workload is timed on the default one and says so in its config
-        return run_reference(args, wl.large_verify,
+        return run_reference(args, wl.large_verify_mixed_k if args.mixed_k else wl.large_verify,
                              BLOCK_SIZES if args.workload == "large_verify_blocks" else None)
     if args.workload == "lmhead":
         return run_ours_lmhead(args)

@@ -18,25 +18,28 @@
 // precedes it.  Output layout: out[(slot0_s + p) * rows + r] (piece-major,
 // shards in order, like the shard-major gathered buffer).
 //
-// Design.  The real pieces of the launch are numbered flat: request by
-// request (its K_i draft rows and its bonus row), inside a request shard by
-// shard, then row, then piece, so consecutive numbers are consecutive memory.
-// With D = the draft blocks and Bn = the bonus blocks met by all the shards
-// of the launch, request i's pieces start at number cu[i] * D + i * Bn, a
-// closed form: a warp finds the request of its first piece with one binary
-// search over cu_num_draft and then walks forward.  Every CTA of the grid
-// (one wave of resident CTAs) takes an equal contiguous range of numbers,
-// dealt round-robin to its warps (so a CTA's warps read neighbouring
-// pieces), and the load is balanced whatever the number of requests and
-// their K_i.  A
-// warp scans a piece as the per-shard kernel scans a row: 16-byte vectors
-// with kUnroll streaming loads in flight per lane, the best vector kept in
-// registers and searched once; the element head (to the first 16-byte
-// boundary) and tail are loaded before the vectors so that their latency
-// overlaps; then a merge across the warp and one stat.  The empty slots (all
-// but a few of a draft row's slots when the bonus block is the smaller one)
-// are plain stores, one thread per row.  Without cu_num_draft every row is a
-// request of one draft row and no bonus row.
+// Design.  The work items of a launch are numbered flat: request by request
+// (its K_i draft rows and its bonus row), inside a request shard by shard,
+// then row, then item, so consecutive numbers are consecutive memory.  An
+// item is one piece, or up to four consecutive short pieces of one row and
+// shard (at most 2 KB each, such as the 1024-id bonus blocks of bf16
+// logits), which a warp scans at once with a group of 8 lanes per piece, so
+// that every lane keeps as many loads in flight as on a long piece.  With
+// D = the draft-row items and Bn = the bonus-row items of all the shards of
+// the launch, request i's items start at number cu[i] * D + i * Bn, a closed
+// form: a warp finds the request of its first item with one binary search
+// over cu_num_draft and then walks forward.  Every CTA of the grid (one wave
+// of resident CTAs) takes an equal contiguous range of numbers, dealt
+// round-robin to its warps (so a CTA's warps read neighbouring items), and
+// the load is balanced whatever the number of requests and their K_i.  A
+// warp (or lane group) scans a piece as the per-shard kernel scans a row:
+// 16-byte vectors with kUnroll streaming loads in flight per lane, the best
+// vector kept in registers and searched once; the element head (to the
+// first 16-byte boundary) and tail are loaded before the vectors so that
+// their latency overlaps; then a merge across the lanes and one stat.  The
+// empty slots (all but a few of a draft row's slots when the bonus block is
+// the smaller one) are plain stores, one thread per row.  Without
+// cu_num_draft every row is a request of one draft row and no bonus row.
 #include "common.cuh"
 #include "scan.cuh"
 
@@ -50,18 +53,22 @@ namespace {
 // (0: the occupancy calculator's number), and how a CTA's range is split
 // (1: round-robin over its warps, 0: a contiguous sub-range per warp).
 // Measured on GB300 with CUDA events around each launch (launches kept
-// apart), large-verify logits (202048 bf16 ids, 3 shards in one launch,
-// blocks 8192 / 1024), 256 requests:
-//   K_i = 15 (4096 rows): 4 warps x 16 loads, 5 CTAs per SM, round-robin
-//     247.8 us (6.68 TB/s); a contiguous sub-range per warp 268.3 us; 8 CTAs
-//     per SM with 8 loads 258-271 us; 10 per SM 268-278 us; 12 per SM with
-//     4 loads 284.7 us; two, four or eight waves of smaller CTAs 274.4,
-//     262.1, 256.0 us; launched without programmatic dependent launch: no
-//     change;
-//   K_i uniform in 0..15 (2271 rows): 172.0 us;
-//   64 requests of K_i = 15 and 192 of K_i = 0 (1216 rows): 118.8 us.
+// apart, one process), large-verify logits (202048 bf16 ids, 3 shards in one
+// launch, blocks 8192 / 1024), 256 requests, for K_i = 15 (4096 rows) /
+// K_i uniform in 0..15 (2271 rows) / 64 requests of K_i = 15 and 192 of
+// K_i = 0 (1216 rows):
+//   4 warps x 16 loads, 5 CTAs per SM, round-robin, short pieces four at a
+//     time: 239.7 / 147.5 / 84.0 us (chosen);
+//   the same with one piece per warp: 244.7 / 170.0 / 119.8 us;
+//   8 loads, 8 CTAs per SM: 241.6 / 141.3 / 84.0 us;
+//   one piece per warp, K_i = 15 only: a contiguous sub-range per warp
+//     268.3 us; 8 CTAs per SM with 8 loads 258-271 us; 10 per SM 268-278 us;
+//     12 per SM with 4 loads 284.7 us; two, four or eight waves of smaller
+//     CTAs 274.4, 262.1, 256.0 us; no programmatic dependent launch: no
+//     change.
 // The earlier kernel (whole CTAs per request, as many for a request of 0
-// drafts as for one of 15) took 250.2, 189.2 and 162.4 us on these three.
+// drafts as for one of 15, one piece per warp) took 250.2 / 189.2 / 162.4
+// us.
 #ifndef SGA_BLOCKS_WARPS
 #define SGA_BLOCKS_WARPS 4
 #endif
@@ -79,12 +86,23 @@ namespace {
 #endif
 constexpr int kWarpsPerCta = SGA_BLOCKS_WARPS;
 constexpr int kUnroll = SGA_BLOCKS_UNROLL;
+// Pieces of at most kShortPieceBytes are taken kGroupPieces at a time, one
+// per group of 32 / kGroupPieces lanes, so that a lane still has up to
+// kUnroll loads in flight (a 1024-id bf16 bonus piece is 2 KB: 4 vectors per
+// lane of a whole warp, 16 per lane of a group of 8).
+#ifndef SGA_BLOCKS_SHORT_PIECE_BYTES
+#define SGA_BLOCKS_SHORT_PIECE_BYTES 2048
+#endif
+constexpr int kGroupPieces = 4;
+constexpr int64_t kShortPieceBytes = SGA_BLOCKS_SHORT_PIECE_BYTES;
 
 // The shards of one launch: shard s covers global ids [start, start + width),
 // held at column col of `logits`, owns the slots slot0 .. slot0 + slots - 1 of
 // every row in the gathered statistics, and meets cnt_d draft blocks and
-// cnt_b bonus blocks; pre_d / pre_b are the prefix sums of cnt_d / cnt_b over
-// the shards (pre_d[n] = D, pre_b[n] = Bn).
+// cnt_b bonus blocks.  A work item is up to group_d consecutive pieces of one
+// draft row (group_b of one bonus row) in one shard: items_d = ceil(cnt_d /
+// group_d) and items_b = ceil(cnt_b / group_b) items per row, and pre_d /
+// pre_b are their prefix sums over the shards (pre_d[n] = D, pre_b[n] = Bn).
 struct BlockShardTable {
   int n;
   int32_t start[kMaxBlockShards];
@@ -94,6 +112,8 @@ struct BlockShardTable {
   int32_t slots[kMaxBlockShards];
   int32_t cnt_d[kMaxBlockShards];
   int32_t cnt_b[kMaxBlockShards];
+  int32_t items_d[kMaxBlockShards];
+  int32_t items_b[kMaxBlockShards];
   int32_t pre_d[kMaxBlockShards + 1];
   int32_t pre_b[kMaxBlockShards + 1];
 };
@@ -183,76 +203,120 @@ __device__ __forceinline__ int64_t request_at(int64_t t, int64_t n, const int32_
   return lo;
 }
 
-// Piece u (0 <= u < q.n_items) of request q.  `s` is the caller's shard
-// cursor inside the request: its pieces only increase, so it only advances.
-template <bool kBf16>
-__device__ __forceinline__ Piece piece_of(int32_t u, int &s, const Request &q,
-                                          const BlockShardTable &tab, int32_t org_vocab,
-                                          int32_t draft_block, int32_t bonus_block,
-                                          const char *logits, int64_t ld_bytes, int64_t rows) {
-  constexpr int kElt = kBf16 ? 2 : 4;
+// Work item u (0 <= u < q.n_items) of request q: row r, shard s, block size
+// B and pieces p0 .. p0 + np - 1.  `s` is the caller's shard cursor inside
+// the request: its items only increase, so it only advances.
+struct Item {
+  int64_t r;
+  int s;
+  int32_t B;
+  int32_t p0;
+  int32_t np;
+  bool grouped;  // the item's row kind takes pieces group_d / group_b > 1 at a time
+};
+
+__device__ __forceinline__ Item item_of(int32_t u, int &s, const Request &q,
+                                        const BlockShardTable &tab, int32_t draft_block,
+                                        int32_t bonus_block, int32_t group_d, int32_t group_b) {
   while (u >= q.k * tab.pre_d[s + 1] + q.bonus * tab.pre_b[s + 1]) ++s;
   const int32_t v = u - (q.k * tab.pre_d[s] + q.bonus * tab.pre_b[s]);
-  const int32_t sd = q.k * tab.cnt_d[s];
-  int32_t rr, p, B;
+  const int32_t sd = q.k * tab.items_d[s];
+  int32_t rr, gi, g, cnt;
+  Item it;
   if (v < sd) {
-    rr = v / tab.cnt_d[s];
-    p = v - rr * tab.cnt_d[s];
-    B = draft_block;
+    rr = v / tab.items_d[s];
+    gi = v - rr * tab.items_d[s];
+    it.B = draft_block;
+    g = group_d;
+    cnt = tab.cnt_d[s];
   } else {
     rr = q.k;
-    p = v - sd;
-    B = bonus_block;
+    gi = v - sd;
+    it.B = bonus_block;
+    g = group_b;
+    cnt = tab.cnt_b[s];
   }
-  const int32_t st = tab.start[s], en = st + tab.width[s];
-  const int32_t b = st / B + p;
-  const int32_t lo = max(st, b * B);
-  const int32_t hi = min(min(en, b * B + B), org_vocab);
-  const int64_t r = q.first + rr;
+  it.r = q.first + rr;
+  it.s = s;
+  it.p0 = gi * g;
+  it.np = min(g, cnt - it.p0);
+  it.grouped = g > 1;
+  return it;
+}
+
+// Piece p of an item's row and shard: ids [max(start, b B), min(end, (b+1) B,
+// org_vocab)) with b = start / B + p.  active = false gives an empty piece.
+template <bool kBf16>
+__device__ __forceinline__ Piece piece_at(const Item &it, int32_t p, bool active,
+                                          const BlockShardTable &tab, int32_t org_vocab,
+                                          const char *logits, int64_t ld_bytes, int64_t rows) {
+  constexpr int kElt = kBf16 ? 2 : 4;
+  const int32_t st = tab.start[it.s], en = st + tab.width[it.s];
+  const int32_t b = st / it.B + p;
+  const int32_t lo = max(st, b * it.B);
+  const int32_t hi = min(min(en, b * it.B + it.B), org_vocab);
   Piece pc;
   pc.lo = lo;
-  pc.n = hi > lo ? hi - lo : 0;
-  pc.q = logits + r * ld_bytes + static_cast<int64_t>(tab.col[s] + (lo - st)) * kElt;
-  pc.out_idx = static_cast<int64_t>(tab.slot0[s] + p) * rows + r;
+  pc.n = active && hi > lo ? hi - lo : 0;
+  pc.q = logits + it.r * ld_bytes + static_cast<int64_t>(tab.col[it.s] + (lo - st)) * kElt;
+  pc.out_idx = static_cast<int64_t>(tab.slot0[it.s] + p) * rows + it.r;
   return pc;
 }
 
-// Argmax (value, global id) of one piece, computed by the whole warp; every
-// lane returns the result.  No element: (-inf, lo).  Per lane the scan order
-// is ascending ids (head element, vectors, tail element), then the merge
-// across the warp takes the full (value, id) order.
-template <bool kBf16>
-__device__ __forceinline__ sga_stat piece_argmax(const Piece &pc, int lane) {
+// (value, id) argmax over groups of kW lanes (kW a power of two <= 32):
+// every lane ends with its group's result.
+template <int kW>
+__device__ __forceinline__ void group_argmax(float &v, int32_t &id) {
+#pragma unroll
+  for (int off = kW / 2; off > 0; off >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+    const int32_t oi = __shfl_xor_sync(0xffffffffu, id, off);
+    if (pair_beats(ov, oi, v, id)) {
+      v = ov;
+      id = oi;
+    }
+  }
+}
+
+// Argmax (value, global id) of one piece, computed by a group of kW lanes of
+// the warp (sl = the lane's index in its group, kW >= 8 so that a group
+// covers the element head and tail); every lane of the group returns the
+// result.  No element: (-inf, lo).  Per lane the scan order is ascending ids
+// (head element, vectors, tail element), then the merge across the group
+// takes the full (value, id) order.  All 32 lanes of the warp call it.
+template <bool kBf16, int kW>
+__device__ __forceinline__ sga_stat piece_argmax(const Piece &pc, int sl) {
   constexpr int kElt = kBf16 ? 2 : 4;
   constexpr int kVec = 16 / kElt;
+  static_assert(kW >= 8 && kW <= 32 && (kW & (kW - 1)) == 0, "group of 8, 16 or 32 lanes");
   const Split<kBf16> sp(pc);
   // the lane's head and tail elements, loaded first so that their latency
   // overlaps the vector loads
   float head_x = __int_as_float(0xff800000), tail_x = __int_as_float(0xff800000);
-  if (lane < sp.head) head_x = load_elem<kBf16>(pc.q, lane);
-  if (lane < sp.tail) tail_x = load_elem<kBf16>(pc.q, sp.head + sp.nvec * kVec + lane);
+  if (sl < sp.head) head_x = load_elem<kBf16>(pc.q, sl);
+  if (sl < sp.tail) tail_x = load_elem<kBf16>(pc.q, sp.head + sp.nvec * kVec + sl);
 
   const uint4 *vp = reinterpret_cast<const uint4 *>(pc.q + sp.head * kElt);
   float vbest = __int_as_float(0xff800000);
   int vbest_idx = -1;
   uint4 vraw = make_uint4(0u, 0u, 0u, 0u);
-  int v = lane;
-  for (; v + (kUnroll - 1) * 32 < sp.nvec; v += kUnroll * 32) {
+  int v = sl;
+  for (; v + (kUnroll - 1) * kW < sp.nvec; v += kUnroll * kW) {
     uint4 a[kUnroll];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) a[u] = ld_stream_v4(vp + v + u * 32);
+    for (int u = 0; u < kUnroll; ++u) a[u] = ld_stream_v4(vp + v + u * kW);
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const float m = vec_max<kBf16>(a[u]);
       if (scan_better(m, vbest)) {
         vbest = m;
-        vbest_idx = v + u * 32;
+        vbest_idx = v + u * kW;
         vraw = a[u];
       }
     }
   }
 #pragma unroll 4
-  for (; v < sp.nvec; v += 32) {
+  for (; v < sp.nvec; v += kW) {
     const uint4 a = ld_stream_v4(vp + v);
     const float m = vec_max<kBf16>(a);
     if (scan_better(m, vbest)) {
@@ -264,16 +328,16 @@ __device__ __forceinline__ sga_stat piece_argmax(const Piece &pc, int lane) {
 
   float best = __int_as_float(0xff800000);
   int32_t best_id = kNoId;
-  if (lane < sp.head && scan_better(head_x, best)) {
+  if (sl < sp.head && scan_better(head_x, best)) {
     best = head_x;
-    best_id = pc.lo + lane;
+    best_id = pc.lo + sl;
   }
   if (vbest_idx >= 0) scan_vec<kBf16>(vraw, pc.lo + sp.head + vbest_idx * kVec, best, best_id);
-  if (lane < sp.tail && scan_better(tail_x, best)) {
+  if (sl < sp.tail && scan_better(tail_x, best)) {
     best = tail_x;
-    best_id = pc.lo + sp.head + sp.nvec * kVec + lane;
+    best_id = pc.lo + sp.head + sp.nvec * kVec + sl;
   }
-  warp_argmax(best, best_id);
+  group_argmax<kW>(best, best_id);
   sga_stat st;
   st.v = best;  // -inf when nothing beat -inf
   st.id = best_id == kNoId ? pc.lo : best_id;
@@ -290,7 +354,8 @@ template <bool kBf16>
 __global__ void __launch_bounds__(kWarpsPerCta * 32, SGA_BLOCKS_MIN_CTAS)
     block_argmax_kernel(const char *__restrict__ logits, int64_t ld_bytes, int64_t rows,
                         const __grid_constant__ BlockShardTable tab, int32_t org_vocab,
-                        int32_t draft_block, int32_t bonus_block, int64_t num_groups,
+                        int32_t draft_block, int32_t bonus_block, int32_t group_d,
+                        int32_t group_b, int64_t num_groups,
                         const int32_t *__restrict__ cu, sga_stat *__restrict__ out,
                         uint32_t *err) {
   pdl_wait();
@@ -336,10 +401,22 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, SGA_BLOCKS_MIN_CTAS)
         t += (next0 - t + step - 1) / step * step;
         continue;
       }
-      const Piece pc = piece_of<kBf16>(static_cast<int32_t>(u), s, q, tab, org_vocab, draft_block,
-                                       bonus_block, logits, ld_bytes, rows);
-      const sga_stat stat = piece_argmax<kBf16>(pc, lane);
-      if (lane == 0) out[pc.out_idx] = stat;
+      const Item it = item_of(static_cast<int32_t>(u), s, q, tab, draft_block, bonus_block,
+                              group_d, group_b);
+      if (!it.grouped) {
+        // one piece, the whole warp
+        const Piece pc = piece_at<kBf16>(it, it.p0, true, tab, org_vocab, logits, ld_bytes, rows);
+        const sga_stat stat = piece_argmax<kBf16, 32>(pc, lane);
+        if (lane == 0) out[pc.out_idx] = stat;
+      } else {
+        // up to kGroupPieces short pieces, one per group of 8 lanes
+        const int sub = lane >> 3;
+        const bool act = sub < it.np;
+        const Piece pc =
+            piece_at<kBf16>(it, it.p0 + (act ? sub : 0), act, tab, org_vocab, logits, ld_bytes, rows);
+        const sga_stat stat = piece_argmax<kBf16, 32 / kGroupPieces>(pc, lane & 7);
+        if (act && (lane & 7) == 0) out[pc.out_idx] = stat;
+      }
       t += step;
     }
   }
@@ -416,6 +493,10 @@ cudaError_t launch_block_argmax_table(const void *logits, int dtype, int64_t row
                                       const int32_t *cu_num_draft, sga_stat *out, int num_sms,
                                       uint32_t *err, cudaStream_t stream) {
   const bool bf16 = dtype == SGA_BF16;
+  const int elt = bf16 ? 2 : 4;
+  // short pieces (the bonus rows' 1024-id blocks) go kGroupPieces at a time
+  const int32_t group_d = draft_block * elt <= kShortPieceBytes ? kGroupPieces : 1;
+  const int32_t group_b = bonus_block * elt <= kShortPieceBytes ? kGroupPieces : 1;
   BlockShardTable tab = {};
   tab.n = num_shards;
   int32_t slot = 0;
@@ -427,13 +508,15 @@ cudaError_t launch_block_argmax_table(const void *logits, int dtype, int64_t row
     tab.slots[s] = static_cast<int32_t>(block_slots(starts[s], widths[s], draft_block, bonus_block));
     tab.cnt_d[s] = static_cast<int32_t>(block_count(starts[s], widths[s], draft_block));
     tab.cnt_b[s] = static_cast<int32_t>(block_count(starts[s], widths[s], bonus_block));
-    tab.pre_d[s + 1] = tab.pre_d[s] + tab.cnt_d[s];
-    tab.pre_b[s + 1] = tab.pre_b[s] + tab.cnt_b[s];
+    tab.items_d[s] = (tab.cnt_d[s] + group_d - 1) / group_d;
+    tab.items_b[s] = (tab.cnt_b[s] + group_b - 1) / group_b;
+    tab.pre_d[s + 1] = tab.pre_d[s] + tab.items_d[s];
+    tab.pre_b[s + 1] = tab.pre_b[s] + tab.items_b[s];
     slot += tab.slots[s];
   }
   const bool by_request = cu_num_draft != nullptr;
   const int64_t groups = by_request ? num_reqs : rows;
-  // pieces of a well-formed layout (rows = cu[num_reqs] + num_reqs); the
+  // work items of a well-formed layout (rows = cu[num_reqs] + num_reqs); the
   // kernel takes the count from cu_num_draft itself, this only sizes the grid
   const int64_t pieces = by_request ? (rows - num_reqs) * tab.pre_d[num_shards] +
                                           static_cast<int64_t>(num_reqs) * tab.pre_b[num_shards]
@@ -453,13 +536,13 @@ cudaError_t launch_block_argmax_table(const void *logits, int dtype, int64_t row
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const int elt = bf16 ? 2 : 4;
   const char *base = static_cast<const char *>(logits);
   auto kern = bf16 ? block_argmax_kernel<true> : block_argmax_kernel<false>;
   return cudaLaunchKernelEx(
       &cfg, kern, base, ld * elt, rows, tab,
       static_cast<int32_t>(org_vocab < SGA_MAX_VOCAB ? org_vocab : SGA_MAX_VOCAB),
-      static_cast<int32_t>(draft_block), static_cast<int32_t>(bonus_block), groups,
+      static_cast<int32_t>(draft_block), static_cast<int32_t>(bonus_block), group_d, group_b,
+      groups,
       cu_num_draft, out, err);
 }
 

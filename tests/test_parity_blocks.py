@@ -186,6 +186,35 @@ def test_request_layout_past_the_rows_sets_error_word(sga_lib):
     assert sga_lib.sga_device_error() == 0
 
 
+@pytest.mark.parametrize("layout", ["uniform_0_15", "skewed", "all_zero"])
+def test_many_requests_variable_k(sga_lib, layout):
+    # 256 requests: the flat piece numbering of the one-launch kernel spans
+    # many requests per CTA and many CTAs per request; every request's rows,
+    # its bonus row's block size and the empty slots must land where the
+    # oracle puts them (per-shard launches and the one launch alike)
+    rng = np.random.default_rng(91)
+    if layout == "uniform_0_15":
+        ks = rng.integers(0, 16, 256)
+    elif layout == "skewed":
+        ks = np.concatenate([np.full(40, 15), np.zeros(216, np.int64)])
+        rng.shuffle(ks)
+    else:
+        ks = np.zeros(256, np.int64)
+    cu = np.concatenate([[0], np.cumsum(ks)]).astype(np.int32)
+    rows = int(cu[-1]) + 256
+    vocab, org = 6000, 5990
+    x = wl.discrete_logits(92, rows, vocab, "bf16", p_nan=0.001, p_inf=0.01)
+    x_dev = gh.to_device(x)
+    shards = [(0, 2001), (2001, 1999), (4000, 2000)]
+    exp, n_exp = oracle.gathered_block_stats(x, shards, org, 512, 128, cu)
+    one, n_one = gpu_block_stats_one_launch(x_dev, shards, org, 512, 128, cu)
+    per, n_per = gpu_block_stats(x_dev, shards, org, 512, 128, cu)
+    assert n_one == n_per == n_exp
+    gh.assert_stats_equal(gh.stats_to_numpy(one), exp)
+    gh.assert_stats_equal(gh.stats_to_numpy(per), exp)
+    assert sga_lib.sga_device_error() == 0
+
+
 def test_decreasing_request_layout_sets_error_word(sga_lib):
     # request 1 ends before it starts (cu 5 -> 3): the launch flags the
     # layout and stays inside the buffers; the error word clears again

@@ -88,6 +88,17 @@ def draft_plan(seed, num_reqs, k, p_accept, vocab):
     return cu, flags, rand_ids
 
 
+def draft_plan_mixed(seed, num_reqs, k_max, p_accept, vocab):
+    """As draft_plan, with each request's draft count K_i drawn uniformly from
+    1..k_max; returns (cu_num_draft, flags, random_ids)."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([int(seed), 7920])))
+    ks = rng.integers(1, k_max + 1, num_reqs)
+    cu = np.concatenate([[0], np.cumsum(ks)]).astype(np.int32)
+    flags = rng.random(int(cu[-1])) < p_accept
+    rand_ids = rng.integers(0, vocab, int(cu[-1]), dtype=np.int64).astype(np.int32)
+    return cu, flags, rand_ids
+
+
 def compose_drafts(target_ids, cu_num_draft, flags, rand_ids):
     """Draft tokens: draft j of request i is the given target token of row
     cu[i] + i + j where its flag is set, else its random id.  target_ids comes
@@ -171,6 +182,26 @@ def large_verify(rows_limit=None):
     plant_edge_ties(x, shards)
     cu, flags, rand_ids = draft_plan(4, n, k, 0.6, v)
     return dict(name="large verify: 256 req x (15+1) = 4096 rows x 202048 bf16, 3 uneven shards",
+                logits=x, shards=shards, org_vocab=v, k=k,
+                cu_num_draft=cu, flags=flags, rand_ids=rand_ids)
+
+
+def large_verify_mixed_k(rows_limit=None):
+    """The large-verify recipe with draft lengths that differ per request: 256
+    requests with K_i uniform in 1..15 (about 2300 rows) x vocab 202048 bf16
+    N(0,3), 3 uneven shards, 1% edge ties, drafts copy the target w.p. 0.6.
+    rows_limit keeps only the first requests (whole requests)."""
+    n, k, v = 256, 15, 202048
+    cu, flags, rand_ids = draft_plan_mixed(6, n, k, 0.6, v)
+    if rows_limit is not None:
+        n = max(1, int(np.searchsorted(cu[1:] + np.arange(1, n + 1), rows_limit, "right")))
+        cu, flags, rand_ids = cu[:n + 1], flags[:cu[n]], rand_ids[:cu[n]]
+    rows = int(cu[-1]) + n
+    shards = even_shards(v, 3)
+    x = normal_matrix(6, rows, v, 3.0)
+    plant_edge_ties(x, shards)
+    return dict(name=f"large verify, mixed K: 256 req x (K_i in 1..15, + 1) = {rows} rows x "
+                     "202048 bf16, 3 uneven shards",
                 logits=x, shards=shards, org_vocab=v, k=k,
                 cu_num_draft=cu, flags=flags, rand_ids=rand_ids)
 
