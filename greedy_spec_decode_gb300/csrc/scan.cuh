@@ -58,27 +58,26 @@ __device__ __forceinline__ void scan_vec(const uint4 a, int32_t id, float &best,
   }
 }
 
-// The scan rule over gathered statistics: entries (s, row) for s = 0..n-1 at
-// stats[s * stride + row], visited in ascending s (ascending ids), the first
-// NaN sticking and ties keeping the lower s.  Eight loads are issued before
-// their comparisons so that the latency of a long list (block-granular
-// statistics have hundreds of entries per row) overlaps; the comparison
-// order is the plain sequential one.
+// The scan rule over gathered statistics: entries (s, row) for s = 0..n-1
+// (n >= 1) at stats[s * stride + row], visited in ascending s (ascending
+// ids), the first NaN sticking and ties keeping the lower s.  The loads go
+// in batches of eight, each batch issued (bounds-predicated, so a short list
+// of two to seven shards is one batch) before its comparisons, so that one
+// memory latency covers eight entries; the comparison order is the plain
+// sequential one.
 __device__ __forceinline__ sga_stat reduce_stats(const sga_stat *__restrict__ stats, int n,
                                                  int64_t stride, int64_t row) {
-  sga_stat b = stats[row];
-  int s = 1;
-  for (; s + 7 < n; s += 8) {
+  sga_stat b;
+  b.v = 0.0f;
+  b.id = 0;
+  for (int s = 0; s < n; s += 8) {
     sga_stat c[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) c[u] = stats[static_cast<int64_t>(s + u) * stride + row];
+    for (int u = 0; u < 8; ++u)
+      if (s + u < n) c[u] = stats[static_cast<int64_t>(s + u) * stride + row];
 #pragma unroll
     for (int u = 0; u < 8; ++u)
-      if (scan_better(c[u].v, b.v)) b = c[u];
-  }
-  for (; s < n; ++s) {
-    const sga_stat c = stats[static_cast<int64_t>(s) * stride + row];
-    if (scan_better(c.v, b.v)) b = c;
+      if (s + u < n && (s + u == 0 || scan_better(c[u].v, b.v))) b = c[u];
   }
   return b;
 }

@@ -122,27 +122,21 @@ __global__ void __launch_bounds__(kWideThreads)
   float bv = __int_as_float(0xff800000);
   int32_t bpos = kNoId, bid = 0;
   if (has_row) {
-    int e = stream;
-    for (; e + 7 * kStreams < num_entries; e += 8 * kStreams) {
+    // batches of eight loads (bounds-predicated) issued before their
+    // comparisons; entries in ascending order per thread
+    for (int e0 = stream; e0 < num_entries; e0 += 8 * kStreams) {
       sga_stat x[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u)
-        x[u] = stats[static_cast<int64_t>(e + u * kStreams) * total_rows + row];
+        if (e0 + u * kStreams < num_entries)
+          x[u] = stats[static_cast<int64_t>(e0 + u * kStreams) * total_rows + row];
 #pragma unroll
       for (int u = 0; u < 8; ++u)
-        if (bpos == kNoId || scan_better(x[u].v, bv)) {
+        if (e0 + u * kStreams < num_entries && (bpos == kNoId || scan_better(x[u].v, bv))) {
           bv = x[u].v;
-          bpos = e + u * kStreams;
+          bpos = e0 + u * kStreams;
           bid = x[u].id;
         }
-    }
-    for (; e < num_entries; e += kStreams) {
-      const sga_stat x = stats[static_cast<int64_t>(e) * total_rows + row];
-      if (bpos == kNoId || scan_better(x.v, bv)) {
-        bv = x.v;
-        bpos = e;
-        bid = x.id;
-      }
     }
   }
   part_v[stream][j] = bv;
