@@ -53,8 +53,8 @@ def parse_args():
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--graph", action="store_true",
-                   help="lmhead workloads: replay each step from a CUDA graph and time the "
-                        "whole step (no per-launch events)")
+                   help="lmhead, draft_top_tokens and greedy_verify workloads: replay each "
+                        "step from a CUDA graph and time the whole step (no per-launch events)")
     p.add_argument("--lmhead-rows", type=int, default=512,
                    help="rows (hidden states) of the fused LM-head workload")
     p.add_argument("--lmhead-shards", type=int, default=2,
@@ -935,6 +935,17 @@ def run_ours_small(args, builder):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    graph = None
+    if args.graph:
+        # the step replayed from one CUDA graph, as a serving engine replays
+        # a decode step
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+    run_step = graph.replay if graph is not None else step
     barrier(world)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
@@ -943,7 +954,7 @@ def run_ours_small(args, builder):
     for a, b in evs:
         flush.zero_()
         a.record()
-        step()
+        run_step()
         b.record()
     torch.cuda.synchronize()
     clocks = sampler.stop()
@@ -963,7 +974,8 @@ def run_ours_small(args, builder):
         "dtype": "bf16" if elt == 2 else "f32", "data": "synthetic",
         "config": {"workload": c["name"], "rows": rows, "shards": [w for _, w in shards],
                    "l2": "inputs fit in L2: 256 MB flush before every timed step",
-                   "step": "one-launch shard argmax + " + ("fused verify" if verify else "shard reduce")},
+                   "step": "one-launch shard argmax + " + ("fused verify" if verify else "shard reduce")
+                   + (", replayed from a CUDA graph" if graph is not None else "")},
         "step_gbs": step_bytes / (step_ms * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": step_bytes / (step_ms * 1e-3) / 1e9, "peak": hbm,
                      "unit": "GB/s", "frac": step_bytes / (step_ms * 1e-3) / 1e9 / hbm,
