@@ -94,6 +94,7 @@ constexpr int kUnroll = SGA_BLOCKS_UNROLL;
 #define SGA_BLOCKS_SHORT_PIECE_BYTES 2048
 #endif
 constexpr int kGroupPieces = 4;
+constexpr int kGroupLanes = 32 / kGroupPieces;
 constexpr int64_t kShortPieceBytes = SGA_BLOCKS_SHORT_PIECE_BYTES;
 
 // The shards of one launch: shard s covers global ids [start, start + width),
@@ -344,10 +345,10 @@ __device__ __forceinline__ sga_stat piece_argmax(const Piece &pc, int sl) {
   return st;
 }
 
-// grid.x = C = resident CTAs (at most); CTA c takes the pieces numbered
-// [T c / C, T (c + 1) / C), its warp j every kWarpsPerCta-th of them from
-// the j-th on (or, without interleaving, warp w of W takes [T w / W,
-// T (w + 1) / W)).  num_groups = num_reqs with cu_num_draft, else
+// grid.x = C = resident CTAs (at most); of the T work items, CTA c takes
+// those numbered [T c / C, T (c + 1) / C), its warp j every kWarpsPerCta-th
+// of them from the j-th on (or, without interleaving, warp w of W takes
+// [T w / W, T (w + 1) / W)).  num_groups = num_reqs with cu_num_draft, else
 // rows.  Ids and block sizes are below 2^24 + 1 and rows x slots below 2^28,
 // so the arithmetic inside a request is 32-bit.
 template <bool kBf16>
@@ -361,7 +362,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, SGA_BLOCKS_MIN_CTAS)
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const int32_t d = tab.pre_d[tab.n], bn = cu != nullptr ? tab.pre_b[tab.n] : 0;
-  const int64_t n_pieces =
+  const int64_t n_items =
       cu != nullptr ? clamp_rows(__ldg(cu + num_groups), rows) * d + num_groups * bn
                     : rows * d;
   const int64_t n_warps = static_cast<int64_t>(gridDim.x) * kWarpsPerCta;
@@ -370,13 +371,13 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, SGA_BLOCKS_MIN_CTAS)
   int64_t t0, t1, step;
   if (SGA_BLOCKS_INTERLEAVE) {
     // the CTA's contiguous range, dealt round-robin to its warps
-    t0 = n_pieces * blockIdx.x / gridDim.x + warp;
-    t1 = n_pieces * (blockIdx.x + 1) / gridDim.x;
+    t0 = n_items * blockIdx.x / gridDim.x + warp;
+    t1 = n_items * (blockIdx.x + 1) / gridDim.x;
     step = kWarpsPerCta;
   } else {
     const int64_t w = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + warp;
-    t0 = n_pieces * w / n_warps;
-    t1 = n_pieces * (w + 1) / n_warps;
+    t0 = n_items * w / n_warps;
+    t1 = n_items * (w + 1) / n_warps;
     step = 1;
   }
 
@@ -409,13 +410,13 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, SGA_BLOCKS_MIN_CTAS)
         const sga_stat stat = piece_argmax<kBf16, 32>(pc, lane);
         if (lane == 0) out[pc.out_idx] = stat;
       } else {
-        // up to kGroupPieces short pieces, one per group of 8 lanes
-        const int sub = lane >> 3;
+        // up to kGroupPieces short pieces, one per group of kGroupLanes lanes
+        const int sub = lane / kGroupLanes, sl = lane % kGroupLanes;
         const bool act = sub < it.np;
         const Piece pc =
             piece_at<kBf16>(it, it.p0 + (act ? sub : 0), act, tab, org_vocab, logits, ld_bytes, rows);
-        const sga_stat stat = piece_argmax<kBf16, 32 / kGroupPieces>(pc, lane & 7);
-        if (act && (lane & 7) == 0) out[pc.out_idx] = stat;
+        const sga_stat stat = piece_argmax<kBf16, kGroupLanes>(pc, sl);
+        if (act && sl == 0) out[pc.out_idx] = stat;
       }
       t += step;
     }
