@@ -1,5 +1,5 @@
-// argmax.cu -- per-shard argmax (with the padding mask) and the cross-shard
-// reduce of the gathered statistics.
+// argmax.cu -- per-shard argmax (with the padding mask); the cross-shard
+// reduce of the gathered statistics is in reduce.cu.
 //
 // vLLM PR #34049, Solution: local argmax on each vocab shard with the index
 // made global, gather of (max_value, global_index), reduction across ranks.
@@ -334,26 +334,6 @@ __global__ void __launch_bounds__(kThreads + (kBulk ? 32 : 0), kBulk ? 2048 / (k
   }
 }
 
-__global__ void shard_reduce_kernel(const sga_stat *__restrict__ stats, int num_shards, int64_t rows,
-                                    float *__restrict__ out_vals, int32_t *__restrict__ out_ids,
-                                    const int64_t *__restrict__ d2t, int64_t d2t_len,
-                                    uint32_t *err) {
-  pdl_wait();
-  for (int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; r < rows;
-       r += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const sga_stat b = reduce_stats(stats, num_shards, rows, r);
-    int32_t id = b.id;
-    if (d2t != nullptr) {
-      if (id >= 0 && id < d2t_len)
-        id = static_cast<int32_t>(id + d2t[id]);
-      else
-        atomicOr(err, SGA_DEVERR_D2T_RANGE);
-    }
-    if (out_vals) out_vals[r] = b.v;
-    out_ids[r] = id;
-  }
-}
-
 // Pieces per (row, shard).  Splitting a row costs two cluster barriers and a
 // shorter-lived CTA (its reduction tail is not streaming), so a row is split
 // (in powers of two) only while the grid stays within half of the resident
@@ -444,25 +424,6 @@ cudaError_t launch_local_argmax(const void *logits, int dtype, int64_t rows, int
   const int64_t col = 0;
   return launch_local_argmax_table(logits, dtype, rows, ld, 1, &shard_start, &col, &valid, out,
                                    num_sms, err, stream);
-}
-
-cudaError_t launch_shard_reduce(const sga_stat *stats, int num_shards, int64_t rows,
-                                float *out_vals, int32_t *out_ids, const int64_t *d2t,
-                                int64_t d2t_len, uint32_t *err, cudaStream_t stream) {
-  const int threads = 256;
-  int64_t blocks = (rows + threads - 1) / threads;
-  if (blocks > 65535) blocks = 65535;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
-  cfg.blockDim = dim3(threads);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, shard_reduce_kernel, stats, num_shards, rows, out_vals, out_ids,
-                            d2t, d2t_len, err);
 }
 
 }  // namespace sga

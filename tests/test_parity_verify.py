@@ -101,3 +101,24 @@ def test_k_above_max_k_sets_error_word(sga_lib, num_shards):
     assert got["num_sampled"][0] >= 1 and got["num_sampled"][2] >= 1
     sga_lib.sga_clear_device_error()
     assert sga_lib.sga_device_error() == 0
+
+
+@pytest.mark.parametrize("num_shards", [1, 3, 8, 16, 17, 40, 200, 257])
+def test_shard_reduce_bit_exact_narrow_and_wide(sga_lib, num_shards):
+    # the cross-shard reduce on its own, over statistics with NaNs, infinities,
+    # signed zeros and ties: the thread-per-row kernel up to 16 entries per
+    # row, the 32-streams-per-row kernel above; values bitwise, ids exact,
+    # then the draft-to-target map applied to the same winners
+    rng = np.random.default_rng(100 + num_shards)
+    for rows in (1, 15, 16, 17, 333):
+        stats_np, _, _ = random_stats(rng, rows, num_shards, 300)
+        stats_dev = torch.from_numpy(stats_np.view(np.int32).reshape(-1, 2).copy()).cuda()
+        vals, ids = gh.gpu_reduce(stats_dev, num_shards, rows)
+        evals, eids = oracle.shard_reduce(stats_np, num_shards, rows)
+        assert (ids == eids).all()
+        assert (vals.view(np.uint32) == np.asarray(evals, np.float32).view(np.uint32)).all()
+        d2t = (rng.integers(0, 50, 300) + np.arange(300) * 3).astype(np.int64) - np.arange(300)
+        _, mapped = gh.gpu_reduce(stats_dev, num_shards, rows,
+                                  d2t=torch.from_numpy(d2t).cuda())
+        assert (mapped == oracle.d2t_map(eids, d2t)).all()
+    assert sga_lib.sga_device_error() == 0
