@@ -54,9 +54,11 @@ __global__ void __launch_bounds__(kThreads)
   bool mismatch = false;
   if (has_row) {
     const int64_t row = static_cast<int64_t>(c) + req + j;
+    // the draft is loaded before the statistics so that both loads overlap
+    const int32_t draft = j < k ? draft_tokens[c + j] : 0;
     t = reduce_stats(stats, num_shards, total_rows, row).id;
     if (out_target_ids) out_target_ids[row] = t;
-    if (j < k) mismatch = draft_tokens[c + j] != t;
+    mismatch = j < k && draft != t;
   }
   const uint32_t ballot = __ballot_sync(0xffffffffu, mismatch);
   const uint32_t mine = (ballot >> (group * 16)) & 0xffffu;
@@ -119,6 +121,8 @@ __global__ void __launch_bounds__(kWideThreads)
   const bool has_row = !bad && j <= k;
   const int64_t row = static_cast<int64_t>(c) + req + j;
 
+  // lanes 0..15 load their draft now so that it overlaps the statistics
+  const int32_t draft = threadIdx.x < 16 && !bad && j < k ? draft_tokens[c + j] : 0;
   float bv = __int_as_float(0xff800000);
   int32_t bpos = kNoId, bid = 0;
   if (has_row) {
@@ -171,7 +175,7 @@ __global__ void __launch_bounds__(kWideThreads)
     return;
   }
   const int32_t t = lane <= k ? t_row[lane] : -1;
-  const bool mismatch = lane < k && draft_tokens[c + lane] != t;
+  const bool mismatch = lane < k && draft != t;
   const uint32_t mine = __ballot_sync(0x0000ffffu, mismatch);
   const int a = mine ? __ffs(mine) - 1 : k;  // accepted drafts
   if (lane <= max_k) sampled_row[lane] = lane <= a ? t : -1;
