@@ -122,3 +122,21 @@ def test_shard_reduce_bit_exact_narrow_and_wide(sga_lib, num_shards):
                                   d2t=torch.from_numpy(d2t).cuda())
         assert (mapped == oracle.d2t_map(eids, d2t)).all()
     assert sga_lib.sga_device_error() == 0
+
+
+@pytest.mark.parametrize("num_shards", [4, 40])
+def test_shard_reduce_d2t_out_of_range_sets_error_word(sga_lib, num_shards):
+    # winners outside the draft-to-target table: the id is left unmapped and
+    # the error word says so (thread-per-row and wide kernels alike)
+    sga_lib.sga_clear_device_error()
+    rng = np.random.default_rng(7)
+    stats_np, _, _ = random_stats(rng, 40, num_shards, 300)
+    stats_dev = torch.from_numpy(stats_np.view(np.int32).reshape(-1, 2).copy()).cuda()
+    _, eids = oracle.shard_reduce(stats_np, num_shards, 40)
+    assert (eids >= 10).any()
+    short = torch.zeros(10, dtype=torch.int64, device="cuda")
+    _, ids = gh.gpu_reduce(stats_dev, num_shards, 40, d2t=short)
+    assert sga_lib.sga_device_error() & sga_lib.SGA_DEVERR_D2T_RANGE
+    assert (ids == eids).all()   # a zero table maps every id to itself
+    sga_lib.sga_clear_device_error()
+    assert sga_lib.sga_device_error() == 0
