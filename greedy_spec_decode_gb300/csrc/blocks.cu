@@ -22,9 +22,10 @@
 // (its K_i draft rows and its bonus row), inside a request shard by shard,
 // then row, then item, so consecutive numbers are consecutive memory.  An
 // item is one piece, or up to four consecutive short pieces of one row and
-// shard (at most 2 KB each, such as the 1024-id bonus blocks of bf16
-// logits), which a warp scans at once with a group of 8 lanes per piece, so
-// that every lane keeps as many loads in flight as on a long piece.  With
+// shard (up to four of at most 2 KB each, such as the 1024-id bonus blocks of
+// bf16 logits, or two of at most 4 KB), which a warp scans at once with a
+// group of 8 or 16 lanes per piece, so that every lane keeps as many loads in
+// flight as on a long piece.  With
 // D = the draft-row items and Bn = the bonus-row items of all the shards of
 // the launch, request i's items start at number cu[i] * D + i * Bn, a closed
 // form: a warp finds the request of its first item with one binary search
@@ -86,16 +87,22 @@ namespace {
 #endif
 constexpr int kWarpsPerCta = SGA_BLOCKS_WARPS;
 constexpr int kUnroll = SGA_BLOCKS_UNROLL;
-// Pieces of at most kShortPieceBytes are taken kGroupPieces at a time, one
-// per group of 32 / kGroupPieces lanes, so that a lane still has up to
-// kUnroll loads in flight (a 1024-id bf16 bonus piece is 2 KB: 4 vectors per
-// lane of a whole warp, 16 per lane of a group of 8).
+// Short pieces are taken several at a time, one per group of lanes, so that
+// a lane still has up to kUnroll loads in flight: pieces of at most
+// kShortPieceBytes four at a time (groups of 8 lanes), of at most twice that
+// two at a time (groups of 16 lanes).  A 1024-id bonus block is 2 KB of bf16
+// (4 vectors per lane of a whole warp, 16 per lane of a group of 8) or 4 KB
+// of fp32.
 #ifndef SGA_BLOCKS_SHORT_PIECE_BYTES
 #define SGA_BLOCKS_SHORT_PIECE_BYTES 2048
 #endif
-constexpr int kGroupPieces = 4;
-constexpr int kGroupLanes = 32 / kGroupPieces;
 constexpr int64_t kShortPieceBytes = SGA_BLOCKS_SHORT_PIECE_BYTES;
+
+// Pieces per work item for a block size (host side).
+inline int32_t group_for(int64_t block_ids, int elt) {
+  const int64_t bytes = block_ids * elt;
+  return bytes <= kShortPieceBytes ? 4 : (bytes <= 2 * kShortPieceBytes ? 2 : 1);
+}
 
 // The shards of one launch: shard s covers global ids [start, start + width),
 // held at column col of `logits`, owns the slots slot0 .. slot0 + slots - 1 of
@@ -213,7 +220,7 @@ struct Item {
   int32_t B;
   int32_t p0;
   int32_t np;
-  bool grouped;  // the item's row kind takes pieces group_d / group_b > 1 at a time
+  int32_t g;  // pieces per item of the item's row kind (1, 2 or 4)
 };
 
 __device__ __forceinline__ Item item_of(int32_t u, int &s, const Request &q,
@@ -241,7 +248,7 @@ __device__ __forceinline__ Item item_of(int32_t u, int &s, const Request &q,
   it.s = s;
   it.p0 = gi * g;
   it.np = min(g, cnt - it.p0);
-  it.grouped = g > 1;
+  it.g = g;
   return it;
 }
 
@@ -345,6 +352,22 @@ __device__ __forceinline__ sga_stat piece_argmax(const Piece &pc, int sl) {
   return st;
 }
 
+// Up to 32 / kW short pieces of one item, one per group of kW lanes; every
+// lane of the warp takes part (the groups past the item's pieces scan an
+// empty piece and store nothing).
+template <bool kBf16, int kW>
+__device__ __forceinline__ void scan_group(const Item &it, int lane, const BlockShardTable &tab,
+                                           int32_t org_vocab, const char *logits,
+                                           int64_t ld_bytes, int64_t rows,
+                                           sga_stat *__restrict__ out) {
+  const int sub = lane / kW, sl = lane % kW;
+  const bool act = sub < it.np;
+  const Piece pc =
+      piece_at<kBf16>(it, it.p0 + (act ? sub : 0), act, tab, org_vocab, logits, ld_bytes, rows);
+  const sga_stat stat = piece_argmax<kBf16, kW>(pc, sl);
+  if (act && sl == 0) out[pc.out_idx] = stat;
+}
+
 // grid.x = C = resident CTAs (at most); of the T work items, CTA c takes
 // those numbered [T c / C, T (c + 1) / C), its warp j every kWarpsPerCta-th
 // of them from the j-th on (or, without interleaving, warp w of W takes
@@ -404,19 +427,15 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, SGA_BLOCKS_MIN_CTAS)
       }
       const Item it = item_of(static_cast<int32_t>(u), s, q, tab, draft_block, bonus_block,
                               group_d, group_b);
-      if (!it.grouped) {
+      if (it.g == 1) {
         // one piece, the whole warp
         const Piece pc = piece_at<kBf16>(it, it.p0, true, tab, org_vocab, logits, ld_bytes, rows);
         const sga_stat stat = piece_argmax<kBf16, 32>(pc, lane);
         if (lane == 0) out[pc.out_idx] = stat;
+      } else if (it.g == 2) {
+        scan_group<kBf16, 16>(it, lane, tab, org_vocab, logits, ld_bytes, rows, out);
       } else {
-        // up to kGroupPieces short pieces, one per group of kGroupLanes lanes
-        const int sub = lane / kGroupLanes, sl = lane % kGroupLanes;
-        const bool act = sub < it.np;
-        const Piece pc =
-            piece_at<kBf16>(it, it.p0 + (act ? sub : 0), act, tab, org_vocab, logits, ld_bytes, rows);
-        const sga_stat stat = piece_argmax<kBf16, kGroupLanes>(pc, sl);
-        if (act && sl == 0) out[pc.out_idx] = stat;
+        scan_group<kBf16, 8>(it, lane, tab, org_vocab, logits, ld_bytes, rows, out);
       }
       t += step;
     }
@@ -495,9 +514,9 @@ cudaError_t launch_block_argmax_table(const void *logits, int dtype, int64_t row
                                       uint32_t *err, cudaStream_t stream) {
   const bool bf16 = dtype == SGA_BF16;
   const int elt = bf16 ? 2 : 4;
-  // short pieces (the bonus rows' 1024-id blocks) go kGroupPieces at a time
-  const int32_t group_d = draft_block * elt <= kShortPieceBytes ? kGroupPieces : 1;
-  const int32_t group_b = bonus_block * elt <= kShortPieceBytes ? kGroupPieces : 1;
+  // short pieces (the bonus rows' 1024-id blocks) go several at a time
+  const int32_t group_d = group_for(draft_block, elt);
+  const int32_t group_b = group_for(bonus_block, elt);
   BlockShardTable tab = {};
   tab.n = num_shards;
   int32_t slot = 0;
