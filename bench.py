@@ -88,9 +88,9 @@ def source_digest(*rel_paths):
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(profile_name, kernel_sources):
-    """DRAM bytes per launch recorded by an ncu capture in profiles/, or None
-    when the kernel source changed since that capture."""
+def ncu_traffic(profile_name, kernel_sources, key="dram_bytes_per_launch"):
+    """DRAM bytes per launch recorded by an ncu capture in profiles/ (the
+    field `key`), or None when the kernel source changed since that capture."""
     path = os.path.join(ROOT, "profiles", profile_name)
     try:
         fields = {}
@@ -101,7 +101,7 @@ def ncu_traffic(profile_name, kernel_sources):
                     fields[k.strip()] = v.strip().strip("`")
         if fields.get("source_digest") != source_digest(*kernel_sources):
             return None
-        return float(fields["dram_bytes_per_launch"])
+        return float(fields[key])
     except (OSError, KeyError, ValueError):
         return None
 
@@ -683,20 +683,23 @@ def lmhead_cpu_baseline(c, fp8, gpu_ids, target_seconds):
 DECODE_MAX_M = 64   # the library's decode-size LM-head kernel covers M <= 64
 
 
-def decode_roofline(weight_bytes, kern_ms, num_shards, fp8):
+def decode_roofline(weight_bytes, kern_ms, num_shards, fp8, captured_shape=True):
     """HBM roofline of the decode-size LM-head kernel: the weight is read once
     per step (one launch per shard)."""
     pk, pk_src = peaks()
     hbm = float(pk.get("hbm_gbs", FALLBACK_HBM_GBS))
     achieved = weight_bytes / (kern_ms * 1e-3) / 1e9
+    # the captures are of one shard of the default shape (2 x 75968 ids, H = 4096)
     traffic = ncu_traffic("lmhead_decode.md", ["greedy_spec_decode_gb300/csrc/lmhead_decode.cu",
                                                "greedy_spec_decode_gb300/csrc/tcgen05.cuh",
-                                               "greedy_spec_decode_gb300/csrc/common.cuh"])
+                                               "greedy_spec_decode_gb300/csrc/common.cuh"],
+                          "dram_bytes_per_launch_fp8" if fp8 else "dram_bytes_per_launch")
     return {"bound": "hbm",
             "kernel": "lmhead_argmax_decode_kernel<%s>" % ("fp8" if fp8 else "bf16"),
             "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-            "traffic": None if (traffic is None or fp8) else traffic,
-            "traffic_unit": "DRAM bytes per launch (one shard), bf16 M = 16 capture",
+            "traffic": traffic if captured_shape else None,
+            "traffic_unit": "DRAM bytes per launch (one shard), %s M = 16 capture"
+                            % ("fp8" if fp8 else "bf16"),
             "peak_source": f"{pk_src} hbm_gbs (MEASURED_PEAKS.json copy bandwidth)"
             if pk_src == "measured" else "fallback 6.8 TB/s",
             "bytes_per_step": weight_bytes, "launches_per_step": num_shards}
@@ -822,7 +825,8 @@ def run_ours_lmhead(args, fp8=False):
         "metric": LMHEAD_METRIC_FP8 if fp8 else LMHEAD_METRIC,
         "value": world * M / (step_ms * 1e-3), "unit": "rows/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8 e4m3 (fp32 accumulate)" if fp8 else "bf16 (fp32 accumulate)",
         "data": "synthetic",
         "config": {"workload": c["name"], "M": M, "H": H, "shards": [w for _, w in shards],
                    "l2": "weight (1.24 GB) larger than L2 (129 MB); no flush",
@@ -831,7 +835,9 @@ def run_ours_lmhead(args, fp8=False):
         "weight_gbs": weight.numel() * weight.element_size() / (kern_ms * 1e-3) / 1e9,
         "kernel_us": {"lmhead_argmax_per_step": round(kern_ms * 1e3, 2),
                       "reduce_and_gaps": round((step_ms - kern_ms) * 1e3, 2)},
-        "roofline": decode_roofline(weight_bytes, kern_ms, S, fp8) if decode else
+        "roofline": decode_roofline(weight_bytes, kern_ms, S, fp8,
+                                    S == 2 and H == 4096 and args.lmhead_vocab == 151936)
+        if decode else
                     {"bound": "tensor",
                      "kernel": "lmhead_argmax_2sm_kernel<fp8>" if fp8 else "lmhead_argmax_2sm_kernel",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
