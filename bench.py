@@ -855,7 +855,11 @@ def run_ours_lmhead(args, fp8=False):
                      "flops_per_step": flops},
         "e2e": {"value": world * M / (e2e_ms * 1e-3), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": M * 4,
-                "ms_per_step": e2e_ms},
+                "ms_per_step": e2e_ms,
+                "note": f"{args.e2e_steps} steps after the timed loop, with the hidden "
+                        "states copied in and the ids read back each step; a tensor-bound "
+                        "step runs under the power cap, so the clocks of the two loops "
+                        "can differ and this figure can exceed `value`"},
         "timing": ("whole step replayed from a CUDA graph" if graph is not None else
                    "CUDA events around each LM-head call (GEMM + finalize)"),
         "gpu_launches": args.steps * (2 * S + 1),
