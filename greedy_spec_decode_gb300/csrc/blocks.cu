@@ -59,9 +59,14 @@ namespace {
 // K_i uniform in 0..15 (2271 rows) / 64 requests of K_i = 15 and 192 of
 // K_i = 0 (1216 rows):
 //   4 warps x 16 loads, 5 CTAs per SM, round-robin, short pieces four at a
-//     time: 239.7 / 147.5 / 84.0 us (chosen);
+//     time: 239.7 / 147.5 / 84.0 us;
 //   the same with one piece per warp: 244.7 / 170.0 / 119.8 us;
 //   8 loads, 8 CTAs per SM: 241.6 / 141.3 / 84.0 us;
+//   on a slower box, registers budgeted for 5 / 6 / 7 / 8 CTAs per SM (96 /
+//     80 / 72 / 64 registers): 243.7 / 247.8 / 249.9 / 243.7 us at
+//     K_i = 15, 147.5 / 147.5 / 147.5 / 143.5 us for the mixed K_i, 85.9 /
+//     86.0 / 88.1 / 86.0 us skewed; 8 warps at 3 per SM 243.7 / 145.4 /
+//     86.1 us.  8 CTAs per SM with 16 loads is chosen;
 //   one piece per warp, K_i = 15 only: a contiguous sub-range per warp
 //     268.3 us; 8 CTAs per SM with 8 loads 258-271 us; 10 per SM 268-278 us;
 //     12 per SM with 4 loads 284.7 us; two, four or eight waves of smaller
@@ -77,7 +82,7 @@ namespace {
 #define SGA_BLOCKS_UNROLL 16
 #endif
 #ifndef SGA_BLOCKS_MIN_CTAS
-#define SGA_BLOCKS_MIN_CTAS 5
+#define SGA_BLOCKS_MIN_CTAS 8
 #endif
 #ifndef SGA_BLOCKS_CTAS_PER_SM
 #define SGA_BLOCKS_CTAS_PER_SM 0
