@@ -7,7 +7,9 @@ counting after a mismatch, a missing bonus-row offset, a wrong count, a dropped
 dot-product term, a wrong bf16 widening, a runner-up equal to the winner, the
 bonus taken from the wrong row, a wrong E4M3 exponent bias, the fp8 scales
 dropped, block boundaries taken from the shard start instead of global ids,
-the bonus row's block size ignored or given to the wrong row), builds it with gcc, points the oracle wrapper
+the bonus row's block size ignored or given to the wrong row, an empty block
+slot naming the shard's first id, a block count off by one, the smaller of
+the two block counts as the slot count), builds it with gcc, points the oracle wrapper
 at it, and runs the pin tests of tests/test_oracle_pins.py: at least one pin
 must fail for every mutant.  The committed oracle source is never modified.
 """
@@ -49,6 +51,13 @@ MUTANTS = {
                                    "const int64_t B = draft_block;"),
     "bonus_row_is_first_row": ("is_bonus[(int64_t)cu_num_draft[i + 1] + i] = 1;",
                                "is_bonus[(int64_t)cu_num_draft[i] + i] = 1;"),
+    "empty_slot_id_at_shard_start": ("st.id = (int32_t)(shard_end - 1);",
+                                     "st.id = (int32_t)(shard_start);"),
+    "block_count_off_by_one": (
+        "return (shard_start + shard_width - 1) / block - shard_start / block + 1;",
+        "return (shard_start + shard_width) / block - shard_start / block + 1;"),
+    "slots_take_the_smaller_count": ("n_draft > n_bonus ? n_draft : n_bonus",
+                                     "n_draft < n_bonus ? n_draft : n_bonus"),
 }
 
 PIN_CALLS = [
