@@ -9,7 +9,8 @@ bonus taken from the wrong row, a wrong E4M3 exponent bias, the fp8 scales
 dropped, block boundaries taken from the shard start instead of global ids,
 the bonus row's block size ignored or given to the wrong row, an empty block
 slot naming the shard's first id, a block count off by one, the smaller of
-the two block counts as the slot count), builds it with gcc, points the oracle wrapper
+the two block counts as the slot count, a draft-to-target map that drops the
+draft id), builds it with gcc, points the oracle wrapper
 at it, and runs the pin tests of tests/test_oracle_pins.py: at least one pin
 must fail for every mutant.  The committed oracle source is never modified.
 """
@@ -58,6 +59,8 @@ MUTANTS = {
         "return (shard_start + shard_width) / block - shard_start / block + 1;"),
     "slots_take_the_smaller_count": ("n_draft > n_bonus ? n_draft : n_bonus",
                                      "n_draft < n_bonus ? n_draft : n_bonus"),
+    "d2t_drops_the_draft_id": ("out_target_ids[r] = (int32_t)(k + d2t[k]);",
+                               "out_target_ids[r] = (int32_t)(d2t[k]);"),
 }
 
 PIN_CALLS = [
@@ -79,6 +82,7 @@ PIN_CALLS = [
     pins.test_lmhead_fp8_logits_match_numpy_with_scales,
     lambda: pins.test_block_stats_match_grouped_brute_force("bf16"),
     pins.test_block_pieces_follow_global_boundaries_across_shard_edges,
+    pins.test_d2t_map_hand_case,
 ]
 
 
