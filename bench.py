@@ -57,6 +57,10 @@ def parse_args():
                         "step from a CUDA graph and time the whole step (no per-launch events)")
     p.add_argument("--lmhead-rows", type=int, default=512,
                    help="rows (hidden states) of the fused LM-head workload")
+    p.add_argument("--lmhead-per-shard", action="store_true",
+                   help="lmhead workloads: one sga_lmhead_argmax call per shard (each "
+                        "emulated rank its own) instead of every shard through one "
+                        "sga_lmhead_argmax_shards call (one decode-size launch for M <= 64)")
     p.add_argument("--lmhead-shards", type=int, default=2,
                    help="vocab shards (emulated TP ranks) of the fused LM-head workload")
     p.add_argument("--lmhead-vocab", type=int, default=151936,
@@ -683,26 +687,30 @@ def lmhead_cpu_baseline(c, fp8, gpu_ids, target_seconds):
 DECODE_MAX_M = 64   # the library's decode-size LM-head kernel covers M <= 64
 
 
-def decode_roofline(weight_bytes, kern_ms, num_shards, fp8, captured_shape=True):
+def decode_roofline(weight_bytes, kern_ms, num_shards, fp8, captured_shape=True,
+                    one_call=True):
     """HBM roofline of the decode-size LM-head kernel: the weight is read once
     per step (one launch per shard)."""
     pk, pk_src = peaks()
     hbm = float(pk.get("hbm_gbs", FALLBACK_HBM_GBS))
     achieved = weight_bytes / (kern_ms * 1e-3) / 1e9
-    # the captures are of one shard of the default shape (2 x 75968 ids, H = 4096)
+    # the captures are of the default shape (2 x 75968 ids, H = 4096): one
+    # launch for both shards (one call), or one shard per launch
+    key = ("dram_bytes_per_launch_all_shards" if one_call else "dram_bytes_per_launch") + \
+        ("_fp8" if fp8 else "")
     traffic = ncu_traffic("lmhead_decode.md", ["greedy_spec_decode_gb300/csrc/lmhead_decode.cu",
                                                "greedy_spec_decode_gb300/csrc/tcgen05.cuh",
-                                               "greedy_spec_decode_gb300/csrc/common.cuh"],
-                          "dram_bytes_per_launch_fp8" if fp8 else "dram_bytes_per_launch")
+                                               "greedy_spec_decode_gb300/csrc/common.cuh"], key)
     return {"bound": "hbm",
             "kernel": "lmhead_argmax_decode_kernel<%s>" % ("fp8" if fp8 else "bf16"),
             "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
             "traffic": traffic if captured_shape else None,
-            "traffic_unit": "DRAM bytes per launch (one shard), %s M = 16 capture"
-                            % ("fp8" if fp8 else "bf16"),
+            "traffic_unit": "DRAM bytes per decode launch (%s), %s M = 16 capture"
+                            % ("every shard" if one_call else "one shard",
+                               "fp8" if fp8 else "bf16"),
             "peak_source": f"{pk_src} hbm_gbs (MEASURED_PEAKS.json copy bandwidth)"
             if pk_src == "measured" else "fallback 6.8 TB/s",
-            "bytes_per_step": weight_bytes, "launches_per_step": num_shards}
+            "bytes_per_step": weight_bytes, "launches_per_step": 1 if one_call else num_shards}
 
 
 def run_ours_lmhead(args, fp8=False):
@@ -734,12 +742,26 @@ def run_ours_lmhead(args, fp8=False):
     shards = c["shards"]
     S = len(shards)
     stats = sga.new_stats(S * M)
-    ws = torch.empty(max(sga.sga_lmhead_argmax_workspace(M, w) for _, w in shards),
-                     dtype=torch.uint8, device="cuda")
+    one_call = not args.lmhead_per_shard
+    ws_bytes = (sga.sga_lmhead_argmax_shards_workspace(M, shards) if one_call else
+                max(sga.sga_lmhead_argmax_workspace(M, w) for _, w in shards))
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     ids = torch.empty(M, dtype=torch.int32, device="cuda")
     w_views = [weight[o:o + w] for o, w in shards]
 
     def step(ev=None):
+        if one_call:
+            if ev is not None:
+                ev[0].record()
+            if fp8:
+                sga.sga_lmhead_argmax_shards_fp8(hidden, hscale, weight, c["weight_scale"],
+                                                 shards, c["org_vocab"], stats, ws)
+            else:
+                sga.sga_lmhead_argmax_shards(hidden, weight, shards, c["org_vocab"], stats, ws)
+            if ev is not None:
+                ev[1].record()
+            sga.sga_shard_reduce(stats, S, M, ids)
+            return
         for s, (o, w) in enumerate(shards):
             if ev is not None:
                 ev[2 * s].record()
@@ -786,8 +808,8 @@ def run_ours_lmhead(args, fp8=False):
     if graph is not None:
         kern_ms = step_ms   # the step as a whole (LM-head launches + finalize + reduce)
     else:
-        kern_ms = sum(sum(e[2 * s].elapsed_time(e[2 * s + 1]) for s in range(S))
-                      for e in ev) / args.steps
+        kern_ms = sum(sum(e[2 * s].elapsed_time(e[2 * s + 1])
+                          for s in range(1 if one_call else S)) for e in ev) / args.steps
     flops = 2.0 * M * H * sum(w for _, w in shards)
     pk, pk_src = peaks()
     peak = float(pk.get("bf16_tflops_sustained", pk.get("bf16_tflops", FALLBACK_BF16_TFLOPS)))
@@ -836,7 +858,8 @@ def run_ours_lmhead(args, fp8=False):
         "kernel_us": {"lmhead_argmax_per_step": round(kern_ms * 1e3, 2),
                       "reduce_and_gaps": round((step_ms - kern_ms) * 1e3, 2)},
         "roofline": decode_roofline(weight_bytes, kern_ms, S, fp8,
-                                    S == 2 and H == 4096 and args.lmhead_vocab == 151936)
+                                    S == 2 and H == 4096 and args.lmhead_vocab == 151936,
+                                    one_call)
         if decode else
                     {"bound": "tensor",
                      "kernel": "lmhead_argmax_2sm_kernel<fp8>" if fp8 else "lmhead_argmax_2sm_kernel",
@@ -862,7 +885,9 @@ def run_ours_lmhead(args, fp8=False):
                         "can differ and this figure can exceed `value`"},
         "timing": ("whole step replayed from a CUDA graph" if graph is not None else
                    "CUDA events around each LM-head call (GEMM + finalize)"),
-        "gpu_launches": args.steps * (2 * S + 1),
+        "calls": ("every shard in one sga_lmhead_argmax_shards call" if one_call else
+                  "one sga_lmhead_argmax call per shard (each emulated rank its own)"),
+        "gpu_launches": args.steps * (3 if one_call and M <= DECODE_MAX_M else 2 * S + 1),
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -61,6 +61,10 @@ def lib():
             "sga_shard_reduce": ([vp, i32, i64, vp, vp, vp, i64, vp], i32),
             "sga_greedy_verify": ([vp, i32, i32, vp, vp, i32, vp, vp, vp, vp, vp, vp], i32),
             "sga_lmhead_argmax_workspace": ([i64, i64], sz),
+            "sga_lmhead_argmax_shards_workspace": ([i64, i32, vp], sz),
+            "sga_lmhead_argmax_shards": ([vp, i64, i64, vp, i32, vp, vp, i64, vp, vp, sz, vp], i32),
+            "sga_lmhead_argmax_shards_fp8": ([vp, vp, i64, i64, vp, ctypes.c_float, i32, vp, vp,
+                                              i64, vp, vp, sz, vp], i32),
             "sga_lmhead_argmax": ([vp, i64, i64, vp, i64, i64, i64, vp, vp, sz, vp], i32),
             "sga_lmhead_argmax_fp8": ([vp, vp, i64, i64, vp, ctypes.c_float, i64, i64, i64, vp,
                                        vp, sz, vp], i32),
@@ -264,6 +268,60 @@ def sga_lmhead_argmax_fp8(hidden_q, hidden_scale, weight_q, weight_scale, shard_
     _check("sga_lmhead_argmax_fp8", lib().sga_lmhead_argmax_fp8(
         _ptr(hidden_q), _ptr(hidden_scale), M, H, _ptr(weight_q), float(weight_scale),
         int(shard_start), width, int(org_vocab), _ptr(out_stats), _ptr(workspace), nbytes,
+        _stream(stream)))
+    return out_stats
+
+
+def _shard_arrays(shards):
+    n = len(shards)
+    return (n, (ctypes.c_int64 * n)(*[int(o) for o, _ in shards]),
+            (ctypes.c_int64 * n)(*[int(w) for _, w in shards]))
+
+
+def sga_lmhead_argmax_shards_workspace(M, shards):
+    n, _, widths = _shard_arrays(shards)
+    return int(lib().sga_lmhead_argmax_shards_workspace(int(M), n, widths))
+
+
+def sga_lmhead_argmax_shards(hidden, weight, shards, org_vocab, out_stats, workspace,
+                             stream=None):
+    """Fused LM head + argmax of several shards of one weight buffer in one call:
+    weight: bf16 [rows, H] contiguous, row 0 = global id shards[0][0]; shards =
+    [(start, width), ...] ascending; out_stats receives len(shards) * M stats,
+    shard-major."""
+    if not (hidden.is_contiguous() and weight.is_contiguous()):
+        raise ValueError("hidden and weight must be contiguous")
+    M, H = hidden.shape
+    if weight.size(1) != H:
+        raise ValueError("hidden and weight must share H")
+    n, starts, widths = _shard_arrays(shards)
+    if starts[n - 1] - starts[0] + widths[n - 1] > weight.size(0):
+        raise ValueError("weight does not span the shards")
+    nbytes = workspace.numel() * workspace.element_size()
+    _check("sga_lmhead_argmax_shards", lib().sga_lmhead_argmax_shards(
+        _ptr(hidden), M, H, _ptr(weight), n, starts, widths, int(org_vocab), _ptr(out_stats),
+        _ptr(workspace), nbytes, _stream(stream)))
+    return out_stats
+
+
+def sga_lmhead_argmax_shards_fp8(hidden_q, hidden_scale, weight_q, weight_scale, shards,
+                                 org_vocab, out_stats, workspace, stream=None):
+    """sga_lmhead_argmax_shards with E4M3 operands (uint8 codes) and one weight
+    scale for the whole weight buffer (see include/sga.h)."""
+    if not (hidden_q.is_contiguous() and weight_q.is_contiguous()):
+        raise ValueError("hidden_q and weight_q must be contiguous")
+    if hidden_q.dtype != torch.uint8 or weight_q.dtype != torch.uint8:
+        raise TypeError("fp8 operands are passed as uint8 E4M3 codes")
+    M, H = hidden_q.shape
+    if weight_q.size(1) != H:
+        raise ValueError("hidden_q and weight_q must share H")
+    n, starts, widths = _shard_arrays(shards)
+    if starts[n - 1] - starts[0] + widths[n - 1] > weight_q.size(0):
+        raise ValueError("weight_q does not span the shards")
+    nbytes = workspace.numel() * workspace.element_size()
+    _check("sga_lmhead_argmax_shards_fp8", lib().sga_lmhead_argmax_shards_fp8(
+        _ptr(hidden_q), _ptr(hidden_scale), M, H, _ptr(weight_q), float(weight_scale), n,
+        starts, widths, int(org_vocab), _ptr(out_stats), _ptr(workspace), nbytes,
         _stream(stream)))
     return out_stats
 

@@ -66,12 +66,32 @@ cudaError_t launch_lmhead_argmax(const void *hidden, int64_t M, int64_t H, const
                                  const float *row_scale = nullptr, float w_scale = 1.0f);
 
 
-// Decode-size LM head (lmhead_decode.cu), M <= 64: writes one partial per
-// (row, CTA) to ws[row * (*ws_stride) + cta] and sets *ws_stride.
+// Shards of one LM-head launch, at most.
+constexpr int kMaxLmShards = 64;
+
+// Fused LM head + argmax of several shards of one weight buffer (row 0 =
+// global id starts[0]; shards ascending): stats of shard s to out[s * M ..];
+// one decode launch and one finalize for M <= 64, else one GEMM + finalize
+// per shard.  Workspace: lmhead_shards_workspace_bytes.
+cudaError_t launch_lmhead_argmax_shards(const void *hidden, int64_t M, int64_t H,
+                                        const void *weight, int num_shards,
+                                        const int64_t *starts, const int64_t *widths,
+                                        const int64_t *valids, sga_stat *out, void *workspace,
+                                        int num_sms, uint32_t *err, cudaStream_t stream,
+                                        bool fp8 = false, const float *row_scale = nullptr,
+                                        float w_scale = 1.0f);
+size_t lmhead_shards_workspace_bytes(int64_t M, int num_shards, const int64_t *widths);
+
+// Decode-size LM head (lmhead_decode.cu), M <= 64, over num_shards shards in
+// one launch: shard s covers global ids [starts[s], starts[s] + valids[s])
+// at weight rows row0s[s] .. (ascending shards).  Writes one partial per
+// (shard, row, CTA) to ws[(s * M + row) * (*ws_stride) + cta] and sets
+// *ws_stride (0 when no shard has a valid id: nothing is launched).
 cudaError_t launch_lmhead_decode(bool fp8, const void *hidden, int64_t M, int64_t H,
-                                 const void *weight, int64_t shard_start, int64_t valid,
-                                 sga_stat *ws, int n_tiles, int num_sms, uint32_t *err,
-                                 cudaStream_t stream, int *ws_stride);
+                                 const void *weight, int num_shards, const int64_t *starts,
+                                 const int64_t *row0s, const int64_t *valids, sga_stat *ws,
+                                 int num_sms, uint32_t *err, cudaStream_t stream,
+                                 int *ws_stride);
 
 // Bounded-wait self-test (lmhead.cu).
 cudaError_t launch_selftest_timeout(unsigned long long limit_ns, uint32_t *err,

@@ -602,15 +602,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 // Values of the fp8 variant are raw accumulators of the E4M3 codes until
 // here; the positive row and weight scales (which cannot change the argmax of
 // a row) are applied to the winning value only.
+// The shards whose partials one finalize launch merges: row r of the output
+// (shard r / M, hidden row r % M) reports shard start[r / M]'s first id when
+// no partial has a valid id.
+struct FinalizeShards {
+  int n;
+  int32_t start[kMaxLmShards];
+};
+
 __global__ void lmhead_finalize_kernel(const sga_stat *__restrict__ ws, int M, int n_tiles,
-                                       int shard_start, sga_stat *__restrict__ out,
+                                       const __grid_constant__ FinalizeShards shards,
+                                       sga_stat *__restrict__ out,
                                        const float *__restrict__ row_scale, float w_scale,
                                        int scaled) {
   pdl_wait();  // the partials of the GEMM kernel are complete and visible
   pdl_launch_dependents();  // the next kernel may start its prologue
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (r >= M) return;
+  if (r >= shards.n * M) return;
+  const int shard_start = shards.start[r / M];
   float bv = __int_as_float(0xff800000);
   int32_t bi = kNoId;
   const sga_stat *row = ws + static_cast<size_t>(r) * n_tiles;
@@ -637,7 +647,7 @@ __global__ void lmhead_finalize_kernel(const sga_stat *__restrict__ ws, int M, i
   warp_argmax(bv, bi);
   if (lane == 0) {
     sga_stat s;
-    s.v = scaled ? bv * ((row_scale ? row_scale[r] : 1.0f) * w_scale) : bv;
+    s.v = scaled ? bv * ((row_scale ? row_scale[r % M] : 1.0f) * w_scale) : bv;
     s.id = bi == kNoId ? shard_start : bi;
     out[r] = s;
   }
@@ -691,9 +701,11 @@ cudaError_t launch_gemm(const void *hidden, int64_t M, int64_t H, const void *we
                         uint32_t *err, cudaStream_t stream, int *ws_stride) {
   const int num_kb = static_cast<int>(H / kBk<kFp8>);
   *ws_stride = n_tiles;
-  if (M <= SGA_LMHEAD_DECODE_MAX_M)
-    return launch_lmhead_decode(kFp8, hidden, M, H, weight, shard_start, valid, ws, n_tiles,
+  if (M <= SGA_LMHEAD_DECODE_MAX_M) {
+    const int64_t row0 = 0;
+    return launch_lmhead_decode(kFp8, hidden, M, H, weight, 1, &shard_start, &row0, &valid, ws,
                                 num_sms, err, stream, ws_stride);
+  }
   if (SGA_LMHEAD_2SM && M >= SGA_LMHEAD_2SM_MIN_M && num_sms >= 2) {
     // 2-SM tiles (256 rows per CTA pair)
     CUtensorMap map_a, map_b;
@@ -738,6 +750,21 @@ cudaError_t launch_selftest_timeout(unsigned long long limit_ns, uint32_t *err,
 // Partials per row: one per 256-id tile, and for decode sizes at least one per
 // CTA of the decode kernel (up to kDecMaxParts), so that narrow shards still
 // spread over every SM.  For M <= 64 the extra is at most 128 KB.
+// Workspace of launch_lmhead_argmax_shards: decode sizes keep num_shards x M
+// x (CTAs of the launch, at most kDecMaxParts) partials; larger M reuses one
+// shard's workspace per shard.
+size_t lmhead_shards_workspace_bytes(int64_t M, int num_shards, const int64_t *widths) {
+  if (M <= SGA_LMHEAD_DECODE_MAX_M)
+    return static_cast<size_t>(num_shards) * static_cast<size_t>(M) * kDecMaxParts *
+           sizeof(sga_stat);
+  size_t most = 0;
+  for (int s = 0; s < num_shards; ++s) {
+    const size_t b = lmhead_workspace_bytes(M, widths[s]);
+    if (b > most) most = b;
+  }
+  return most;
+}
+
 size_t lmhead_workspace_bytes(int64_t M, int64_t width) {
   int64_t parts = (width + BN - 1) / BN;
   if (M <= SGA_LMHEAD_DECODE_MAX_M) {
@@ -747,6 +774,30 @@ size_t lmhead_workspace_bytes(int64_t M, int64_t width) {
   }
   return static_cast<size_t>(parts * M) * sizeof(sga_stat);
 }
+
+namespace {
+
+// The finalize launch over every (shard, row) of a step: 8 rows per block;
+// programmatic dependent launch lets the blocks become resident while the
+// GEMM kernel drains (they wait in pdl_wait()).
+cudaError_t launch_finalize(const sga_stat *ws, int64_t M, int ws_stride,
+                            const FinalizeShards &shards, sga_stat *out,
+                            const float *row_scale, float w_scale, bool fp8,
+                            cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((shards.n * M + 7) / 8));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, lmhead_finalize_kernel, ws, static_cast<int>(M), ws_stride,
+                            shards, out, row_scale, w_scale, fp8 ? 1 : 0);
+}
+
+}  // namespace
 
 cudaError_t launch_lmhead_argmax(const void *hidden, int64_t M, int64_t H, const void *weight,
                                  int64_t shard_start, int64_t width, int64_t valid,
@@ -765,20 +816,46 @@ cudaError_t launch_lmhead_argmax(const void *hidden, int64_t M, int64_t H, const
                                  err, stream, &ws_stride);
     if (e != cudaSuccess) return e;
   }
-  // 8 rows per block; programmatic dependent launch lets the blocks become
-  // resident while the GEMM kernel drains (they wait in pdl_wait()).
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>((M + 7) / 8));
-  cfg.blockDim = dim3(256);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, lmhead_finalize_kernel, static_cast<const sga_stat *>(ws),
-                            static_cast<int>(M), ws_stride, static_cast<int>(shard_start), out,
-                            row_scale, w_scale, fp8 ? 1 : 0);
+  FinalizeShards fs = {};
+  fs.n = 1;
+  fs.start[0] = static_cast<int32_t>(shard_start);
+  return launch_finalize(ws, M, ws_stride, fs, out, row_scale, w_scale, fp8, stream);
+}
+
+cudaError_t launch_lmhead_argmax_shards(const void *hidden, int64_t M, int64_t H,
+                                        const void *weight, int num_shards,
+                                        const int64_t *starts, const int64_t *widths,
+                                        const int64_t *valids, sga_stat *out, void *workspace,
+                                        int num_sms, uint32_t *err, cudaStream_t stream,
+                                        bool fp8, const float *row_scale, float w_scale) {
+  sga_stat *ws = static_cast<sga_stat *>(workspace);
+  if (M > SGA_LMHEAD_DECODE_MAX_M) {
+    // tensor-bound sizes: one GEMM + finalize per shard, the workspace reused
+    // (each launch waits for the previous one before touching it)
+    const size_t row_bytes = static_cast<size_t>(H) * (fp8 ? 1 : 2);
+    for (int s = 0; s < num_shards; ++s) {
+      const void *w = static_cast<const char *>(weight) +
+                      static_cast<size_t>(starts[s] - starts[0]) * row_bytes;
+      const cudaError_t e =
+          launch_lmhead_argmax(hidden, M, H, w, starts[s], widths[s], valids[s], out + s * M,
+                               workspace, num_sms, err, stream, fp8, row_scale, w_scale);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
+  // decode sizes: every shard in one launch, one finalize for all of them
+  int64_t row0s[kMaxLmShards];
+  FinalizeShards fs = {};
+  fs.n = num_shards;
+  for (int s = 0; s < num_shards; ++s) {
+    row0s[s] = starts[s] - starts[0];
+    fs.start[s] = static_cast<int32_t>(starts[s]);
+  }
+  int ws_stride = 0;
+  const cudaError_t e = launch_lmhead_decode(fp8, hidden, M, H, weight, num_shards, starts, row0s,
+                                             valids, ws, num_sms, err, stream, &ws_stride);
+  if (e != cudaSuccess) return e;
+  return launch_finalize(ws, M, ws_stride, fs, out, row_scale, w_scale, fp8, stream);
 }
 
 }  // namespace sga

@@ -74,6 +74,18 @@ struct SharedDec {
   int32_t part_i[4][kN];
 };
 
+// The shards of one launch (one, or all the shards a GPU holds): shard s
+// covers global ids [start, start + valid) (its non-padding ids) at weight
+// rows row0 .. row0 + valid - 1 of the launch's weight map, and its tiles are
+// numbers tile0[s] .. tile0[s + 1] - 1 of the launch.
+struct DecShardTable {
+  int n;
+  int32_t start[kMaxLmShards];
+  int32_t row0[kMaxLmShards];
+  int32_t valid[kMaxLmShards];
+  int32_t tile0[kMaxLmShards + 1];
+};
+
 template <int kN>
 constexpr int dec_smem_bytes =
     1024 + dec_stages<kN> * dec_stage_bytes<kN> + static_cast<int>(sizeof(SharedDec<kN>));
@@ -181,7 +193,7 @@ template <bool kFp8, int kN>
 __global__ void __launch_bounds__(THREADS, 1)
     lmhead_argmax_decode_kernel(const __grid_constant__ CUtensorMap tmap_w,
                                 const __grid_constant__ CUtensorMap tmap_h, int M, int num_kb,
-                                int n_tiles, int valid, int shard_start,
+                                const __grid_constant__ DecShardTable tab,
                                 sga_stat *__restrict__ ws, uint32_t *err) {
   constexpr int kStages = dec_stages<kN>;
   constexpr int kStageBytes = dec_stage_bytes<kN>;
@@ -198,6 +210,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const volatile int *abort_flag = &sh->abort;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int n_tiles = tab.tile0[tab.n];
 
   if (SGA_LMHEAD_DEC_PREFETCH && threadIdx.x == 64 && blockIdx.x < n_tiles) {
     // Warm L2 with what the ring loads first (this CTA's first tile, one
@@ -205,9 +218,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     // only moves lines into L2, which stays coherent with any later write, so
     // it may precede griddepcontrol.wait.
     const int n = blockIdx.x;
+    int s = 0;
+    while (n >= tab.tile0[s + 1]) ++s;
+    const int row = tab.row0[s] + (n - tab.tile0[s]) * kTileIds;
     for (int kb = 0; kb < num_kb && kb < kStages * kChunks; ++kb)
       for (int h = 0; h < kHalves; ++h)
-        tma_prefetch_2d(&tmap_w, kb * kBk<kFp8>, n * kTileIds + h * 128);
+        tma_prefetch_2d(&tmap_w, kb * kBk<kFp8>, row + h * 128);
   }
 
   if (threadIdx.x == 0) {
@@ -247,7 +263,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
+      int s = 0;  // the shard of tile n (the tiles only increase)
       for (int n = blockIdx.x; n < n_tiles && !*abort_flag; n += gridDim.x) {
+        while (n >= tab.tile0[s + 1]) ++s;
+        const int row = tab.row0[s] + (n - tab.tile0[s]) * kTileIds;
         for (int kb = 0; kb < num_kb; kb += kChunks) {
           if (!mbar_wait(smem_u32(&sh->empty[prod_stage]), prod_phase ^ 1, abort_flag)) {
             raise_abort_dec(sh, err);
@@ -260,7 +279,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int c = 0; c < chunks; ++c) {
             for (int h = 0; h < kHalves; ++h)
               tma_load_2d(stage_addr + (c * kHalves + h) * DEC_SUB_BYTES, &tmap_w,
-                          (kb + c) * kBk<kFp8>, n * kTileIds + h * 128, full);
+                          (kb + c) * kBk<kFp8>, row + h * 128, full);
             tma_load_2d(stage_addr + dec_a_bytes<kN> + c * kN * ROW_BYTES, &tmap_h,
                         (kb + c) * kBk<kFp8>, 0, full);
           }
@@ -320,17 +339,54 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------- epilogue
+    // The CTA's tiles cross each shard edge at most once, in shard order.  At
+    // every edge (and for every shard without a tile of this CTA) the four
+    // epilogue warps flush the shard's per-row bests: each writes its rows'
+    // bests to shared memory, then epilogue thread e < M merges row e's four
+    // and stores the CTA's partial of (shard, row e).  Every warp flushes
+    // every shard exactly once, in order, also after an abort, so the
+    // 128-thread barriers of the flushes always match.
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 belong to this warp
+    const int e = static_cast<int>(threadIdx.x) - 64;  // epilogue thread 0 .. 127
     float rv[kSlots];
     int32_t ri[kSlots];
 #pragma unroll
-    for (int s = 0; s < kSlots; ++s) {
-      rv[s] = __int_as_float(0xff800000);
-      ri[s] = kNoId;
+    for (int g = 0; g < kSlots; ++g) {
+      rv[g] = __int_as_float(0xff800000);
+      ri[g] = kNoId;
     }
+    auto flush = [&](int s) {
+#pragma unroll
+      for (int g = 0; g < kSlots; ++g) {
+        // lane l holds row l of the group (kG = 32) or row l / 2 (kG = 16;
+        // both lanes of a pair hold it)
+        if (kG == 32 || (lane & 1) == 0) {
+          const int j = g * kG + (kG == 32 ? lane : lane >> 1);
+          sh->part_v[quarter][j] = rv[g];
+          sh->part_i[quarter][j] = ri[g];
+        }
+        rv[g] = __int_as_float(0xff800000);
+        ri[g] = kNoId;
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (e < M) {
+        // (any order: the (value, id) order is total)
+        float v = sh->part_v[0][e];
+        int32_t id = sh->part_i[0][e];
+#pragma unroll
+        for (int q = 1; q < 4; ++q) keep_better(v, id, sh->part_v[q][e], sh->part_i[q][e]);
+        sga_stat st;
+        st.v = v;
+        st.id = id;
+        ws[(static_cast<size_t>(s) * M + e) * gridDim.x + blockIdx.x] = st;
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");  // before the next flush's writes
+    };
+    int cur = 0;  // the shard whose bests rv / ri hold
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int n = blockIdx.x; n < n_tiles; n += gridDim.x) {
+      while (n >= tab.tile0[cur + 1]) flush(cur++);
       bool ok = mbar_wait(smem_u32(&sh->tmem_full[acc]), acc_phase, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
@@ -338,11 +394,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         break;
       }
       tc_fence_after();
+      const int tile_local = (n - tab.tile0[cur]) * kTileIds;
 #pragma unroll 1
       for (int h = 0; h < kHalves; ++h) {
-        const int local = n * kTileIds + h * 128 + quarter * 32 + lane;  // shard-local id
-        const bool live = local < valid;
-        const int32_t id = live ? shard_start + local : kNoId;
+        const int local = tile_local + h * 128 + quarter * 32 + lane;  // shard-local id
+        const bool live = local < tab.valid[cur];
+        const int32_t id = live ? tab.start[cur] + local : kNoId;
         const uint32_t taddr =
             tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + (acc * kHalves + h) * kN;
 #pragma unroll
@@ -365,16 +422,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
-#pragma unroll
-    for (int g = 0; g < kSlots; ++g) {
-      // lane l holds row l of the group (kG = 32) or row l / 2 (kG = 16; both
-      // lanes of a pair hold it)
-      if (kG == 32 || (lane & 1) == 0) {
-        const int j = g * kG + (kG == 32 ? lane : lane >> 1);
-        sh->part_v[quarter][j] = rv[g];
-        sh->part_i[quarter][j] = ri[g];
-      }
-    }
+    while (cur < tab.n) flush(cur++);
   }
 
   pdl_launch_dependents();
@@ -401,25 +449,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   }
   __syncthreads();
-  if (threadIdx.x < M) {
-    // merge the four epilogue warps' bests of row threadIdx.x (any order: the
-    // (value, id) order is total)
-    float v = sh->part_v[0][threadIdx.x];
-    int32_t id = sh->part_i[0][threadIdx.x];
-#pragma unroll
-    for (int q = 1; q < 4; ++q) {
-      const float cv = sh->part_v[q][threadIdx.x];
-      const int32_t ci = sh->part_i[q][threadIdx.x];
-      if (pair_beats(cv, ci, v, id)) {
-        v = cv;
-        id = ci;
-      }
-    }
-    sga_stat st;
-    st.v = v;
-    st.id = id;
-    ws[static_cast<size_t>(threadIdx.x) * gridDim.x + blockIdx.x] = st;
-  }
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
@@ -430,48 +459,52 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 template <bool kFp8, int kN>
 cudaError_t launch_decode(const void *hidden, int64_t M, int64_t H, const void *weight,
-                          int64_t shard_start, int64_t valid, sga_stat *ws, int n_tiles,
-                          int num_sms, uint32_t *err, cudaStream_t stream, int *ws_stride) {
+                          int num_shards, const int64_t *starts, const int64_t *row0s,
+                          const int64_t *valids, sga_stat *ws, int num_sms, uint32_t *err,
+                          cudaStream_t stream, int *ws_stride) {
+  const int tile_ids = 128 * dec_halves<kN>;
+  DecShardTable tab = {};
+  tab.n = num_shards;
+  int64_t map_rows = 0;  // weight rows the launch reads: up to the last shard's last valid row
+  for (int s = 0; s < num_shards; ++s) {
+    tab.start[s] = static_cast<int32_t>(starts[s]);
+    tab.row0[s] = static_cast<int32_t>(row0s[s]);
+    tab.valid[s] = static_cast<int32_t>(valids[s]);
+    tab.tile0[s + 1] = tab.tile0[s] + static_cast<int32_t>((valids[s] + tile_ids - 1) / tile_ids);
+    if (valids[s] > 0 && row0s[s] + valids[s] > map_rows) map_rows = row0s[s] + valids[s];
+  }
+  const int n_tiles = tab.tile0[num_shards];
+  // one CTA per SM, at most one per tile and kDecMaxParts; the workspace
+  // holds num_shards x M x grid partials
+  int grid = n_tiles < num_sms ? n_tiles : num_sms;
+  if (grid > kDecMaxParts) grid = kDecMaxParts;
+  *ws_stride = grid;
+  if (grid == 0) return cudaSuccess;  // every shard is padding: the finalize alone reports it
   CUtensorMap map_w, map_h;
-  if (!make_map(&map_w, weight, valid, H, 128, kFp8) || !make_map(&map_h, hidden, M, H, kN, kFp8))
+  if (!make_map(&map_w, weight, map_rows, H, 128, kFp8) || !make_map(&map_h, hidden, M, H, kN, kFp8))
     return cudaErrorInvalidValue;
   auto kern = lmhead_argmax_decode_kernel<kFp8, kN>;
   const int slot = 4 + (kFp8 ? 4 : 0) + (kN == 16 ? 0 : kN == 32 ? 1 : kN == 64 ? 2 : 3);
   cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), dec_smem_bytes<kN>, slot);
   if (e != cudaSuccess) return e;
-  // one CTA per SM, at most one per tile; the workspace holds
-  // min(ceil(width / 128), kDecMaxParts) partials per row for M <= 64
-  (void)n_tiles;
-  const int tile_ids = 128 * dec_halves<kN>;
-  const int dec_tiles = static_cast<int>((valid + tile_ids - 1) / tile_ids);
-  int grid = dec_tiles < num_sms ? dec_tiles : num_sms;
-  if (grid > kDecMaxParts) grid = kDecMaxParts;
-  *ws_stride = grid;
   return launch_pdl(kern, grid, dec_smem_bytes<kN>, stream, map_w, map_h, static_cast<int>(M),
-                    static_cast<int>(H / kBk<kFp8>), dec_tiles, static_cast<int>(valid),
-                    static_cast<int>(shard_start), ws, err);
+                    static_cast<int>(H / kBk<kFp8>), tab, ws, err);
 }
 
 }  // namespace
 
 cudaError_t launch_lmhead_decode(bool fp8, const void *hidden, int64_t M, int64_t H,
-                                 const void *weight, int64_t shard_start, int64_t valid,
-                                 sga_stat *ws, int n_tiles, int num_sms, uint32_t *err,
-                                 cudaStream_t stream, int *ws_stride) {
-  if (M <= 16)
-    return fp8 ? launch_decode<true, 16>(hidden, M, H, weight, shard_start, valid, ws, n_tiles,
-                                         num_sms, err, stream, ws_stride)
-               : launch_decode<false, 16>(hidden, M, H, weight, shard_start, valid, ws, n_tiles,
-                                          num_sms, err, stream, ws_stride);
-  if (M <= 32)
-    return fp8 ? launch_decode<true, 32>(hidden, M, H, weight, shard_start, valid, ws, n_tiles,
-                                         num_sms, err, stream, ws_stride)
-               : launch_decode<false, 32>(hidden, M, H, weight, shard_start, valid, ws, n_tiles,
-                                          num_sms, err, stream, ws_stride);
-  return fp8 ? launch_decode<true, 64>(hidden, M, H, weight, shard_start, valid, ws, n_tiles,
-                                       num_sms, err, stream, ws_stride)
-             : launch_decode<false, 64>(hidden, M, H, weight, shard_start, valid, ws, n_tiles,
-                                        num_sms, err, stream, ws_stride);
+                                 const void *weight, int num_shards, const int64_t *starts,
+                                 const int64_t *row0s, const int64_t *valids, sga_stat *ws,
+                                 int num_sms, uint32_t *err, cudaStream_t stream,
+                                 int *ws_stride) {
+#define SGA_DEC_LAUNCH(F, N)                                                                   \
+  launch_decode<F, N>(hidden, M, H, weight, num_shards, starts, row0s, valids, ws, num_sms, err, \
+                      stream, ws_stride)
+  if (M <= 16) return fp8 ? SGA_DEC_LAUNCH(true, 16) : SGA_DEC_LAUNCH(false, 16);
+  if (M <= 32) return fp8 ? SGA_DEC_LAUNCH(true, 32) : SGA_DEC_LAUNCH(false, 32);
+  return fp8 ? SGA_DEC_LAUNCH(true, 64) : SGA_DEC_LAUNCH(false, 64);
+#undef SGA_DEC_LAUNCH
 }
 
 }  // namespace sga

@@ -320,6 +320,81 @@ int sga_lmhead_argmax_fp8(const void *hidden_q, const float *hidden_scale, int64
   return launch_status(e);
 }
 
+// Shared checks of the multi-shard LM-head entry points: the shards (each as
+// in sga_lmhead_argmax, ascending, non-overlapping) and their valid ids.
+static int check_lm_shards(int num_shards, const int64_t *starts, const int64_t *widths,
+                           int64_t org_vocab, int64_t *valids) {
+  if (num_shards < 1 || num_shards > sga::kMaxLmShards) return SGA_ERR_SIZE;
+  if (starts == nullptr || widths == nullptr) return SGA_ERR_NULL;
+  for (int s = 0; s < num_shards; ++s) {
+    const int st = check_shard(starts[s], widths[s], org_vocab);
+    if (st != SGA_OK) return st;
+    if (s > 0 && starts[s] < starts[s - 1] + widths[s - 1]) return SGA_ERR_SHARD;
+    valids[s] = valid_ids(starts[s], widths[s], org_vocab);
+  }
+  return SGA_OK;
+}
+
+size_t sga_lmhead_argmax_shards_workspace(int64_t M, int num_shards,
+                                          const int64_t *shard_widths) {
+  if (M <= 0 || num_shards < 1 || num_shards > sga::kMaxLmShards || shard_widths == nullptr)
+    return 0;
+  for (int s = 0; s < num_shards; ++s)
+    if (shard_widths[s] <= 0) return 0;
+  return sga::lmhead_shards_workspace_bytes(M, num_shards, shard_widths);
+}
+
+static int lmhead_shards_common(const void *hidden, const float *hidden_scale, int64_t M,
+                                int64_t H, const void *weight, bool fp8, float weight_scale,
+                                int num_shards, const int64_t *shard_starts,
+                                const int64_t *shard_widths, int64_t org_vocab,
+                                sga_stat *out_stats, void *workspace, size_t workspace_bytes,
+                                sga_stream stream) {
+  if (M < 0 || M > (int64_t(1) << 20)) return SGA_ERR_SIZE;
+  if (H <= 0 || H % (fp8 ? 128 : 64) != 0 || H > (int64_t(1) << 20)) return SGA_ERR_SIZE;
+  if (fp8 && (!(weight_scale > 0.0f) || !(weight_scale < 3.4e38f))) return SGA_ERR_SIZE;
+  int64_t valids[sga::kMaxLmShards];
+  int st = check_lm_shards(num_shards, shard_starts, shard_widths, org_vocab, valids);
+  if (st != SGA_OK) return st;
+  if (M == 0) return SGA_OK;
+  if (hidden == nullptr || weight == nullptr || out_stats == nullptr || workspace == nullptr)
+    return SGA_ERR_NULL;
+  if (misaligned(hidden, 16) || misaligned(weight, 16) || misaligned(out_stats, 8) ||
+      misaligned(workspace, 8) || misaligned(hidden_scale, 4))
+    return SGA_ERR_ALIGN;
+  if (workspace_bytes < sga::lmhead_shards_workspace_bytes(M, num_shards, shard_widths))
+    return SGA_ERR_WORKSPACE;
+  DeviceInfo d;
+  if ((st = current_device(&d)) != SGA_OK) return st;
+  const cudaError_t e = sga::launch_lmhead_argmax_shards(
+      hidden, M, H, weight, num_shards, shard_starts, shard_widths, valids, out_stats, workspace,
+      d.num_sms, d.err, static_cast<cudaStream_t>(stream), fp8, fp8 ? hidden_scale : nullptr,
+      fp8 ? weight_scale : 1.0f);
+  if (e == cudaErrorNotSupported) return SGA_ERR_UNSUPPORTED;
+  return launch_status(e);
+}
+
+int sga_lmhead_argmax_shards(const void *hidden, int64_t M, int64_t H, const void *weight,
+                             int num_shards, const int64_t *shard_starts,
+                             const int64_t *shard_widths, int64_t org_vocab,
+                             sga_stat *out_stats, void *workspace, size_t workspace_bytes,
+                             sga_stream stream) {
+  return lmhead_shards_common(hidden, nullptr, M, H, weight, false, 1.0f, num_shards,
+                              shard_starts, shard_widths, org_vocab, out_stats, workspace,
+                              workspace_bytes, stream);
+}
+
+int sga_lmhead_argmax_shards_fp8(const void *hidden_q, const float *hidden_scale, int64_t M,
+                                 int64_t H, const void *weight_q, float weight_scale,
+                                 int num_shards, const int64_t *shard_starts,
+                                 const int64_t *shard_widths, int64_t org_vocab,
+                                 sga_stat *out_stats, void *workspace, size_t workspace_bytes,
+                                 sga_stream stream) {
+  return lmhead_shards_common(hidden_q, hidden_scale, M, H, weight_q, true, weight_scale,
+                              num_shards, shard_starts, shard_widths, org_vocab, out_stats,
+                              workspace, workspace_bytes, stream);
+}
+
 // Same work as sga_lmhead_argmax, with the library's fixed scratch array in
 // place of a caller workspace, for callers that cannot allocate device memory.
 int sga_lmhead_argmax_noalloc(const void *hidden, int64_t M, int64_t H,

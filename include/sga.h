@@ -343,6 +343,49 @@ int sga_lmhead_argmax_fp8(const void *hidden_q, const float *hidden_scale, int64
                           void *workspace, size_t workspace_bytes, sga_stream stream);
 
 /*
+ * sga_lmhead_argmax_shards -- sga_lmhead_argmax for several vocab shards of
+ * one weight buffer in a single call (one GPU holding the vocab slices of
+ * several tensor-parallel ranks), as sga_local_argmax_shards is for the
+ * per-shard argmax.  At decode sizes (M <= 64) every shard runs in one
+ * launch of the decode-size kernel and one finalize launch, instead of a
+ * launch pair per shard; for larger M each shard runs as in
+ * sga_lmhead_argmax, one after the other.  The statistics are identical to
+ * num_shards sga_lmhead_argmax calls.
+ * Page: as sga_lmhead_argmax (vLLM PR #62604, Purpose; PR #39419, Changes).
+ *
+ *   weight        device [rows, H] (bf16), 16-byte aligned; row g -
+ *                 shard_starts[0] holds global id g (the buffer spans every
+ *                 shard, and any gap between them).
+ *   num_shards    1 .. 64.
+ *   shard_starts, shard_widths   HOST arrays, shards ascending and
+ *                 non-overlapping, each as sga_lmhead_argmax's.
+ *   out_stats     device, num_shards * M entries, 8-byte aligned: shard s's
+ *                 stats at out_stats[s * M + r] (the gathered layout).
+ *   workspace     device, >= sga_lmhead_argmax_shards_workspace(M,
+ *                 num_shards, shard_widths) bytes, 8-byte aligned, as
+ *                 sga_lmhead_argmax's.
+ * Other arguments and the errors as sga_lmhead_argmax.
+ */
+size_t sga_lmhead_argmax_shards_workspace(int64_t M, int num_shards, const int64_t *shard_widths);
+int sga_lmhead_argmax_shards(const void *hidden, int64_t M, int64_t H, const void *weight,
+                             int num_shards, const int64_t *shard_starts,
+                             const int64_t *shard_widths, int64_t org_vocab,
+                             sga_stat *out_stats, void *workspace, size_t workspace_bytes,
+                             sga_stream stream);
+
+/*
+ * sga_lmhead_argmax_shards_fp8 -- sga_lmhead_argmax_shards with the E4M3
+ * operands of sga_lmhead_argmax_fp8: one weight_scale for the whole weight
+ * buffer; otherwise as sga_lmhead_argmax_fp8 and sga_lmhead_argmax_shards.
+ */
+int sga_lmhead_argmax_shards_fp8(const void *hidden_q, const float *hidden_scale, int64_t M,
+                                 int64_t H, const void *weight_q, float weight_scale,
+                                 int num_shards, const int64_t *shard_starts,
+                                 const int64_t *shard_widths, int64_t org_vocab,
+                                 sga_stat *out_stats, void *workspace, size_t workspace_bytes,
+                                 sga_stream stream);
+
+/*
  * sga_lmhead_argmax_noalloc -- sga_lmhead_argmax for callers that must not
  * allocate device memory.  The pages have no counterpart to this entry point.
  *

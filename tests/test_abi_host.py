@@ -94,6 +94,43 @@ def test_lmhead_validation(sga_lib):
     assert f(FAKE, 4, 64, FAKE, 0, 64, 0, FAKE, FAKE, ws, None) == -4
 
 
+def test_lmhead_shards_validation(sga_lib):
+    L = sga_lib.lib()
+
+    def arr(v):
+        return (ctypes.c_int64 * len(v))(*v)
+
+    wsf = L.sga_lmhead_argmax_shards_workspace
+    assert wsf(16, 2, arr([75968, 75968])) == 2 * 16 * 256 * 8   # decode sizes: one launch
+    assert wsf(512, 2, arr([75968, 1000])) == L.sga_lmhead_argmax_workspace(512, 75968)
+    assert wsf(16, 0, arr([1])) == 0 and wsf(16, 65, None) == 0 and wsf(16, 1, arr([0])) == 0
+    ws = wsf(16, 2, arr([64, 64]))
+    f = L.sga_lmhead_argmax_shards
+
+    def call(starts, widths, M=16, H=64, org=128, hidden=FAKE, weight=FAKE, out=FAKE,
+             work=FAKE, nbytes=ws):
+        return f(hidden, M, H, weight, len(starts), arr(starts), arr(widths), org, out, work,
+                 nbytes, None)
+
+    assert call([0, 40], [64, 64]) == -3                        # overlap
+    assert call([0, 64], [64, 0]) == -3                         # empty shard
+    assert call([0, 64], [64, 64], H=100) == -2                 # H % 64
+    assert call([0, 64], [64, 64], M=-1) == -2
+    assert call([0, 64], [64, 64], M=0) == 0
+    assert call([0, 64], [64, 64], weight=None) == -1
+    assert call([0, 64], [64, 64], weight=ctypes.c_void_p(0x10008)) == -6
+    assert call([0, 64], [64, 64], nbytes=ws - 8) == -7
+    assert call([0, 64], [64, 64], org=0) == -4
+    assert f(FAKE, 16, 64, FAKE, 0, None, None, 128, FAKE, FAKE, ws, None) == -2
+    assert f(FAKE, 16, 64, FAKE, 65, None, None, 128, FAKE, FAKE, ws, None) == -2
+    assert f(FAKE, 16, 64, FAKE, 2, None, None, 128, FAKE, FAKE, ws, None) == -1
+    g = L.sga_lmhead_argmax_shards_fp8
+    a0, a1 = arr([0, 128]), arr([128, 128])
+    assert g(FAKE, None, 16, 128, FAKE, 0.0, 2, a0, a1, 256, FAKE, FAKE, ws, None) == -2
+    assert g(FAKE, None, 16, 64, FAKE, 1.0, 2, a0, a1, 256, FAKE, FAKE, ws, None) == -2
+    assert g(FAKE, BAD_F32, 16, 128, FAKE, 1.0, 2, a0, a1, 256, FAKE, FAKE, ws, None) == -6
+
+
 def test_missing_library_fails_loudly(monkeypatch, sga_lib):
     monkeypatch.setattr(sga_lib, "_lib", None)
     monkeypatch.setattr(sga_lib, "LIB_PATH", os.path.join(ROOT, "nonexistent", "libsga.so"))

@@ -1,0 +1,91 @@
+"""GPU parity of sga_lmhead_argmax_shards / _fp8: the LM head over several vocab
+shards of one weight buffer in one call (at decode sizes one launch of the
+decode-size kernel and one finalize for every shard).  Each tile's
+accumulation is the same as in one call per shard and the per-row merge uses
+the total (value, id) order, so the statistics must be bit-identical to
+num_shards sga_lmhead_argmax calls; sampled rows are also checked against the
+oracle's fp64 logits within the LM-head tolerance.  vLLM PR #62604, Purpose
+(vocab-parallel LM head), item 2 (fused get_top_tokens).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+import gpu_helpers as gh
+import test_parity_lmhead as lm
+import test_parity_lmhead_fp8 as f8
+
+pytestmark = pytest.mark.gpu
+
+
+def one_call(sga, h, w, shards, org_vocab, fp8=False, hs=None, w_scale=1.0):
+    """All shards through one sga_lmhead_argmax_shards[_fp8] call; w spans
+    [shards[0][0], last end)."""
+    M = h.shape[0]
+    stats = torch.full((len(shards) * M, 2), -5, dtype=torch.int32, device="cuda")
+    ws = torch.empty(max(8, sga.sga_lmhead_argmax_shards_workspace(M, shards)),
+                     dtype=torch.uint8, device="cuda")
+    if fp8:
+        sga.sga_lmhead_argmax_shards_fp8(h, hs, w, w_scale, shards, org_vocab, stats, ws)
+    else:
+        sga.sga_lmhead_argmax_shards(h, w, shards, org_vocab, stats, ws)
+    assert sga.sga_device_error() == 0
+    return gh.stats_to_numpy(stats)
+
+
+@pytest.mark.parametrize("M", [1, 7, 16, 17, 32, 33, 64, 65, 200])
+@pytest.mark.parametrize("layout", ["uneven3", "gap", "padded", "eight", "single"])
+def test_bf16_one_call_equals_per_shard_calls(sga_lib, M, layout):
+    H = 256
+    if layout == "uneven3":
+        vocab, org, shards = 10000, 10000, [(0, 3334), (3334, 3333), (6667, 3333)]
+    elif layout == "gap":          # a GPU holding shards 0 and 2 of three
+        vocab, org, shards = 9000, 9000, [(0, 3000), (6000, 3000)]
+    elif layout == "padded":       # the last shard past org_vocab, the one before it partly
+        vocab, org, shards = 6144, 3500, [(0, 2048), (2048, 2048), (4096, 2048)]
+    elif layout == "eight":
+        vocab, org, shards = 16384, 16000, wl.even_shards(16384, 8)
+    else:
+        vocab, org, shards = 5000, 4990, [(0, 5000)]
+    hidden = wl.normal_matrix(M + 11, M, H, 1.0)
+    weight = wl.normal_matrix(M + 12, vocab, H, 1.0 / np.sqrt(H))
+    per, vals, ids = lm.run_gpu(hidden, weight, shards, org)
+    o0, end = shards[0][0], shards[-1][0] + shards[-1][1]
+    one = one_call(sga_lib, gh.to_device(hidden), gh.to_device(weight)[o0:end], shards, org)
+    gh.assert_stats_equal(one, per)
+    if layout != "gap":   # (the oracle's full-vocab argmax would see the ids between shards)
+        rows = np.arange(M) if M <= 20 else np.arange(0, M, 7)
+        lm.check_rows(rows, hidden, weight, shards, org, per, vals, ids)
+
+
+@pytest.mark.parametrize("M", [1, 16, 40, 64, 100])
+def test_fp8_one_call_equals_per_shard_calls(sga_lib, M):
+    H, vocab = 256, 12288
+    shards = [(0, 4096), (4096, 4096), (8192, 4096)]
+    org = 12200
+    hq, hs, wq, w_scale = f8.make(M, H, vocab, 900 + M)
+    per, vals, ids = f8.run_gpu(sga_lib, hq, hs, wq, w_scale, shards, org)
+    hs_d = torch.from_numpy(np.ascontiguousarray(hs, np.float32)).cuda()
+    one = one_call(sga_lib, f8.u8(hq), f8.u8(wq), shards, org, fp8=True, hs=hs_d,
+                   w_scale=w_scale)
+    gh.assert_stats_equal(one, per)
+    f8.check(np.arange(0, M, 5), hq, hs, wq, w_scale, shards, org, per, vals, ids)
+
+
+def test_fused_lmhead_decode_shape_every_shard_in_one_launch(sga_lib):
+    # the fused LM-head weight (151936 x 4096, 2 and 8 shards) at M = 16,
+    # against the per-shard calls bit for bit
+    c = wl.fused_lmhead(m=16)
+    h = torch.from_numpy(c["hidden"].view(np.int16)).view(torch.bfloat16).cuda()
+    w = torch.from_numpy(c["weight"].view(np.int16)).view(torch.bfloat16).cuda()
+    for shards in (c["shards"], wl.even_shards(151936, 8)):
+        M = 16
+        per = torch.full((len(shards) * M, 2), -5, dtype=torch.int32, device="cuda")
+        ws = torch.empty(max(sga_lib.sga_lmhead_argmax_workspace(M, wd) for _, wd in shards),
+                         dtype=torch.uint8, device="cuda")
+        for s, (o, wd) in enumerate(shards):
+            sga_lib.sga_lmhead_argmax(h, w[o:o + wd], o, c["org_vocab"], per[s * M:(s + 1) * M], ws)
+        one = one_call(sga_lib, h, w, shards, c["org_vocab"])
+        gh.assert_stats_equal(one, gh.stats_to_numpy(per))
