@@ -32,6 +32,17 @@ static int host_checks(void) {
   if (sga_local_argmax_blocks((const void *)0x10000, SGA_BF16, 4, 100, 0, 100, 100, 0, 16, 0, 0,
                               (sga_stat *)0x10000, 0) != SGA_ERR_SIZE)
     bad |= 64;
+  /* the LM head over several shards in one call: the workspace size is host
+   * arithmetic, and overlapping shards are rejected before any CUDA call */
+  {
+    const int64_t starts[2] = {0, 40}, widths[2] = {64, 64};
+    const size_t ws = sga_lmhead_argmax_shards_workspace(16, 2, widths);
+    if (ws != 2u * 16u * 256u * 8u) bad |= 128;
+    if (sga_lmhead_argmax_shards((const void *)0x10000, 16, 64, (const void *)0x10000, 2, starts,
+                                 widths, 128, (sga_stat *)0x10000, (void *)0x10000, ws,
+                                 0) != SGA_ERR_SHARD)
+      bad |= 128;
+  }
   return bad;
 }
 
