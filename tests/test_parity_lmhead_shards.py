@@ -89,3 +89,27 @@ def test_fused_lmhead_decode_shape_every_shard_in_one_launch(sga_lib):
             sga_lib.sga_lmhead_argmax(h, w[o:o + wd], o, c["org_vocab"], per[s * M:(s + 1) * M], ws)
         one = one_call(sga_lib, h, w, shards, c["org_vocab"])
         gh.assert_stats_equal(one, gh.stats_to_numpy(per))
+
+
+@pytest.mark.parametrize("M", [1, 16, 64])
+@pytest.mark.parametrize("case", ["sixty_four_narrow", "padding_after_first", "tiny_widths"])
+def test_one_call_edge_layouts(sga_lib, M, case):
+    # the epilogue's per-shard flushes where most CTAs hold tiles of few or no
+    # shards: 64 narrow shards (the most one call takes), every shard but the
+    # first past org_vocab (no tiles at all), shards narrower than a tile
+    H = 128
+    if case == "sixty_four_narrow":
+        vocab, org = 64 * 300, 64 * 300 - 7
+        shards = wl.even_shards(vocab, 64)
+    elif case == "padding_after_first":
+        vocab, org = 4000, 900
+        shards = [(0, 1000), (1000, 1000), (2000, 1000), (3000, 1000)]
+    else:
+        vocab, org = 500, 500
+        shards = [(0, 3), (3, 1), (4, 100), (104, 5), (109, 391)]
+    hidden = wl.normal_matrix(M + 31, M, H, 1.0)
+    weight = wl.normal_matrix(M + 32, vocab, H, 1.0 / np.sqrt(H))
+    per, vals, ids = lm.run_gpu(hidden, weight, shards, org)
+    one = one_call(sga_lib, gh.to_device(hidden), gh.to_device(weight), shards, org)
+    gh.assert_stats_equal(one, per)
+    lm.check_rows(np.arange(0, M, 5), hidden, weight, shards, org, per, vals, ids)
