@@ -47,7 +47,7 @@ def configure(L):
         "oracle_full_argmax": ([vp, cint, i64, i64, i64, i64, vp, vp], None),
         "oracle_shard_argmax": ([vp, cint, i64, i64, i64, i64, i64, vp], None),
         "oracle_shard_reduce": ([vp, cint, i64, vp, vp], None),
-        "oracle_greedy_verify": ([vp, cint, cint, vp, vp, cint, vp, vp, vp, vp, vp], cint),
+        "oracle_greedy_verify": ([vp, cint, cint, vp, vp, cint, vp, vp, vp, vp, vp, vp], cint),
         "oracle_d2t_map": ([vp, i64, vp, i64, vp], cint),
         "oracle_lmhead_logits": ([vp, i64, vp, i64, vp, i64, vp], None),
         "oracle_argmax_f64": ([vp, i64, i64, i64, i64, vp, vp, vp], None),
@@ -191,10 +191,11 @@ def shard_reduce(stats, num_shards, rows):
     return vals, ids
 
 
-def greedy_verify(stats, num_shards, cu_num_draft, draft_tokens, max_k):
+def greedy_verify(stats, num_shards, cu_num_draft, draft_tokens, max_k, in_prefill=None):
     """Greedy verification from gathered stats.  Returns a dict with
     sampled [N, max_k+1], num_sampled [N], num_rejected [N], bonus [N],
-    target_ids [R_tot]."""
+    target_ids [R_tot].  in_prefill (optional, [N], nonzero = the request is
+    still in prefill) makes a request emit nothing."""
     stats = np.ascontiguousarray(stats, STAT)
     cu = np.ascontiguousarray(cu_num_draft, np.int32)
     drafts = np.ascontiguousarray(draft_tokens, np.int32)
@@ -212,9 +213,14 @@ def greedy_verify(stats, num_shards, cu_num_draft, draft_tokens, max_k):
     if n > 0:
         if drafts.size == 0:
             drafts = np.zeros(1, np.int32)
+        mask = None
+        if in_prefill is not None:
+            mask = np.ascontiguousarray(np.asarray(in_prefill) != 0, np.uint8)
+            if mask.shape != (n,):
+                raise ValueError("in_prefill must hold one flag per request")
         st = lib().oracle_greedy_verify(
             _ptr(stats), num_shards, n, _ptr(cu), _ptr(drafts), max_k,
-            _ptr(out["sampled"]), _ptr(out["num_sampled"]), _ptr(out["num_rejected"]),
+            None if mask is None else _ptr(mask), _ptr(out["sampled"]), _ptr(out["num_sampled"]), _ptr(out["num_rejected"]),
             _ptr(out["bonus"]), _ptr(out["target_ids"]))
         if st != 0:
             raise ValueError(f"oracle_greedy_verify status {st}")

@@ -164,13 +164,17 @@ void oracle_shard_reduce(const oracle_stat *stats, int num_shards, int64_t rows,
  * Outputs: out_sampled[i * (max_k + 1) + j] = target argmax of row b_i + j
  * for j <= a_i, else -1; num_sampled = a_i + 1; num_rejected = K_i - a_i;
  * bonus = target argmax of row b_i + a_i.  target_ids (nullable) gets the
- * per-row global argmax ids.  Returns 0; -1 if some K_i is outside
- * [0, max_k] (nothing is written for that request); -2 if out of memory. */
+ * per-row global argmax ids.  in_prefill (nullable) marks the requests
+ * still in prefill ([P4] Test Plan names "prefilling requests"; reading:
+ * such a request emits nothing this step): sampled all -1, num_sampled =
+ * num_rejected = 0, bonus = -1; its rows' target ids are still reported.
+ * Returns 0; -1 if some K_i is outside [0, max_k] (nothing is written for
+ * that request); -2 if out of memory. */
 int oracle_greedy_verify(const oracle_stat *stats, int num_shards, int num_reqs,
                          const int32_t *cu_num_draft, const int32_t *draft_tokens,
-                         int max_k, int32_t *out_sampled, int32_t *out_num_sampled,
-                         int32_t *out_num_rejected, int32_t *out_bonus,
-                         int32_t *out_target_ids) {
+                         int max_k, const uint8_t *in_prefill, int32_t *out_sampled,
+                         int32_t *out_num_sampled, int32_t *out_num_rejected,
+                         int32_t *out_bonus, int32_t *out_target_ids) {
   int status = 0;
   int64_t total_rows = (int64_t)cu_num_draft[num_reqs] + num_reqs;
   if (total_rows <= 0) return 0;
@@ -192,6 +196,13 @@ int oracle_greedy_verify(const oracle_stat *stats, int num_shards, int num_reqs,
     int64_t b = (int64_t)c + i;
     if (k < 0 || k > max_k) {
       status = -1;
+      continue;
+    }
+    if (in_prefill && in_prefill[i]) {
+      for (int j = 0; j <= max_k; ++j) out_sampled[(int64_t)i * (max_k + 1) + j] = -1;
+      out_num_sampled[i] = 0;
+      out_num_rejected[i] = 0;
+      out_bonus[i] = -1;
       continue;
     }
     int a = 0;

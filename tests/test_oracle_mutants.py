@@ -10,7 +10,8 @@ dropped, block boundaries taken from the shard start instead of global ids,
 the bonus row's block size ignored or given to the wrong row, an empty block
 slot naming the shard's first id, a block count off by one, the smaller of
 the two block counts as the slot count, a draft-to-target map that drops the
-draft id), builds it with gcc, points the oracle wrapper
+draft id, the prefill mask ignored, a request in prefill counting its drafts
+as rejected), builds it with gcc, points the oracle wrapper
 at it, and runs the pin tests of tests/test_oracle_pins.py: at least one pin
 must fail for every mutant.  The committed oracle source is never modified.
 """
@@ -59,6 +60,9 @@ MUTANTS = {
         "return (shard_start + shard_width) / block - shard_start / block + 1;"),
     "slots_take_the_smaller_count": ("n_draft > n_bonus ? n_draft : n_bonus",
                                      "n_draft < n_bonus ? n_draft : n_bonus"),
+    "prefill_mask_ignored": ("if (in_prefill && in_prefill[i]) {", "if (0 && in_prefill) {"),
+    "prefill_counts_drafts_rejected": ("      out_num_sampled[i] = 0;\n      out_num_rejected[i] = 0;",
+                                       "      out_num_sampled[i] = 0;\n      out_num_rejected[i] = k;"),
     "d2t_drops_the_draft_id": ("out_target_ids[r] = (int32_t)(k + d2t[k]);",
                                "out_target_ids[r] = (int32_t)(d2t[k]);"),
 }
@@ -74,6 +78,7 @@ PIN_CALLS = [
     pins.test_torch_argmax_third_opinion_unpadded,
     pins.test_tiny_workload_planted_rows,
     pins.test_verify_hand_cases,
+    pins.test_verify_prefill_hand_cases,
     pins.test_verify_random_variable_k_matches_brute_force,
     pins.test_verify_reduces_stats_across_shards_first,
     pins.test_lmhead_logits_match_numpy_fp64_matmul,

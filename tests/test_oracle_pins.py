@@ -209,6 +209,40 @@ def test_verify_hand_cases():
             assert (out["target_ids"] == t).all()
 
 
+def prefill_batch():
+    """The hand cases of verify_prefill_cases.txt as one batch: (cu, drafts,
+    t, max_k, in_prefill, expected per request)."""
+    table = read_table("verify_prefill_cases.txt")
+    ks = [int(r[1]) for r in table]
+    max_k = max(ks)
+    cu = np.concatenate([[0], np.cumsum(ks)]).astype(np.int32)
+    drafts = np.array([int(v) for r in table for v in r[2].split()], np.int32)
+    t = np.array([int(v) for r in table for v in r[3].split()], np.int32)
+    mask = np.array([int(r[0]) for r in table], np.uint8)
+    exp = []
+    for r in table:
+        samp = [int(v) for v in r[4].split()]
+        exp.append((samp + [-1] * (max_k + 1 - len(samp)), int(r[5]), int(r[6]), int(r[7])))
+    return cu, drafts, t, max_k, mask, exp
+
+
+def test_verify_prefill_hand_cases():
+    cu, drafts, t, max_k, mask, exp = prefill_batch()
+    assert len(t) == int(cu[-1]) + len(exp)
+    for num_shards in (1, 3):
+        st = stats_for_targets(t, num_shards)
+        out = oracle.greedy_verify(st, num_shards, cu, drafts, max_k, in_prefill=mask)
+        for i, (samp, ns, nr, b) in enumerate(exp):
+            assert list(out["sampled"][i]) == samp, i
+            assert (out["num_sampled"][i], out["num_rejected"][i], out["bonus"][i]) == (ns, nr, b), i
+        assert (out["target_ids"] == t).all()
+        # without the mask the same batch follows the greedy rule everywhere
+        plain = oracle.greedy_verify(st, num_shards, cu, drafts, max_k)
+        for i, (samp, ns, nr, b) in enumerate(brute_verify(t, cu, drafts, max_k)):
+            assert list(plain["sampled"][i]) == samp
+            assert (plain["num_sampled"][i], plain["num_rejected"][i], plain["bonus"][i]) == (ns, nr, b)
+
+
 def brute_verify(t, cu, drafts, max_k):
     """Prefix-length reading of greedy acceptance, written independently."""
     res = []
