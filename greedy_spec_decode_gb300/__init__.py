@@ -60,6 +60,8 @@ def lib():
                                                 i32, vp, vp, vp], i32),
             "sga_shard_reduce": ([vp, i32, i64, vp, vp, vp, i64, vp], i32),
             "sga_greedy_verify": ([vp, i32, i32, vp, vp, i32, vp, vp, vp, vp, vp, vp], i32),
+            "sga_greedy_verify_prefill": ([vp, i32, i32, vp, vp, vp, i32, vp, vp, vp, vp, vp,
+                                           vp], i32),
             "sga_lmhead_argmax_workspace": ([i64, i64], sz),
             "sga_lmhead_argmax_shards_workspace": ([i64, i32, vp], sz),
             "sga_lmhead_argmax_shards": ([vp, i64, i64, vp, i32, vp, vp, i64, vp, vp, sz, vp], i32),
@@ -229,6 +231,21 @@ def sga_greedy_verify(stats, num_shards, cu_num_draft, draft_tokens, max_k, out_
         _ptr(out_bonus), _ptr(out_target_ids), _stream(stream)))
 
 
+def sga_greedy_verify_prefill(stats, num_shards, cu_num_draft, draft_tokens, in_prefill, max_k,
+                              out_sampled, out_num_sampled, out_num_rejected, out_bonus,
+                              out_target_ids=None, stream=None):
+    """sga_greedy_verify where in_prefill (a uint8/bool CUDA tensor [num_reqs],
+    or None) marks the requests still in prefill, which emit nothing."""
+    num_reqs = cu_num_draft.numel() - 1
+    if in_prefill is not None and in_prefill.dtype not in (torch.uint8, torch.bool):
+        raise ValueError("in_prefill must be a uint8 or bool tensor")
+    _check("sga_greedy_verify_prefill", lib().sga_greedy_verify_prefill(
+        _ptr(stats), int(num_shards), int(num_reqs), _ptr(cu_num_draft),
+        _ptr(draft_tokens) if draft_tokens is not None and draft_tokens.numel() else None,
+        _ptr(in_prefill), int(max_k), _ptr(out_sampled), _ptr(out_num_sampled),
+        _ptr(out_num_rejected), _ptr(out_bonus), _ptr(out_target_ids), _stream(stream)))
+
+
 def sga_lmhead_argmax_workspace(M, shard_width):
     return int(lib().sga_lmhead_argmax_workspace(int(M), int(shard_width)))
 
@@ -350,7 +367,8 @@ def sga_lmhead_argmax_noalloc(hidden, weight_shard, shard_start, org_vocab, out_
     pre-sized memory pool, or a loop where cudaMalloc would synchronise the
     device).  Partial statistics go to a fixed 4 MiB scratch array inside the
     library, shared by every call on the device: calls that overlap on the
-    GPU race.  Rejects M * ceil(width / 256) * 8 > 4 MiB with SGA_ERR_WORKSPACE.
+    GPU race.  Rejects sga_lmhead_argmax_workspace(M, width) > 4 MiB with
+    SGA_ERR_WORKSPACE.
     The first call on a device resolves the scratch address for that device;
     make it before any stream capture."""
     fn = lib().sga_lmhead_argmax_noalloc

@@ -9,6 +9,14 @@
 
 namespace sga {
 
+// Key of the CUDA context current on the calling thread (0 while none is
+// current).  What the library caches per device -- symbol addresses, function
+// attributes -- belongs to one context; an entry whose key differs from the
+// current one is looked up again, so a device reset (which destroys the
+// context and reloads the module) or a different context never meets a
+// stale address.
+uintptr_t current_context_key();
+
 // ---------------------------------------------------------------------------
 // Launchers (host).  Arguments are already validated by sga_abi.cu.
 // ---------------------------------------------------------------------------
@@ -53,7 +61,8 @@ cudaError_t launch_greedy_verify(const sga_stat *stats, int num_shards, int num_
                                  const int32_t *cu_num_draft, const int32_t *draft_tokens,
                                  int max_k, int32_t *out_sampled, int32_t *out_num_sampled,
                                  int32_t *out_num_rejected, int32_t *out_bonus,
-                                 int32_t *out_target_ids, uint32_t *err, cudaStream_t stream);
+                                 int32_t *out_target_ids, uint32_t *err, cudaStream_t stream,
+                                 const uint8_t *in_prefill = nullptr);
 
 size_t lmhead_workspace_bytes(int64_t M, int64_t width);
 // fp8 = false: bf16 hidden/weight (row_scale, w_scale unused).  fp8 = true:

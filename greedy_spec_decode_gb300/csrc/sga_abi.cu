@@ -2,6 +2,8 @@
 // validation (before any CUDA call, so a bad call enqueues nothing), the
 // per-device cache (SM count, compute capability, address of the device error
 // word) and dispatch to the kernel launchers.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -13,7 +15,8 @@ namespace {
 
 struct DeviceInfo {
   bool ready;
-  int status;  // SGA_OK or the error the set-up hit
+  uintptr_t ctx;  // context the entry was looked up in
+  int status;     // SGA_OK or the error the set-up hit
   int num_sms;
   uint32_t *err;
 };
@@ -22,14 +25,15 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 DeviceInfo g_devices[kMaxDevices];
 
-// Per-device facts for the current device, looked up once.
+// Per-device facts for the current device, looked up once per context.
 int current_device(DeviceInfo *out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SGA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return SGA_ERR_DEVICE;
+  const uintptr_t ctx = sga::current_context_key();
   std::lock_guard<std::mutex> lock(g_mutex);
   DeviceInfo &d = g_devices[dev];
-  if (!d.ready) {
+  if (!d.ready || ctx == 0 || ctx != d.ctx) {
     int major = 0, minor = 0, sms = 0;
     d.status = SGA_OK;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -44,11 +48,38 @@ int current_device(DeviceInfo *out) {
       d.err = static_cast<uint32_t *>(p);
       d.num_sms = sms;
     }
+    d.ctx = sga::current_context_key();  // the look-up above made a context current
     d.ready = true;
   }
   *out = d;
   return d.status;
 }
+
+}  // namespace
+
+namespace sga {
+
+uintptr_t current_context_key() {
+  using GetCurrent = CUresult (*)(CUcontext *);
+  static GetCurrent fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<GetCurrent>(p);
+  });
+  if (fn == nullptr) return 1;  // no driver entry point: one context per device assumed
+  CUcontext c = nullptr;
+  if (fn(&c) != CUDA_SUCCESS) return 0;
+  return reinterpret_cast<uintptr_t>(c);
+}
+
+}  // namespace sga
+
+namespace {
 
 bool misaligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) != 0; }
 
@@ -242,6 +273,16 @@ int sga_greedy_verify(const sga_stat *stats, int num_shards, int num_reqs,
                       int32_t *out_sampled, int32_t *out_num_sampled,
                       int32_t *out_num_rejected, int32_t *out_bonus,
                       int32_t *out_target_ids, sga_stream stream) {
+  return sga_greedy_verify_prefill(stats, num_shards, num_reqs, cu_num_draft, draft_tokens,
+                                   nullptr, max_k, out_sampled, out_num_sampled,
+                                   out_num_rejected, out_bonus, out_target_ids, stream);
+}
+
+int sga_greedy_verify_prefill(const sga_stat *stats, int num_shards, int num_reqs,
+                              const int32_t *cu_num_draft, const int32_t *draft_tokens,
+                              const uint8_t *in_prefill, int max_k, int32_t *out_sampled,
+                              int32_t *out_num_sampled, int32_t *out_num_rejected,
+                              int32_t *out_bonus, int32_t *out_target_ids, sga_stream stream) {
   if (num_shards < 1 || num_shards > 4096) return SGA_ERR_SIZE;
   if (num_reqs < 0 || num_reqs > (1 << 26)) return SGA_ERR_SIZE;
   if (max_k < 1 || max_k > SGA_MAX_K) return SGA_ERR_MAXK;
@@ -260,7 +301,7 @@ int sga_greedy_verify(const sga_stat *stats, int num_shards, int num_reqs,
   return launch_status(sga::launch_greedy_verify(
       stats, num_shards, num_reqs, cu_num_draft, draft_tokens, max_k, out_sampled,
       out_num_sampled, out_num_rejected, out_bonus, out_target_ids, d.err,
-      static_cast<cudaStream_t>(stream)));
+      static_cast<cudaStream_t>(stream), in_prefill));
 }
 
 size_t sga_lmhead_argmax_workspace(int64_t M, int64_t shard_width) {

@@ -6,7 +6,9 @@
 // do not define them): a draft is accepted while it equals the target argmax
 // of its own row; with a accepted drafts the request emits the target
 // argmaxes of rows 0..a, num_sampled = a + 1, num_rejected = K - a, and the
-// bonus token is the last emitted one.
+// bonus token is the last emitted one.  A request flagged as still in prefill
+// (Test Plan: "prefilling requests") emits nothing: sampled all -1, both
+// counts 0, bonus -1; its rows' target ids are still reported.
 //
 // Layout: 16 lanes per request (K <= 15, so K + 1 <= 16 rows), two requests
 // per warp.  Lane j reduces row j of its request over the gathered statistics
@@ -30,7 +32,8 @@ constexpr int kWideEntries = SGA_VERIFY_WIDE_ENTRIES;
 __global__ void __launch_bounds__(kThreads)
     greedy_verify_kernel(const sga_stat *__restrict__ stats, int num_shards, int num_reqs,
                          const int32_t *__restrict__ cu_num_draft,
-                         const int32_t *__restrict__ draft_tokens, int max_k,
+                         const int32_t *__restrict__ draft_tokens,
+                         const uint8_t *__restrict__ in_prefill, int max_k,
                          int32_t *__restrict__ out_sampled, int32_t *__restrict__ out_num_sampled,
                          int32_t *__restrict__ out_num_rejected, int32_t *__restrict__ out_bonus,
                          int32_t *__restrict__ out_target_ids, uint32_t *err) {
@@ -43,9 +46,11 @@ __global__ void __launch_bounds__(kThreads)
   const int64_t total_rows = static_cast<int64_t>(cu_num_draft[num_reqs]) + num_reqs;
 
   int32_t c = 0, k = 0;
+  bool prefill = false;
   if (live) {
     c = cu_num_draft[req];
     k = cu_num_draft[req + 1] - c;
+    prefill = in_prefill != nullptr && in_prefill[req] != 0;
   }
   const bool bad = live && (k < 0 || k > max_k);
   const bool has_row = live && !bad && j <= k;
@@ -76,6 +81,16 @@ __global__ void __launch_bounds__(kThreads)
     }
     return;
   }
+  if (prefill) {
+    // a request still in prefill emits nothing this step
+    if (j <= max_k) sampled_row[j] = -1;
+    if (j == 0) {
+      out_num_sampled[req] = 0;
+      out_num_rejected[req] = 0;
+      out_bonus[req] = -1;
+    }
+    return;
+  }
   if (j <= max_k) sampled_row[j] = j <= a ? t : -1;
   if (j == a) out_bonus[req] = t;
   if (j == 0) {
@@ -99,7 +114,8 @@ constexpr int kStreams = kWideThreads / 16;
 __global__ void __launch_bounds__(kWideThreads)
     greedy_verify_wide_kernel(const sga_stat *__restrict__ stats, int num_entries, int num_reqs,
                               const int32_t *__restrict__ cu_num_draft,
-                              const int32_t *__restrict__ draft_tokens, int max_k,
+                              const int32_t *__restrict__ draft_tokens,
+                              const uint8_t *__restrict__ in_prefill, int max_k,
                               int32_t *__restrict__ out_sampled,
                               int32_t *__restrict__ out_num_sampled,
                               int32_t *__restrict__ out_num_rejected,
@@ -123,6 +139,7 @@ __global__ void __launch_bounds__(kWideThreads)
 
   // lanes 0..15 load their draft now so that it overlaps the statistics
   const int32_t draft = threadIdx.x < 16 && !bad && j < k ? draft_tokens[c + j] : 0;
+  const bool prefill = threadIdx.x < 16 && in_prefill != nullptr && in_prefill[req] != 0;
   float bv = __int_as_float(0xff800000);
   int32_t bpos = kNoId, bid = 0;
   if (has_row) {
@@ -174,6 +191,16 @@ __global__ void __launch_bounds__(kWideThreads)
     }
     return;
   }
+  if (prefill) {
+    // a request still in prefill emits nothing this step
+    if (lane <= max_k) sampled_row[lane] = -1;
+    if (lane == 0) {
+      out_num_sampled[req] = 0;
+      out_num_rejected[req] = 0;
+      out_bonus[req] = -1;
+    }
+    return;
+  }
   const int32_t t = lane <= k ? t_row[lane] : -1;
   const bool mismatch = lane < k && draft != t;
   const uint32_t mine = __ballot_sync(0x0000ffffu, mismatch);
@@ -192,7 +219,8 @@ cudaError_t launch_greedy_verify(const sga_stat *stats, int num_shards, int num_
                                  const int32_t *cu_num_draft, const int32_t *draft_tokens,
                                  int max_k, int32_t *out_sampled, int32_t *out_num_sampled,
                                  int32_t *out_num_rejected, int32_t *out_bonus,
-                                 int32_t *out_target_ids, uint32_t *err, cudaStream_t stream) {
+                                 int32_t *out_target_ids, uint32_t *err, cudaStream_t stream,
+                                 const uint8_t *in_prefill) {
   cudaLaunchConfig_t cfg = {};
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -204,15 +232,15 @@ cudaError_t launch_greedy_verify(const sga_stat *stats, int num_shards, int num_
     cfg.gridDim = dim3(static_cast<unsigned>(num_reqs));
     cfg.blockDim = dim3(kWideThreads);
     return cudaLaunchKernelEx(&cfg, greedy_verify_wide_kernel, stats, num_shards, num_reqs,
-                              cu_num_draft, draft_tokens, max_k, out_sampled, out_num_sampled,
-                              out_num_rejected, out_bonus, out_target_ids, err);
+                              cu_num_draft, draft_tokens, in_prefill, max_k, out_sampled,
+                              out_num_sampled, out_num_rejected, out_bonus, out_target_ids, err);
   }
   const int64_t threads_needed = static_cast<int64_t>(num_reqs) * 16;
   cfg.gridDim = dim3(static_cast<unsigned>((threads_needed + kThreads - 1) / kThreads));
   cfg.blockDim = dim3(kThreads);
   return cudaLaunchKernelEx(&cfg, greedy_verify_kernel, stats, num_shards, num_reqs, cu_num_draft,
-                            draft_tokens, max_k, out_sampled, out_num_sampled, out_num_rejected,
-                            out_bonus, out_target_ids, err);
+                            draft_tokens, in_prefill, max_k, out_sampled, out_num_sampled,
+                            out_num_rejected, out_bonus, out_target_ids, err);
 }
 
 }  // namespace sga

@@ -284,6 +284,28 @@ int sga_greedy_verify(const sga_stat *stats, int num_shards, int num_reqs,
                       int32_t *out_target_ids, sga_stream stream);
 
 /*
+ * sga_greedy_verify_prefill -- sga_greedy_verify for a batch that mixes
+ * decoding requests with requests still in prefill.
+ * Page: vLLM PR #62604, Test Plan (the sharded verifier handles "prefilling
+ * requests").  The pages do not say what such a request yields; this library
+ * reads it as: a request still in prefill emits nothing this step.
+ *
+ *   in_prefill     device uint8 [num_reqs] or NULL (NULL = sga_greedy_verify):
+ *                  nonzero marks request i as still in prefill.  Such a
+ *                  request gets out_sampled row all -1, out_num_sampled =
+ *                  out_num_rejected = 0 and out_bonus = -1; the target
+ *                  argmaxes of its rows still go to out_target_ids.  Its
+ *                  K_i must still lie in [0, max_k] (else the K_i error
+ *                  result of sga_greedy_verify applies).
+ * Other arguments, results and errors as sga_greedy_verify.
+ */
+int sga_greedy_verify_prefill(const sga_stat *stats, int num_shards, int num_reqs,
+                              const int32_t *cu_num_draft, const int32_t *draft_tokens,
+                              const uint8_t *in_prefill, int max_k, int32_t *out_sampled,
+                              int32_t *out_num_sampled, int32_t *out_num_rejected,
+                              int32_t *out_bonus, int32_t *out_target_ids, sga_stream stream);
+
+/*
  * sga_lmhead_argmax -- fused LM-head GEMM + per-shard argmax: the shard's
  * logits hidden . weight_shard^T are computed on the tensor cores (tcgen05,
  * fp32 accumulation in tensor memory) and reduced to per-row statistics in
@@ -401,12 +423,17 @@ int sga_lmhead_argmax_shards_fp8(const void *hidden_q, const float *hidden_scale
  * routine.
  *
  *   Arguments and results: as sga_lmhead_argmax, without workspace.
- *   Limit: M * ceil(shard_width / 256) * 8 bytes must not exceed
- *          SGA_LMHEAD_NOALLOC_SCRATCH_BYTES; larger calls return
+ *   Limit: sga_lmhead_argmax_workspace(M, shard_width) must not exceed
+ *          SGA_LMHEAD_NOALLOC_SCRATCH_BYTES (M * ceil(shard_width / 256) * 8
+ *          bytes; for M <= 64 the count per row is at least
+ *          min(ceil(shard_width / 128), 256)); larger calls return
  *          SGA_ERR_WORKSPACE and enqueue nothing.
  *   Set-up: the first call on a device looks up the device address of the
  *          scratch array for that device (with that device current), so make
- *          the first call on each device before any stream capture.
+ *          the first call on each device before any stream capture.  The
+ *          address is looked up again when the device's current context has
+ *          changed (after cudaDeviceReset, for instance); make the first call
+ *          after such a change outside any stream capture as well.
  *   Sharing: every call on a device uses the same scratch array, which keeps
  *          the last call's contents; each call writes every scratch entry it
  *          reads, so nothing has to start at zero.  Calls whose kernels

@@ -140,3 +140,60 @@ def test_shard_reduce_d2t_out_of_range_sets_error_word(sga_lib, num_shards):
     assert (ids == eids).all()   # a zero table maps every id to itself
     sga_lib.sga_clear_device_error()
     assert sga_lib.sga_device_error() == 0
+
+
+def gpu_verify_prefill(stats_dev, num_shards, cu, drafts, max_k, mask):
+    import greedy_spec_decode_gb300 as sga
+    n = len(cu) - 1
+    total = int(cu[-1]) + n
+    i32 = dict(dtype=torch.int32, device="cuda")
+    out = dict(sampled=torch.full((n, max_k + 1), -99, **i32),
+               num_sampled=torch.full((n,), -99, **i32), num_rejected=torch.full((n,), -99, **i32),
+               bonus=torch.full((n,), -99, **i32), target_ids=torch.full((total,), -99, **i32))
+    sga.sga_greedy_verify_prefill(
+        stats_dev, num_shards, torch.from_numpy(np.asarray(cu, np.int32)).cuda(),
+        torch.from_numpy(np.asarray(drafts, np.int32)).cuda(),
+        torch.from_numpy(np.asarray(mask, np.uint8)).cuda(), max_k, out["sampled"],
+        out["num_sampled"], out["num_rejected"], out["bonus"], out["target_ids"])
+    return {k: v.cpu().numpy() for k, v in out.items()}
+
+
+@pytest.mark.parametrize("num_shards", [1, 3, 40])
+def test_prefill_hand_cases(sga_lib, num_shards):
+    # the hand-computed batch of tests/golden/verify_prefill_cases.txt; 40
+    # entries per row runs the wide kernel
+    import test_oracle_pins as pins
+    cu, drafts, t, max_k, mask, exp = pins.prefill_batch()
+    st = pins.stats_for_targets(t, num_shards)
+    got = gpu_verify_prefill(torch.from_numpy(st.view(np.int32).reshape(-1, 2).copy()).cuda(),
+                             num_shards, cu, drafts, max_k, mask)
+    for i, (samp, ns, nr, b) in enumerate(exp):
+        assert list(got["sampled"][i]) == samp, i
+        assert (got["num_sampled"][i], got["num_rejected"][i], got["bonus"][i]) == (ns, nr, b), i
+    assert (got["target_ids"] == t).all()
+    assert sga_lib.sga_device_error() == 0
+
+
+@pytest.mark.parametrize("num_shards,n_reqs", [(2, 1), (3, 37), (8, 256), (24, 33), (200, 9)])
+def test_prefill_mask_random_matches_oracle(sga_lib, num_shards, n_reqs):
+    rng = np.random.default_rng(num_shards * 1000 + n_reqs)
+    max_k = int(rng.integers(1, 16))
+    ks = rng.integers(0, max_k + 1, n_reqs)
+    cu = np.concatenate([[0], np.cumsum(ks)]).astype(np.int32)
+    rows = int(cu[-1]) + n_reqs
+    st, x, shards = random_stats(rng, rows, num_shards, max(4 * num_shards, 300))
+    _, t = oracle.full_argmax(x, x.shape[1])
+    flags = rng.random(int(cu[-1])) < 0.7
+    drafts = wl.compose_drafts(t, cu, flags, rng.integers(-1, x.shape[1], int(cu[-1])).astype(np.int32))
+    mask = (rng.random(n_reqs) < 0.3).astype(np.uint8)
+    dev = torch.from_numpy(st.view(np.int32).reshape(-1, 2).copy()).cuda()
+    got = gpu_verify_prefill(dev, num_shards, cu, drafts, max_k, mask)
+    exp = oracle.greedy_verify(st, num_shards, cu, drafts, max_k, in_prefill=mask)
+    for key in ("sampled", "num_sampled", "num_rejected", "bonus", "target_ids"):
+        assert (got[key] == exp[key]).all(), key
+    # an all-zero mask is the plain entry point's result
+    none = gpu_verify_prefill(dev, num_shards, cu, drafts, max_k, np.zeros(n_reqs, np.uint8))
+    plain = gh.gpu_verify(dev, num_shards, cu, drafts, max_k)
+    for key in plain:
+        assert (none[key] == plain[key]).all(), key
+    assert sga_lib.sga_device_error() == 0
