@@ -865,13 +865,16 @@ cudaError_t launch_lmhead_argmax_shards(const void *hidden, int64_t M, int64_t H
 // in this fixed array instead of a caller-provided workspace.  Host code must
 // not use the array's name as a device pointer (on the host it only stands in
 // for the symbol); lmhead_noalloc_scratch() looks up its device address once
-// per device, with that device current.
+// per device, with that device current, and again if the device's context
+// has changed since (a device reset reloads the module, and the array may
+// move).
 // ---------------------------------------------------------------------------
 namespace {
 constexpr size_t kNoallocScratchBytes = SGA_LMHEAD_NOALLOC_SCRATCH_BYTES;
 constexpr int kNoallocMaxDevices = 64;
 std::mutex g_noalloc_mutex;
 sga_stat *g_noalloc_ptr[kNoallocMaxDevices];
+uintptr_t g_noalloc_ctx[kNoallocMaxDevices];
 }  // namespace
 
 static __device__ __align__(256) sga_stat g_lmhead_noalloc_scratch[kNoallocScratchBytes / sizeof(sga_stat)];
@@ -885,12 +888,14 @@ cudaError_t lmhead_noalloc_scratch(sga_stat **out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kNoallocMaxDevices) return cudaErrorInvalidDevice;
+  const uintptr_t ctx = current_context_key();
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (g_noalloc_ptr[dev] == nullptr) {
+  if (g_noalloc_ptr[dev] == nullptr || ctx == 0 || ctx != g_noalloc_ctx[dev]) {
     void *p = nullptr;
     e = cudaGetSymbolAddress(&p, g_lmhead_noalloc_scratch);
     if (e != cudaSuccess) return e;
     g_noalloc_ptr[dev] = static_cast<sga_stat *>(p);
+    g_noalloc_ctx[dev] = current_context_key();
   }
   *out = g_noalloc_ptr[dev];
   return cudaSuccess;

@@ -189,21 +189,22 @@ bool make_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, int
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Raise a kernel's dynamic shared-memory limit once per device (slot picks the
-// kernel), so that later calls, including calls inside a stream capture, make
-// no function-attribute call.
+// Raise a kernel's dynamic shared-memory limit once per device and context
+// (slot picks the kernel), so that later calls, including calls inside a
+// stream capture, make no function-attribute call.
 cudaError_t set_smem_once(const void *kernel, int bytes, int slot) {
   static std::mutex mu;
-  static bool done[12][64] = {};
+  static uintptr_t done_ctx[12][64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const uintptr_t ctx = current_context_key();
   std::lock_guard<std::mutex> lock(mu);
-  if (!done[slot][dev]) {
+  if (ctx == 0 || done_ctx[slot][dev] != ctx) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
-    done[slot][dev] = true;
+    done_ctx[slot][dev] = current_context_key();
   }
   return cudaSuccess;
 }
