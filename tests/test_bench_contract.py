@@ -30,7 +30,7 @@ def check_common(d, unit):
                 "roofline", "e2e", "gpu_launches", "clocks"):
         assert key in d, key
     assert d["unit"] == unit and d["value"] > 0 and d["n_gpus"] == 1
-    assert d["higher_is_better"] is True and d["scaling"] == "weak"
+    assert d["higher_is_better"] is True and d["scaling"] in ("weak", "strong")
     assert "workload" in d["config"]
     r = d["roofline"]
     assert r["bound"] in ("hbm", "tensor") and r["achieved"] > 0 and r["peak"] > 0
@@ -41,13 +41,32 @@ def check_common(d, unit):
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
 
 
-def test_large_verify_line_with_oracle_leg():
+def test_large_verify_line_with_oracle_leg_and_nested_records():
     d = run_bench("--rows", "512", "--steps", "16", "--warmup", "3", "--e2e-steps", "1",
                   "--cpu-seconds", "1")
     check_common(d, "rows/s")
     assert d["roofline"]["unit"] == "GB/s"
+    assert d["kernel_us"]["local_argmax_all_shards"]["launches"] >= 20
+    k = d["kernel_us"]["local_argmax_all_shards"]
+    assert k["min_us"] <= k["median_us"] <= k["max_us"]
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["cpu_baseline"]["single_thread"]["cores"] == 1
+    assert "bit-exact" in d["parity"]
+    # the other configurations ride along as nested records
+    lm = d["lmhead"]
+    check_common(lm, "rows/s")
+    assert lm["roofline"]["bound"] == "tensor" and lm["roofline"]["unit"] == "TFLOP/s"
+    assert lm["config"]["M"] == 512 and lm["config"]["shards"] == [75968, 75968]
+    assert lm["cpu_baseline"]["kind"] == "oracle" and "tolerance" in lm["parity"]
+    for key in ("draft_top_tokens", "greedy_verify_small"):
+        check_common(d[key], "rows/s")
+        assert "bit-exact" in d[key]["parity"]
+
+
+def test_tensor_parallel_line_one_rank():
+    d = run_bench("--tp", "--rows", "512", "--steps", "16", "--warmup", "3", "--e2e-steps", "1")
+    check_common(d, "rows/s")
+    assert d["scaling"] == "strong" and d["exchange"]["bytes_per_rank"] == 512 * 8
     assert "bit-exact" in d["parity"]
 
 
