@@ -37,9 +37,6 @@ constexpr int BM = 128;          // rows of hidden per tile (TMEM lanes)
 #ifndef SGA_LMHEAD_STAGES
 #define SGA_LMHEAD_STAGES 4
 #endif
-#ifndef SGA_LMHEAD_2SM
-#define SGA_LMHEAD_2SM 1  // 2-SM tiles when M >= SGA_LMHEAD_2SM_MIN_M
-#endif
 #ifndef SGA_LMHEAD_2SM_MIN_M
 #define SGA_LMHEAD_2SM_MIN_M 129
 #endif
@@ -385,11 +382,73 @@ __device__ __forceinline__ void raise_abort2(Shared2 *sh, uint32_t *err) {
   atomicOr(err, SGA_DEVERR_TIMEOUT);
 }
 
+// The shards of one GEMM launch (one, or every shard a GPU holds): shard s
+// covers global ids [start, start + valid) (its non-padding ids) at rows
+// row0 .. row0 + valid - 1 of the launch's weight map, and its 256-id tiles
+// are numbers tile0[s] .. tile0[s + 1] - 1 of the launch (a shard without
+// valid ids has none).
+// Partial slots per (shard, row) of the 2-SM kernel, at most: the chunks a
+// launch cuts its tiles into (one per CTA pair of a row block).
+constexpr int kMaxChunks = 128;
+
+struct GemmShardTable {
+  int n;
+  int32_t start[kMaxLmShards];
+  int32_t row0[kMaxLmShards];
+  int32_t valid[kMaxLmShards];
+  int32_t tile0[kMaxLmShards + 1];
+};
+
+// First tile of chunk c when T tiles are cut into C contiguous chunks, and
+// the chunk that holds tile t (the inverse); C <= T, so no chunk is empty.
+__host__ __device__ __forceinline__ int chunk_first_tile(int c, int T, int C) {
+  return static_cast<int>(static_cast<int64_t>(c) * T / C);
+}
+__host__ __device__ __forceinline__ int chunk_of_tile(int t, int T, int C) {
+  return static_cast<int>((static_cast<int64_t>(t + 1) * C - 1) / T);
+}
+
+// Scan of 32 accumulator columns (ids id0 .. id0 + 31, all valid) in id
+// order with the scan rule.  A NaN-propagating max of the 32 values goes
+// first: when it cannot beat `best` (the common case once a tile is under
+// way) no element can, and the ordered scan is skipped.
+__device__ __forceinline__ void scan32(const uint32_t (&r)[32], int32_t id0, float &best,
+                                       int32_t &best_id) {
+  float m[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m[i] = max_nan(__uint_as_float(r[i]), __uint_as_float(r[i + 16]));
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1) {
+#pragma unroll
+    for (int i = 0; i < w; ++i) m[i] = max_nan(m[i], m[i + w]);
+  }
+  if (scan_better(m[0], best)) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float x = __uint_as_float(r[i]);
+      if (scan_better(x, best)) {
+        best = x;
+        best_id = id0 + i;
+      }
+    }
+  }
+}
+
+// Work: the launch's T tiles (all shards, in id order) are cut into C
+// contiguous chunks; a unit is (chunk c, 256-row block mp), numbered u = c *
+// m_pairs + mp so that the pairs of one chunk, which stream the same weight
+// tiles, run side by side and share them through L2.  Pair p takes units
+// p, p + pairs, ...  Each epilogue thread keeps one hidden row's running
+// (max, id) over all tiles of its unit and writes one partial per (shard,
+// row, chunk) -- at the unit's end and at each shard edge inside it -- to
+// ws[(s * M + row) * C + c]; the finalize kernel merges the chunks that meet
+// shard s.
 template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     lmhead_argmax_2sm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                              const __grid_constant__ CUtensorMap tmap_b, int M, int num_kb,
-                             int m_pairs, int n_tiles, int valid, int shard_start,
+                             int m_pairs, int num_chunks,
+                             const __grid_constant__ GemmShardTable tab,
                              sga_stat *__restrict__ ws, uint32_t *err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>(
@@ -435,7 +494,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   // set-up, TMEM allocation) overlaps the previous kernel's tail; inputs and
   // the workspace are touched only after that kernel has completed
   pdl_wait();
-  const int total = m_pairs * n_tiles;
+  const int T = tab.tile0[tab.n];
+  const int total = m_pairs * num_chunks;
 
   int prod_stage = 0;
   uint32_t prod_phase = 0;
@@ -443,23 +503,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
   if (warp == 0 && lane == 0) {
     // -------------------------------------------------------------- producer
-    for (int item = pair; item < total && !*abort_flag; item += num_pairs) {
-      const int n = item / m_pairs, mp = item % m_pairs;
-      for (int kb = 0; kb < num_kb; ++kb) {
-        if (!mbar_wait(smem_u32(&sh->empty[prod_stage]), prod_phase ^ 1, abort_flag)) {
-          raise_abort2(sh, err);
-          break;
-        }
-        const uint32_t full_leader = map_to_rank(smem_u32(&sh->full[prod_stage]), 0);
-        if (leader) mbar_expect_tx(smem_u32(&sh->full[prod_stage]), 2 * STAGE2_BYTES);
-        tma_load_2d_pair(smem_u32(a_tiles + prod_stage * A2_BYTES), &tmap_a, kb * kBk<kFp8>,
-                         mp * 256 + static_cast<int>(rank) * 128, full_leader);
-        tma_load_2d_pair(smem_u32(b_tiles + prod_stage * B2_BYTES), &tmap_b, kb * kBk<kFp8>,
-                         n * 256 + static_cast<int>(rank) * 128, full_leader);
-        ++issued;
-        if (++prod_stage == STAGES2) {
-          prod_stage = 0;
-          prod_phase ^= 1;
+    for (int u = pair; u < total && !*abort_flag; u += num_pairs) {
+      const int c = u / m_pairs, mp = u % m_pairs;
+      const int t1 = chunk_first_tile(c + 1, T, num_chunks);
+      int s = 0;
+      for (int t = chunk_first_tile(c, T, num_chunks); t < t1 && !*abort_flag; ++t) {
+        while (t >= tab.tile0[s + 1]) ++s;
+        const int wrow = tab.row0[s] + (t - tab.tile0[s]) * BN + static_cast<int>(rank) * 128;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(smem_u32(&sh->empty[prod_stage]), prod_phase ^ 1, abort_flag)) {
+            raise_abort2(sh, err);
+            break;
+          }
+          const uint32_t full_leader = map_to_rank(smem_u32(&sh->full[prod_stage]), 0);
+          if (leader) mbar_expect_tx(smem_u32(&sh->full[prod_stage]), 2 * STAGE2_BYTES);
+          tma_load_2d_pair(smem_u32(a_tiles + prod_stage * A2_BYTES), &tmap_a, kb * kBk<kFp8>,
+                           mp * 256 + static_cast<int>(rank) * 128, full_leader);
+          tma_load_2d_pair(smem_u32(b_tiles + prod_stage * B2_BYTES), &tmap_b, kb * kBk<kFp8>,
+                           wrow, full_leader);
+          ++issued;
+          if (++prod_stage == STAGES2) {
+            prod_stage = 0;
+            prod_phase ^= 1;
+          }
         }
       }
     }
@@ -467,36 +533,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     // -------------------------------------------------- MMA issuer (leader)
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
-    for (int item = pair; item < total && !*abort_flag; item += num_pairs) {
-      if (!mbar_wait(smem_u32(&sh->tmem_empty[acc]), acc_phase ^ 1, abort_flag)) {
-        raise_abort2(sh, err);
-        break;
-      }
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + acc * BN;
-      bool ok = true;
-      for (int kb = 0; kb < num_kb; ++kb) {
-        if (!mbar_wait(smem_u32(&sh->full[stage]), phase, abort_flag)) {
+    bool ok = true;
+    for (int u = pair; u < total && ok && !*abort_flag; u += num_pairs) {
+      const int c = u / m_pairs;
+      const int tiles = chunk_first_tile(c + 1, T, num_chunks) - chunk_first_tile(c, T, num_chunks);
+      for (int t = 0; t < tiles && ok; ++t) {
+        if (!mbar_wait(smem_u32(&sh->tmem_empty[acc]), acc_phase ^ 1, abort_flag)) {
           raise_abort2(sh, err);
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint64_t a_desc = smem_desc_sw128(smem_u32(a_tiles + stage * A2_BYTES));
-        const uint64_t b_desc = smem_desc_sw128(smem_u32(b_tiles + stage * B2_BYTES));
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(smem_u32(&sh->full[stage]), phase, abort_flag)) {
+            raise_abort2(sh, err);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t a_desc = smem_desc_sw128(smem_u32(a_tiles + stage * A2_BYTES));
+          const uint64_t b_desc = smem_desc_sw128(smem_u32(b_tiles + stage * B2_BYTES));
 #pragma unroll
-        for (int kk = 0; kk < ROW_BYTES / 32; ++kk)
-          mma_pair<kFp8>(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, (kb | kk) != 0);
-        mma_commit_pair(smem_u32(&sh->empty[stage]));
-        if (++stage == STAGES2) {
-          stage = 0;
-          phase ^= 1;
+          for (int kk = 0; kk < ROW_BYTES / 32; ++kk)
+            mma_pair<kFp8>(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, (kb | kk) != 0);
+          mma_commit_pair(smem_u32(&sh->empty[stage]));
+          if (++stage == STAGES2) {
+            stage = 0;
+            phase ^= 1;
+          }
         }
+        if (!ok) break;
+        mma_commit_pair(smem_u32(&sh->tmem_full[acc]));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
       }
-      if (!ok) break;
-      mma_commit_pair(smem_u32(&sh->tmem_full[acc]));
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1;
     }
   } else if (warp >= 2) {
     // -------------------------------------------------- epilogue (both CTAs)
@@ -506,53 +577,67 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                                       map_to_rank(smem_u32(&sh->tmem_empty[1]), 0)};
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int item = pair; item < total; item += num_pairs) {
-      const int n = item / m_pairs, mp = item % m_pairs;
-      bool ok = mbar_wait(smem_u32(&sh->tmem_full[acc]), acc_phase, abort_flag);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) {
-        if (lane == 0) raise_abort2(sh, err);
-        break;
-      }
-      tc_fence_after();
+    bool ok = true;
+    for (int u = pair; u < total && ok; u += num_pairs) {
+      const int c = u / m_pairs, mp = u % m_pairs;
+      const int row = mp * 256 + row_in_tile;
+      const int t0 = chunk_first_tile(c, T, num_chunks);
+      const int t1 = chunk_first_tile(c + 1, T, num_chunks);
+      int s = 0;
+      while (t0 >= tab.tile0[s + 1]) ++s;
       float best = __int_as_float(0xff800000);
       int32_t best_id = kNoId;
-      const int col0 = n * BN;
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+      for (int t = t0; t < t1; ++t) {
+        if (t >= tab.tile0[s + 1]) {
+          // shard edge inside the unit: flush the finished shard's partial
+          if (row < M) ws[(static_cast<size_t>(s) * M + row) * num_chunks + c] = {best, best_id};
+          best = __int_as_float(0xff800000);
+          best_id = kNoId;
+          while (t >= tab.tile0[s + 1]) ++s;
+        }
+        ok = mbar_wait(smem_u32(&sh->tmem_full[acc]), acc_phase, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+          if (lane == 0) raise_abort2(sh, err);
+          break;
+        }
+        tc_fence_after();
+        const int col0 = (t - tab.tile0[s]) * BN;
+        const int valid = tab.valid[s];
+        const int32_t id_base = tab.start[s];
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(taddr + c * 32, r);
-        tmem_ld_wait();
-        const int cbase = col0 + c * 32;
-        if (cbase < valid) {
+        for (int q = 0; q < BN / 32; ++q) {
+          uint32_t r[32];
+          tmem_ld32(taddr + q * 32, r);
+          tmem_ld_wait();
+          const int cbase = col0 + q * 32;
+          if (cbase + 32 <= valid) {
+            scan32(r, id_base + cbase, best, best_id);
+          } else if (cbase < valid) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float x = __uint_as_float(r[i]);
-            if (cbase + i < valid && scan_better(x, best)) {
-              best = x;
-              best_id = shard_start + cbase + i;
+            for (int i = 0; i < 32; ++i) {
+              const float x = __uint_as_float(r[i]);
+              if (cbase + i < valid && scan_better(x, best)) {
+                best = x;
+                best_id = id_base + cbase + i;
+              }
             }
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader)
+            mbar_arrive(smem_u32(&sh->tmem_empty[acc]));
+          else
+            mbar_arrive_remote(empty_leader[acc]);
+        }
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (leader)
-          mbar_arrive(smem_u32(&sh->tmem_empty[acc]));
-        else
-          mbar_arrive_remote(empty_leader[acc]);
-      }
-      const int row = mp * 256 + row_in_tile;
-      if (row < M) {
-        sga_stat st;
-        st.v = best;
-        st.id = best_id;
-        ws[static_cast<size_t>(row) * n_tiles + n] = st;
-      }
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1;
+      if (ok && row < M)
+        ws[(static_cast<size_t>(s) * M + row) * num_chunks + c] = {best, best_id};
     }
   }
 
@@ -597,20 +682,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   }
 }
 
-// One warp per row: lanes stride over the row's per-tile partials (contiguous,
+// One warp per row: lanes stride over the row's partials (contiguous,
 // row-major workspace) and merge them with the (value, id) order.
 // Values of the fp8 variant are raw accumulators of the E4M3 codes until
 // here; the positive row and weight scales (which cannot change the argmax of
 // a row) are applied to the winning value only.
 // The shards whose partials one finalize launch merges: row r of the output
-// (shard r / M, hidden row r % M) reports shard start[r / M]'s first id when
-// no partial has a valid id.
+// (shard s = r / M, hidden row r % M) merges the cnt[s] partials at
+// ws[r * stride + lo[s] ...], and reports shard start[s]'s first id when no
+// partial has a valid id (or when cnt[s] is 0: a shard without valid ids).
 struct FinalizeShards {
   int n;
   int32_t start[kMaxLmShards];
+  int32_t lo[kMaxLmShards];
+  int32_t cnt[kMaxLmShards];
 };
 
-__global__ void lmhead_finalize_kernel(const sga_stat *__restrict__ ws, int M, int n_tiles,
+__global__ void lmhead_finalize_kernel(const sga_stat *__restrict__ ws, int M, int stride,
                                        const __grid_constant__ FinalizeShards shards,
                                        sga_stat *__restrict__ out,
                                        const float *__restrict__ row_scale, float w_scale,
@@ -620,17 +708,19 @@ __global__ void lmhead_finalize_kernel(const sga_stat *__restrict__ ws, int M, i
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= shards.n * M) return;
-  const int shard_start = shards.start[r / M];
+  const int s_idx = r / M;
+  const int shard_start = shards.start[s_idx];
+  const int count = shards.cnt[s_idx];
   float bv = __int_as_float(0xff800000);
   int32_t bi = kNoId;
-  const sga_stat *row = ws + static_cast<size_t>(r) * n_tiles;
+  const sga_stat *row = ws + static_cast<size_t>(r) * stride + shards.lo[s_idx];
   constexpr int kInFlight = 4;  // loads issued before the first compare
-  for (int n0 = lane; n0 < n_tiles; n0 += 32 * kInFlight) {
+  for (int n0 = lane; n0 < count; n0 += 32 * kInFlight) {
     sga_stat c[kInFlight];
 #pragma unroll
     for (int u = 0; u < kInFlight; ++u) {
       const int n = n0 + 32 * u;
-      if (n < n_tiles) {
+      if (n < count) {
         c[u] = row[n];
       } else {
         c[u].v = __int_as_float(0xff800000);
@@ -693,38 +783,13 @@ int resident_pairs(int num_sms) {
   return cache[dev];
 }
 
-// Partial statistics go to ws[row * (*ws_stride) + part]; *ws_stride <=
-// n_tiles, so a workspace of M x n_tiles stats always suffices.
+// 1-SM kernel (65 <= M <= 128) over one shard: one partial per (row, 256-id
+// tile) at ws[row * n_tiles + tile].
 template <bool kFp8>
-cudaError_t launch_gemm(const void *hidden, int64_t M, int64_t H, const void *weight,
-                        int64_t shard_start, int64_t valid, sga_stat *ws, int n_tiles, int num_sms,
-                        uint32_t *err, cudaStream_t stream, int *ws_stride) {
+cudaError_t launch_gemm_1sm(const void *hidden, int64_t M, int64_t H, const void *weight,
+                            int64_t shard_start, int64_t valid, sga_stat *ws, int n_tiles,
+                            int num_sms, uint32_t *err, cudaStream_t stream) {
   const int num_kb = static_cast<int>(H / kBk<kFp8>);
-  *ws_stride = n_tiles;
-  if (M <= SGA_LMHEAD_DECODE_MAX_M) {
-    const int64_t row0 = 0;
-    return launch_lmhead_decode(kFp8, hidden, M, H, weight, 1, &shard_start, &row0, &valid, ws,
-                                num_sms, err, stream, ws_stride);
-  }
-  if (SGA_LMHEAD_2SM && M >= SGA_LMHEAD_2SM_MIN_M && num_sms >= 2) {
-    // 2-SM tiles (256 rows per CTA pair)
-    CUtensorMap map_a, map_b;
-    if (!make_map(&map_a, hidden, M, H, 128, kFp8) || !make_map(&map_b, weight, valid, H, 128, kFp8))
-      return cudaErrorInvalidValue;
-    cudaError_t e = set_smem_once(reinterpret_cast<const void *>(lmhead_argmax_2sm_kernel<kFp8>),
-                                  SMEM2_BYTES, kFp8 ? 2 : 0);
-    if (e != cudaSuccess) return e;
-    const int m_pairs = static_cast<int>((M + 255) / 256);
-    const int total = m_pairs * n_tiles;
-    // A persistent grid must be fully resident: a cluster needs both CTAs in
-    // one GPC, so fewer than num_sms / 2 pairs may fit at once.
-    const int resident = resident_pairs<kFp8>(num_sms);
-    if (resident <= 0) return cudaErrorLaunchOutOfResources;
-    const int pairs = total < resident ? total : resident;
-    return launch_pdl(lmhead_argmax_2sm_kernel<kFp8>, 2 * pairs, SMEM2_BYTES, stream, map_a,
-                      map_b, static_cast<int>(M), num_kb, m_pairs, n_tiles,
-                      static_cast<int>(valid), static_cast<int>(shard_start), ws, err);
-  }
   CUtensorMap map_a, map_b;
   if (!make_map(&map_a, hidden, M, H, BM, kFp8) || !make_map(&map_b, weight, valid, H, BN, kFp8))
     return cudaErrorInvalidValue;
@@ -739,6 +804,40 @@ cudaError_t launch_gemm(const void *hidden, int64_t M, int64_t H, const void *we
                     static_cast<int>(shard_start), ws, err);
 }
 
+// 2-SM kernel (M >= 129) over every shard of the table in one launch; the
+// weight map spans map_rows rows.  Sets *chunks to the partial slots per
+// (shard, row) (0 when there is no tile: nothing is launched).
+template <bool kFp8>
+cudaError_t launch_gemm_2sm(const void *hidden, int64_t M, int64_t H, const void *weight,
+                            int64_t map_rows, const GemmShardTable &tab, sga_stat *ws,
+                            int num_sms, uint32_t *err, cudaStream_t stream, int *chunks) {
+  *chunks = 0;
+  const int T = tab.tile0[tab.n];
+  if (T == 0) return cudaSuccess;
+  if (num_sms < 2) return cudaErrorNotSupported;
+  const int num_kb = static_cast<int>(H / kBk<kFp8>);
+  CUtensorMap map_a, map_b;
+  if (!make_map(&map_a, hidden, M, H, 128, kFp8) || !make_map(&map_b, weight, map_rows, H, 128, kFp8))
+    return cudaErrorInvalidValue;
+  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(lmhead_argmax_2sm_kernel<kFp8>),
+                                SMEM2_BYTES, kFp8 ? 2 : 0);
+  if (e != cudaSuccess) return e;
+  // A persistent grid must be fully resident: a cluster needs both CTAs in
+  // one GPC, so fewer than num_sms / 2 pairs may fit at once.
+  const int resident = resident_pairs<kFp8>(num_sms);
+  if (resident <= 0) return cudaErrorLaunchOutOfResources;
+  const int m_pairs = static_cast<int>((M + 255) / 256);
+  int C = resident / m_pairs;
+  if (C < 1) C = 1;
+  if (C > T) C = T;
+  if (C > kMaxChunks) C = kMaxChunks;
+  const int units = m_pairs * C;
+  const int pairs = units < resident ? units : resident;
+  *chunks = C;
+  return launch_pdl(lmhead_argmax_2sm_kernel<kFp8>, 2 * pairs, SMEM2_BYTES, stream, map_a, map_b,
+                    static_cast<int>(M), num_kb, m_pairs, C, tab, ws, err);
+}
+
 }  // namespace
 
 cudaError_t launch_selftest_timeout(unsigned long long limit_ns, uint32_t *err,
@@ -747,32 +846,39 @@ cudaError_t launch_selftest_timeout(unsigned long long limit_ns, uint32_t *err,
   return cudaGetLastError();
 }
 
-// Partials per row: one per 256-id tile, and for decode sizes at least one per
-// CTA of the decode kernel (up to kDecMaxParts), so that narrow shards still
-// spread over every SM.  For M <= 64 the extra is at most 128 KB.
-// Workspace of launch_lmhead_argmax_shards: decode sizes keep num_shards x M
-// x (CTAs of the launch, at most kDecMaxParts) partials; larger M reuses one
-// shard's workspace per shard.
-size_t lmhead_shards_workspace_bytes(int64_t M, int num_shards, const int64_t *widths) {
-  if (M <= SGA_LMHEAD_DECODE_MAX_M)
-    return static_cast<size_t>(num_shards) * static_cast<size_t>(M) * kDecMaxParts *
-           sizeof(sga_stat);
-  size_t most = 0;
-  for (int s = 0; s < num_shards; ++s) {
-    const size_t b = lmhead_workspace_bytes(M, widths[s]);
-    if (b > most) most = b;
-  }
-  return most;
+// Workspace (partial statistics) of one call:
+//   M <= 64 (decode kernel): one partial per (shard, row, CTA), the CTAs of a
+//     launch at most kDecMaxParts; for one shard at least one per 256-id tile;
+//   65 <= M <= 128 (1-SM kernel, one launch per shard, the workspace reused):
+//     one partial per (row, 256-id tile) of the widest shard;
+//   M >= 129 (2-SM kernel, one launch for every shard): one partial per
+//     (shard, row, chunk), at most min(kMaxChunks, tiles of all shards)
+//     chunks.
+size_t lmhead_workspace_bytes(int64_t M, int64_t width) {
+  return lmhead_shards_workspace_bytes(M, 1, &width);
 }
 
-size_t lmhead_workspace_bytes(int64_t M, int64_t width) {
-  int64_t parts = (width + BN - 1) / BN;
-  if (M <= SGA_LMHEAD_DECODE_MAX_M) {
-    int64_t dec = (width + 127) / 128;
-    if (dec > kDecMaxParts) dec = kDecMaxParts;
-    if (dec > parts) parts = dec;
+size_t lmhead_shards_workspace_bytes(int64_t M, int num_shards, const int64_t *widths) {
+  int64_t all_tiles = 0, most_tiles = 0;
+  for (int s = 0; s < num_shards; ++s) {
+    const int64_t t = (widths[s] + BN - 1) / BN;
+    all_tiles += t;
+    if (t > most_tiles) most_tiles = t;
   }
-  return static_cast<size_t>(parts * M) * sizeof(sga_stat);
+  if (M <= SGA_LMHEAD_DECODE_MAX_M) {
+    if (num_shards == 1) {
+      int64_t parts = (widths[0] + 127) / 128;
+      if (parts > kDecMaxParts) parts = kDecMaxParts;
+      if (parts < most_tiles) parts = most_tiles;
+      return static_cast<size_t>(parts * M) * sizeof(sga_stat);
+    }
+    return static_cast<size_t>(num_shards) * static_cast<size_t>(M) * kDecMaxParts *
+           sizeof(sga_stat);
+  }
+  if (M < SGA_LMHEAD_2SM_MIN_M) return static_cast<size_t>(most_tiles * M) * sizeof(sga_stat);
+  const int64_t chunks = all_tiles < kMaxChunks ? all_tiles : kMaxChunks;
+  return static_cast<size_t>(num_shards) * static_cast<size_t>(M) *
+         static_cast<size_t>(chunks) * sizeof(sga_stat);
 }
 
 namespace {
@@ -804,22 +910,8 @@ cudaError_t launch_lmhead_argmax(const void *hidden, int64_t M, int64_t H, const
                                  sga_stat *out, void *workspace, int num_sms, uint32_t *err,
                                  cudaStream_t stream, bool fp8, const float *row_scale,
                                  float w_scale) {
-  (void)width;
-  sga_stat *ws = static_cast<sga_stat *>(workspace);
-  const int n_tiles = static_cast<int>((valid + BN - 1) / BN);
-  int ws_stride = n_tiles;  // partials per row in the workspace
-  if (n_tiles > 0) {
-    const cudaError_t e =
-        fp8 ? launch_gemm<true>(hidden, M, H, weight, shard_start, valid, ws, n_tiles, num_sms,
-                                err, stream, &ws_stride)
-            : launch_gemm<false>(hidden, M, H, weight, shard_start, valid, ws, n_tiles, num_sms,
-                                 err, stream, &ws_stride);
-    if (e != cudaSuccess) return e;
-  }
-  FinalizeShards fs = {};
-  fs.n = 1;
-  fs.start[0] = static_cast<int32_t>(shard_start);
-  return launch_finalize(ws, M, ws_stride, fs, out, row_scale, w_scale, fp8, stream);
+  return launch_lmhead_argmax_shards(hidden, M, H, weight, 1, &shard_start, &width, &valid, out,
+                                     workspace, num_sms, err, stream, fp8, row_scale, w_scale);
 }
 
 cudaError_t launch_lmhead_argmax_shards(const void *hidden, int64_t M, int64_t H,
@@ -828,34 +920,80 @@ cudaError_t launch_lmhead_argmax_shards(const void *hidden, int64_t M, int64_t H
                                         const int64_t *valids, sga_stat *out, void *workspace,
                                         int num_sms, uint32_t *err, cudaStream_t stream,
                                         bool fp8, const float *row_scale, float w_scale) {
+  (void)widths;
   sga_stat *ws = static_cast<sga_stat *>(workspace);
-  if (M > SGA_LMHEAD_DECODE_MAX_M) {
-    // tensor-bound sizes: one GEMM + finalize per shard, the workspace reused
-    // (each launch waits for the previous one before touching it)
-    const size_t row_bytes = static_cast<size_t>(H) * (fp8 ? 1 : 2);
+  const size_t row_bytes = static_cast<size_t>(H) * (fp8 ? 1 : 2);
+  FinalizeShards fs = {};
+  fs.n = num_shards;
+  for (int s = 0; s < num_shards; ++s) fs.start[s] = static_cast<int32_t>(starts[s]);
+
+  if (M <= SGA_LMHEAD_DECODE_MAX_M) {
+    // decode sizes: every shard in one launch, one finalize for all of them
+    int64_t row0s[kMaxLmShards];
+    for (int s = 0; s < num_shards; ++s) row0s[s] = starts[s] - starts[0];
+    int ws_stride = 0;
+    const cudaError_t e = launch_lmhead_decode(fp8, hidden, M, H, weight, num_shards, starts,
+                                               row0s, valids, ws, num_sms, err, stream,
+                                               &ws_stride);
+    if (e != cudaSuccess) return e;
+    for (int s = 0; s < num_shards; ++s) fs.cnt[s] = ws_stride;
+    return launch_finalize(ws, M, ws_stride, fs, out, row_scale, w_scale, fp8, stream);
+  }
+
+  if (M < SGA_LMHEAD_2SM_MIN_M) {
+    // 1-SM kernel: one GEMM + finalize per shard, the workspace reused (each
+    // launch waits for the previous one before touching it)
     for (int s = 0; s < num_shards; ++s) {
       const void *w = static_cast<const char *>(weight) +
                       static_cast<size_t>(starts[s] - starts[0]) * row_bytes;
+      const int n_tiles = static_cast<int>((valids[s] + BN - 1) / BN);
+      if (n_tiles > 0) {
+        const cudaError_t e =
+            fp8 ? launch_gemm_1sm<true>(hidden, M, H, w, starts[s], valids[s], ws, n_tiles,
+                                        num_sms, err, stream)
+                : launch_gemm_1sm<false>(hidden, M, H, w, starts[s], valids[s], ws, n_tiles,
+                                         num_sms, err, stream);
+        if (e != cudaSuccess) return e;
+      }
+      FinalizeShards one = {};
+      one.n = 1;
+      one.start[0] = fs.start[s];
+      one.cnt[0] = n_tiles;
       const cudaError_t e =
-          launch_lmhead_argmax(hidden, M, H, w, starts[s], widths[s], valids[s], out + s * M,
-                               workspace, num_sms, err, stream, fp8, row_scale, w_scale);
+          launch_finalize(ws, M, n_tiles, one, out + s * M, row_scale, w_scale, fp8, stream);
       if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
   }
-  // decode sizes: every shard in one launch, one finalize for all of them
-  int64_t row0s[kMaxLmShards];
-  FinalizeShards fs = {};
-  fs.n = num_shards;
+
+  // 2-SM kernel: every shard in one launch, one finalize for all of them
+  GemmShardTable tab = {};
+  tab.n = num_shards;
+  int64_t map_rows = 0;
+  int tiles = 0;
   for (int s = 0; s < num_shards; ++s) {
-    row0s[s] = starts[s] - starts[0];
-    fs.start[s] = static_cast<int32_t>(starts[s]);
+    tab.start[s] = static_cast<int32_t>(starts[s]);
+    tab.row0[s] = static_cast<int32_t>(starts[s] - starts[0]);
+    tab.valid[s] = static_cast<int32_t>(valids[s]);
+    tab.tile0[s] = tiles;
+    tiles += static_cast<int>((valids[s] + BN - 1) / BN);
+    if (valids[s] > 0 && tab.row0[s] + valids[s] > map_rows) map_rows = tab.row0[s] + valids[s];
   }
-  int ws_stride = 0;
-  const cudaError_t e = launch_lmhead_decode(fp8, hidden, M, H, weight, num_shards, starts, row0s,
-                                             valids, ws, num_sms, err, stream, &ws_stride);
+  tab.tile0[num_shards] = tiles;
+  int chunks = 0;
+  const cudaError_t e =
+      fp8 ? launch_gemm_2sm<true>(hidden, M, H, weight, map_rows, tab, ws, num_sms, err, stream,
+                                  &chunks)
+          : launch_gemm_2sm<false>(hidden, M, H, weight, map_rows, tab, ws, num_sms, err, stream,
+                                   &chunks);
   if (e != cudaSuccess) return e;
-  return launch_finalize(ws, M, ws_stride, fs, out, row_scale, w_scale, fp8, stream);
+  for (int s = 0; s < num_shards; ++s) {
+    if (tab.tile0[s + 1] > tab.tile0[s]) {
+      fs.lo[s] = chunk_of_tile(tab.tile0[s], tiles, chunks);
+      fs.cnt[s] = chunk_of_tile(tab.tile0[s + 1] - 1, tiles, chunks) - fs.lo[s] + 1;
+    }
+  }
+  return launch_finalize(ws, M, chunks, fs, out, row_scale, w_scale, fp8, stream);
 }
 
 }  // namespace sga

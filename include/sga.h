@@ -327,7 +327,7 @@ int sga_greedy_verify_prefill(const sga_stat *stats, int num_shards, int num_req
  *                 the kernel's, so values match an exact dot product only to
  *                 fp32 rounding and near-ties may resolve to either id.
  *   workspace     device, >= sga_lmhead_argmax_workspace(M, shard_width)
- *                 bytes, 8-byte aligned; holds per-tile partial statistics.
+ *                 bytes, 8-byte aligned; holds partial statistics.
  *                 Contents on entry are ignored; the caller must not use it
  *                 concurrently from two calls.
  * Requires a GPU of compute capability 10.3 (SGA_ERR_DEVICE otherwise).
@@ -424,10 +424,11 @@ int sga_lmhead_argmax_shards_fp8(const void *hidden_q, const float *hidden_scale
  *
  *   Arguments and results: as sga_lmhead_argmax, without workspace.
  *   Limit: sga_lmhead_argmax_workspace(M, shard_width) must not exceed
- *          SGA_LMHEAD_NOALLOC_SCRATCH_BYTES (M * ceil(shard_width / 256) * 8
- *          bytes; for M <= 64 the count per row is at least
- *          min(ceil(shard_width / 128), 256)); larger calls return
- *          SGA_ERR_WORKSPACE and enqueue nothing.
+ *          SGA_LMHEAD_NOALLOC_SCRATCH_BYTES (M * P * 8 bytes, P partials per
+ *          row: for M >= 129 P = min(ceil(shard_width / 256), 128); for
+ *          65 <= M <= 128 P = ceil(shard_width / 256); for M <= 64 P =
+ *          max(ceil(shard_width / 256), min(ceil(shard_width / 128), 256)));
+ *          larger calls return SGA_ERR_WORKSPACE and enqueue nothing.
  *   Set-up: the first call on a device looks up the device address of the
  *          scratch array for that device (with that device current), so make
  *          the first call on each device before any stream capture.  The

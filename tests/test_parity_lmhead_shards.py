@@ -35,7 +35,7 @@ def one_call(sga, h, w, shards, org_vocab, fp8=False, hs=None, w_scale=1.0):
     return gh.stats_to_numpy(stats)
 
 
-@pytest.mark.parametrize("M", [1, 7, 16, 17, 32, 33, 64, 65, 200])
+@pytest.mark.parametrize("M", [1, 7, 16, 17, 32, 33, 64, 65, 200, 513])
 @pytest.mark.parametrize("layout", ["uneven3", "gap", "padded", "eight", "single"])
 def test_bf16_one_call_equals_per_shard_calls(sga_lib, M, layout):
     H = 256
@@ -60,7 +60,7 @@ def test_bf16_one_call_equals_per_shard_calls(sga_lib, M, layout):
         lm.check_rows(rows, hidden, weight, shards, org, per, vals, ids)
 
 
-@pytest.mark.parametrize("M", [1, 16, 40, 64, 100])
+@pytest.mark.parametrize("M", [1, 16, 40, 64, 100, 300])
 def test_fp8_one_call_equals_per_shard_calls(sga_lib, M):
     H, vocab = 256, 12288
     shards = [(0, 4096), (4096, 4096), (8192, 4096)]
@@ -91,7 +91,7 @@ def test_fused_lmhead_decode_shape_every_shard_in_one_launch(sga_lib):
         gh.assert_stats_equal(one, gh.stats_to_numpy(per))
 
 
-@pytest.mark.parametrize("M", [1, 16, 64])
+@pytest.mark.parametrize("M", [1, 16, 64, 130, 300])
 @pytest.mark.parametrize("case", ["sixty_four_narrow", "padding_after_first", "tiny_widths"])
 def test_one_call_edge_layouts(sga_lib, M, case):
     # the epilogue's per-shard flushes where most CTAs hold tiles of few or no

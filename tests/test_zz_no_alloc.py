@@ -95,7 +95,7 @@ def test_noalloc_refuses_more_than_its_scratch(sga_lib):
     vp = ctypes.c_void_p
     fake = vp(0x10000)   # never dereferenced: the size check comes first
     # the limit is sga_lmhead_argmax_workspace(M, width) <= 4 MiB
-    assert sga_lib.sga_lmhead_argmax_workspace(4096, 200000) > (4 << 20)
-    assert fn(fake, 4096, 4096, fake, 0, 200000, 200000, fake, None) == -7
+    assert sga_lib.sga_lmhead_argmax_workspace(8192, 200000) > (4 << 20)
+    assert fn(fake, 8192, 4096, fake, 0, 200000, 200000, fake, None) == -7
     # decode sizes count up to 256 partials per row: 64 rows x 256 x 8 B = 128 KiB fits
     assert sga_lib.sga_lmhead_argmax_workspace(64, 200000) <= (4 << 20)
