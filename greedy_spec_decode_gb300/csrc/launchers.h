@@ -93,14 +93,16 @@ size_t lmhead_shards_workspace_bytes(int64_t M, int num_shards, const int64_t *w
 
 // Decode-size LM head (lmhead_decode.cu), M <= 64, over num_shards shards in
 // one launch: shard s covers global ids [starts[s], starts[s] + valids[s])
-// at weight rows row0s[s] .. (ascending shards).  Writes one partial per
-// (shard, row, CTA) to ws[(s * M + row) * (*ws_stride) + cta] and sets
-// *ws_stride (0 when no shard has a valid id: nothing is launched).
+// at weight rows row0s[s] .. (ascending shards).  The CTAs merge their
+// winners in library-owned memory and the last one writes the statistics of
+// shard s, row r to out[s * M + r] (values scaled by row_scale[r] * w_scale
+// when fp8).  *launched is false when no shard has a valid id (nothing is
+// launched and out is not written).
 cudaError_t launch_lmhead_decode(bool fp8, const void *hidden, int64_t M, int64_t H,
                                  const void *weight, int num_shards, const int64_t *starts,
-                                 const int64_t *row0s, const int64_t *valids, sga_stat *ws,
-                                 int num_sms, uint32_t *err, cudaStream_t stream,
-                                 int *ws_stride);
+                                 const int64_t *row0s, const int64_t *valids, sga_stat *out,
+                                 const float *row_scale, float w_scale, int num_sms,
+                                 uint32_t *err, cudaStream_t stream, bool *launched);
 
 // Bounded-wait self-test (lmhead.cu).
 cudaError_t launch_selftest_timeout(unsigned long long limit_ns, uint32_t *err,

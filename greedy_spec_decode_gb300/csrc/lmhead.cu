@@ -928,16 +928,17 @@ cudaError_t launch_lmhead_argmax_shards(const void *hidden, int64_t M, int64_t H
   for (int s = 0; s < num_shards; ++s) fs.start[s] = static_cast<int32_t>(starts[s]);
 
   if (M <= SGA_LMHEAD_DECODE_MAX_M) {
-    // decode sizes: every shard in one launch, one finalize for all of them
+    // decode sizes: every shard in one launch, which also merges its CTAs'
+    // winners (no finalize launch, no workspace)
     int64_t row0s[kMaxLmShards];
     for (int s = 0; s < num_shards; ++s) row0s[s] = starts[s] - starts[0];
-    int ws_stride = 0;
+    bool launched = false;
     const cudaError_t e = launch_lmhead_decode(fp8, hidden, M, H, weight, num_shards, starts,
-                                               row0s, valids, ws, num_sms, err, stream,
-                                               &ws_stride);
-    if (e != cudaSuccess) return e;
-    for (int s = 0; s < num_shards; ++s) fs.cnt[s] = ws_stride;
-    return launch_finalize(ws, M, ws_stride, fs, out, row_scale, w_scale, fp8, stream);
+                                               row0s, valids, out, row_scale, w_scale, num_sms,
+                                               err, stream, &launched);
+    if (e != cudaSuccess || launched) return e;
+    // every shard is padding: the finalize with no partials reports them
+    return launch_finalize(ws, M, 0, fs, out, row_scale, w_scale, fp8, stream);
   }
 
   if (M < SGA_LMHEAD_2SM_MIN_M) {

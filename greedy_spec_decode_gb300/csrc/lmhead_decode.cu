@@ -6,6 +6,8 @@
 // get_top_tokens); vLLM PR #39419, Changes (lm_head on the hidden states,
 // then the local argmax).  At decode sizes the step is a weight stream, so
 // this kernel is shaped for HBM, not for the tensor pipe.
+#include <atomic>
+
 #include "tcgen05.cuh"
 
 namespace sga {
@@ -70,9 +72,48 @@ struct SharedDec {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
+  int is_last;
   float part_v[4][kN];
   int32_t part_i[4][kN];
 };
+
+// Cross-CTA merge of a decode launch, in library-owned device memory: each
+// CTA folds its (shard, row) winners into 64-bit keys with atomicMax; the
+// last CTA to finish (a ticket) turns the keys into the statistics, scales
+// fp8 values, and resets keys and ticket to zero for the next launch that
+// uses the slot.  A launch takes slot (call number mod kMergeSlots); launches
+// that share a slot must not overlap on the GPU.
+constexpr int kMergeSlots = 32;
+constexpr int kMergeKeys = kMaxLmShards * SGA_LMHEAD_DECODE_MAX_M;  // shards x rows
+__device__ unsigned long long g_dec_keys[kMergeSlots][kMergeKeys];
+__device__ unsigned int g_dec_ticket[kMergeSlots];
+
+// Key of a (value, id) pair whose unsigned order is the argmax order: the
+// high word orders values (NaN above +inf, +0 and -0 equal), the low word
+// (0xffffffff - id) puts the lower id above on equal values.  Key 0 is below
+// every pair (an empty slot).
+__device__ __forceinline__ unsigned long long merge_key(float v, int32_t id) {
+  const uint32_t b = __float_as_uint(v);
+  uint32_t o;
+  if (is_nan(v))
+    o = 0xffffffffu;
+  else if ((b & 0x7fffffffu) == 0)
+    o = 0x80000000u;
+  else
+    o = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return (static_cast<unsigned long long>(o) << 32) | (0xffffffffu - static_cast<uint32_t>(id));
+}
+
+// The pair of a nonzero key (a NaN comes back as the canonical quiet NaN,
+// -0 as +0).
+__device__ __forceinline__ void merge_unkey(unsigned long long key, float &v, int32_t &id) {
+  const uint32_t o = static_cast<uint32_t>(key >> 32);
+  id = static_cast<int32_t>(0xffffffffu - static_cast<uint32_t>(key));
+  if (o == 0xffffffffu)
+    v = __uint_as_float(0x7fc00000u);
+  else
+    v = __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
 
 // The shards of one launch (one, or all the shards a GPU holds): shard s
 // covers global ids [start, start + valid) (its non-padding ids) at weight
@@ -193,8 +234,9 @@ template <bool kFp8, int kN>
 __global__ void __launch_bounds__(THREADS, 1)
     lmhead_argmax_decode_kernel(const __grid_constant__ CUtensorMap tmap_w,
                                 const __grid_constant__ CUtensorMap tmap_h, int M, int num_kb,
-                                const __grid_constant__ DecShardTable tab,
-                                sga_stat *__restrict__ ws, uint32_t *err) {
+                                const __grid_constant__ DecShardTable tab, int slot,
+                                sga_stat *__restrict__ out, const float *__restrict__ row_scale,
+                                float w_scale, int scaled, uint32_t *err) {
   constexpr int kStages = dec_stages<kN>;
   constexpr int kStageBytes = dec_stage_bytes<kN>;
   constexpr int kChunks = dec_chunks<kN>;
@@ -237,6 +279,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     mbar_init(smem_u32(&sh->drain), 1);
     sh->abort = 0;
+    sh->is_last = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -375,10 +418,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         int32_t id = sh->part_i[0][e];
 #pragma unroll
         for (int q = 1; q < 4; ++q) keep_better(v, id, sh->part_v[q][e], sh->part_i[q][e]);
-        sga_stat st;
-        st.v = v;
-        st.id = id;
-        ws[(static_cast<size_t>(s) * M + e) * gridDim.x + blockIdx.x] = st;
+        if (id != kNoId) atomicMax(&g_dec_keys[slot][s * M + e], merge_key(v, id));
       }
       asm volatile("bar.sync 1, 128;" ::: "memory");  // before the next flush's writes
     };
@@ -423,6 +463,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (acc == 0) acc_phase ^= 1;
     }
     while (cur < tab.n) flush(cur++);
+    __threadfence();  // this CTA's merges before its ticket
   }
 
   pdl_launch_dependents();
@@ -455,13 +496,38 @@ __global__ void __launch_bounds__(THREADS, 1)
                  "r"(kCols)
                  : "memory");
   }
+  // Every CTA takes one ticket (also after an abort, so the count always
+  // returns to zero); its merges are ordered before the ticket.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    sh->is_last = atomicAdd(&g_dec_ticket[slot], 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (sh->is_last) {
+    __threadfence();
+    for (int r = threadIdx.x; r < tab.n * M; r += blockDim.x) {
+      const unsigned long long key = atomicExch(&g_dec_keys[slot][r], 0ull);
+      sga_stat st;
+      if (key == 0) {
+        st.v = __int_as_float(0xff800000);  // no element of the shard: its first id, -inf
+        st.id = tab.start[r / M];
+      } else {
+        merge_unkey(key, st.v, st.id);
+        if (scaled) st.v *= (row_scale ? row_scale[r % M] : 1.0f) * w_scale;
+      }
+      out[r] = st;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) atomicExch(&g_dec_ticket[slot], 0u);
+  }
 }
 
 template <bool kFp8, int kN>
 cudaError_t launch_decode(const void *hidden, int64_t M, int64_t H, const void *weight,
                           int num_shards, const int64_t *starts, const int64_t *row0s,
-                          const int64_t *valids, sga_stat *ws, int num_sms, uint32_t *err,
-                          cudaStream_t stream, int *ws_stride) {
+                          const int64_t *valids, sga_stat *out, const float *row_scale,
+                          float w_scale, int num_sms, uint32_t *err, cudaStream_t stream,
+                          bool *launched) {
   const int tile_ids = 128 * dec_halves<kN>;
   DecShardTable tab = {};
   tab.n = num_shards;
@@ -474,12 +540,11 @@ cudaError_t launch_decode(const void *hidden, int64_t M, int64_t H, const void *
     if (valids[s] > 0 && row0s[s] + valids[s] > map_rows) map_rows = row0s[s] + valids[s];
   }
   const int n_tiles = tab.tile0[num_shards];
-  // one CTA per SM, at most one per tile and kDecMaxParts; the workspace
-  // holds num_shards x M x grid partials
+  // one CTA per SM, at most one per tile and kDecMaxParts
   int grid = n_tiles < num_sms ? n_tiles : num_sms;
   if (grid > kDecMaxParts) grid = kDecMaxParts;
-  *ws_stride = grid;
-  if (grid == 0) return cudaSuccess;  // every shard is padding: the finalize alone reports it
+  *launched = grid > 0;
+  if (grid == 0) return cudaSuccess;  // every shard is padding: the caller reports it
   CUtensorMap map_w, map_h;
   if (!make_map(&map_w, weight, map_rows, H, 128, kFp8) || !make_map(&map_h, hidden, M, H, kN, kFp8))
     return cudaErrorInvalidValue;
@@ -487,20 +552,24 @@ cudaError_t launch_decode(const void *hidden, int64_t M, int64_t H, const void *
   const int slot = 4 + (kFp8 ? 4 : 0) + (kN == 16 ? 0 : kN == 32 ? 1 : kN == 64 ? 2 : 3);
   cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), dec_smem_bytes<kN>, slot);
   if (e != cudaSuccess) return e;
+  // a merge slot per call, in turn (see g_dec_keys)
+  static std::atomic<unsigned> next_slot{0};
+  const int merge_slot = static_cast<int>(next_slot.fetch_add(1) % kMergeSlots);
   return launch_pdl(kern, grid, dec_smem_bytes<kN>, stream, map_w, map_h, static_cast<int>(M),
-                    static_cast<int>(H / kBk<kFp8>), tab, ws, err);
+                    static_cast<int>(H / kBk<kFp8>), tab, merge_slot, out, row_scale, w_scale,
+                    kFp8 ? 1 : 0, err);
 }
 
 }  // namespace
 
 cudaError_t launch_lmhead_decode(bool fp8, const void *hidden, int64_t M, int64_t H,
                                  const void *weight, int num_shards, const int64_t *starts,
-                                 const int64_t *row0s, const int64_t *valids, sga_stat *ws,
-                                 int num_sms, uint32_t *err, cudaStream_t stream,
-                                 int *ws_stride) {
-#define SGA_DEC_LAUNCH(F, N)                                                                   \
-  launch_decode<F, N>(hidden, M, H, weight, num_shards, starts, row0s, valids, ws, num_sms, err, \
-                      stream, ws_stride)
+                                 const int64_t *row0s, const int64_t *valids, sga_stat *out,
+                                 const float *row_scale, float w_scale, int num_sms,
+                                 uint32_t *err, cudaStream_t stream, bool *launched) {
+#define SGA_DEC_LAUNCH(F, N)                                                                 \
+  launch_decode<F, N>(hidden, M, H, weight, num_shards, starts, row0s, valids, out, row_scale, \
+                      w_scale, num_sms, err, stream, launched)
   if (M <= 16) return fp8 ? SGA_DEC_LAUNCH(true, 16) : SGA_DEC_LAUNCH(false, 16);
   if (M <= 32) return fp8 ? SGA_DEC_LAUNCH(true, 32) : SGA_DEC_LAUNCH(false, 32);
   return fp8 ? SGA_DEC_LAUNCH(true, 64) : SGA_DEC_LAUNCH(false, 64);

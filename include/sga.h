@@ -25,7 +25,8 @@
  * Conventions for every entry point:
  *   - Every pointer is a DEVICE pointer unless stated otherwise; the caller
  *     owns every buffer.  The library allocates no memory and keeps no state
- *     besides per-device cached kernel attributes and a device error word.
+ *     besides per-device cached kernel attributes, a device error word, and
+ *     the merge slots of the decode-size LM head (see sga_lmhead_argmax).
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and the call returns without synchronising.
  *   - Arguments are validated on the host BEFORE anything is launched; a
@@ -329,7 +330,14 @@ int sga_greedy_verify_prefill(const sga_stat *stats, int num_shards, int num_req
  *   workspace     device, >= sga_lmhead_argmax_workspace(M, shard_width)
  *                 bytes, 8-byte aligned; holds partial statistics.
  *                 Contents on entry are ignored; the caller must not use it
- *                 concurrently from two calls.
+ *                 concurrently from two calls.  Unused for M <= 64.
+ * Decode sizes (M <= 64): one kernel launch, whose CTAs merge their per-row
+ * winners in library-owned device memory (32 merge slots per device, one
+ * taken per call in turn; the last CTA writes out_stats and clears the
+ * slot).  Calls whose kernels overlap on the GPU must not share a slot: at
+ * most 32 decode-size LM-head calls (of any LM-head entry point) may be in
+ * flight on one device at once, and a captured graph that holds such a call
+ * must not be replayed concurrently with itself.
  * Requires a GPU of compute capability 10.3 (SGA_ERR_DEVICE otherwise).
  */
 size_t sga_lmhead_argmax_workspace(int64_t M, int64_t shard_width);
