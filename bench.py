@@ -1087,7 +1087,10 @@ def measure_lmhead(args, fp8, rank, world):
                    "CUDA events around each LM-head call (GEMM + finalize)"),
         "calls": ("every shard in one sga_lmhead_argmax_shards call" if one_call else
                   "one sga_lmhead_argmax call per shard (each emulated rank its own)"),
-        "gpu_launches": args.steps * (3 if one_call and M <= DECODE_MAX_M else 2 * S + 1),
+        # one call: decode sizes 1 launch (the CTAs merge in-kernel), else the
+        # GEMM + finalize; per shard: the same per call; + the reduce
+        "gpu_launches": args.steps * (((1 if M <= DECODE_MAX_M else 2) * (1 if one_call else S))
+                                      + 1),
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
