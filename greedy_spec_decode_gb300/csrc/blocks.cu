@@ -74,7 +74,14 @@ namespace {
 //     change.
 // The earlier kernel (whole CTAs per request, as many for a request of 0
 // drafts as for one of 15, one piece per warp) took 250.2 / 189.2 / 162.4
-// us.
+// us.  Tried and dropped since (same process, median of 30 launches; K_i =
+// 15 / K_i uniform in 1..15): an L2 prefetch of each warp's next item
+// (255.0 -> 276.5 / 149.5 -> 171.6 us); the per-shard kernel's bulk-copy
+// ring with a CTA per (row, shard) walking the pieces in order (whole
+// vectors from the ring, a 128-thread reduction and barrier per piece):
+// 483-500 / 331-339 us against 254-258 / 150-152 us -- issue-bound (ncu: 97 M
+// warp instructions for 414 MB), because a 2 KB bonus piece gives each of
+// the 128 threads one vector and still costs a full CTA reduction.
 #ifndef SGA_BLOCKS_WARPS
 #define SGA_BLOCKS_WARPS 4
 #endif
