@@ -1,6 +1,7 @@
 """GPU parity of sga_lmhead_argmax_shards / _fp8: the LM head over several vocab
 shards of one weight buffer in one call (at decode sizes one launch of the
-decode-size kernel and one finalize for every shard).  Each tile's
+decode-size kernel, whose CTAs also merge the shards' statistics; from M =
+129 one 2-SM GEMM launch and one finalize for every shard).  Each tile's
 accumulation is the same as in one call per shard and the per-row merge uses
 the total (value, id) order, so the statistics must be bit-identical to
 num_shards sga_lmhead_argmax calls; sampled rows are also checked against the
@@ -113,3 +114,30 @@ def test_one_call_edge_layouts(sga_lib, M, case):
     one = one_call(sga_lib, gh.to_device(hidden), gh.to_device(weight), shards, org)
     gh.assert_stats_equal(one, per)
     lm.check_rows(np.arange(0, M, 5), hidden, weight, shards, org, per, vals, ids)
+
+
+def test_decode_merge_slots_come_back_clean(sga_lib):
+    # The decode-size kernel merges its CTAs' winners in one of 32 library-
+    # owned slots per call, taken in turn, which the last CTA clears.  Run 80
+    # calls in a row (every slot at least twice) over shapes with different
+    # shard and row counts -- including an all-padding shard, whose slot keys
+    # are never set -- and check each against the per-shard calls' statistics,
+    # themselves checked against the oracle: a key a call left behind would
+    # change a later result.
+    H = 128
+    cases = []
+    for n in range(8):
+        M = [1, 5, 16, 17, 33, 64, 2, 40][n]
+        vocab = 900 + 37 * n
+        shards = wl.random_shards(n + 101, vocab, 1 + n % 3)
+        # even n with several shards: the last shard all padding
+        org = vocab - (shards[-1][1] if n % 2 == 0 and len(shards) > 1 else 0)
+        hidden = wl.normal_matrix(n + 201, M, H, 1.0)
+        weight = wl.normal_matrix(n + 301, vocab, H, 1.0 / np.sqrt(H))
+        st, v, i = lm.run_gpu(hidden, weight, shards, org)
+        lm.check_rows(np.arange(M), hidden, weight, shards, org, st, v, i)
+        cases.append((gh.to_device(hidden), gh.to_device(weight), shards, org, st))
+    for k in range(80):
+        h, w, sh, org, ref = cases[k % len(cases)]
+        gh.assert_stats_equal(one_call(sga_lib, h, w, sh, org), ref)
+    assert sga_lib.sga_device_error() == 0
