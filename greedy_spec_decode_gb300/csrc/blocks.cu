@@ -30,9 +30,11 @@
 // the launch, request i's items start at number cu[i] * D + i * Bn, a closed
 // form: a warp finds the request of its first item with one binary search
 // over cu_num_draft and then walks forward.  Every CTA of the grid (one wave
-// of resident CTAs) takes an equal contiguous range of numbers, dealt
-// round-robin to its warps (so a CTA's warps read neighbouring items), and
-// the load is balanced whatever the number of requests and their K_i.  A
+// of resident CTAs) takes an equal contiguous range of numbers, so the load is
+// balanced whatever the number of requests and their K_i; inside that range
+// its warps take the items one at a time from a counter in shared memory (a
+// CTA's warps read neighbouring items), so that warps the memory system
+// serves faster take more.  A
 // warp (or lane group) scans a piece as the per-shard kernel scans a row:
 // 16-byte vectors with kUnroll streaming loads in flight per lane, the best
 // vector kept in registers and searched once; the element head (to the
@@ -86,14 +88,26 @@ namespace {
 // search over cu_num_draft) instead of by items: 274 / 166 us against 258 /
 // 152 us; the empty slots written by the warp of each row's first item,
 // during the stream, instead of after it: 266 / 154 us.
+// Per-warp timestamps of the round-robin kernel showed warps with equal work
+// finishing up to 30 us apart inside one SM (mixed K_i: first warp 104 us,
+// median 130 us, last 146 us): the memory system serves warps unevenly.
+// Items taken one at a time from a shared counter per CTA (the current
+// kernel): 8 warps x 4 CTAs per SM 248.1 / 143.4 us (0.988 / 0.960 of copy);
+// 4 x 8 per SM 252.2 / 147.5; 16 x 2 per SM 251.5 / 152.6; one CTA of 32
+// warps per SM 270 / 174; 8 x 4 with 8 loads in flight 250.1 / 145.4 us.
+#ifndef SGA_BLOCKS_DYNAMIC
+// 1: the warps of a CTA take its items one at a time from a shared-memory
+// counter (8-warp CTAs, 4 per SM).  0: 4-warp CTAs, items dealt round-robin.
+#define SGA_BLOCKS_DYNAMIC 1
+#endif
 #ifndef SGA_BLOCKS_WARPS
-#define SGA_BLOCKS_WARPS 4
+#define SGA_BLOCKS_WARPS (SGA_BLOCKS_DYNAMIC ? 8 : 4)
 #endif
 #ifndef SGA_BLOCKS_UNROLL
 #define SGA_BLOCKS_UNROLL 16
 #endif
 #ifndef SGA_BLOCKS_MIN_CTAS
-#define SGA_BLOCKS_MIN_CTAS 8
+#define SGA_BLOCKS_MIN_CTAS (SGA_BLOCKS_DYNAMIC ? 4 : 8)
 #endif
 #ifndef SGA_BLOCKS_CTAS_PER_SM
 #define SGA_BLOCKS_CTAS_PER_SM 0
@@ -420,6 +434,51 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, SGA_BLOCKS_MIN_CTAS)
     step = 1;
   }
 
+#if SGA_BLOCKS_DYNAMIC
+  // the CTA's contiguous range [t0 - warp, t1); each warp takes the next
+  // number from a shared counter, so the warps of an SM that the memory
+  // system serves faster take more items and all of them finish together
+  __shared__ unsigned long long next_item;
+  if (threadIdx.x == 0) next_item = static_cast<unsigned long long>(t0 - warp);
+  __syncthreads();
+  unsigned long long grabbed = 0;
+  if (lane == 0) grabbed = atomicAdd(&next_item, 1ull);
+  int64_t t = static_cast<int64_t>(__shfl_sync(0xffffffffu, grabbed, 0));
+  if (t < t1) {
+    int64_t g = request_at(t, num_groups, cu, rows, d, bn);
+    Request q = request_of(g, cu, rows, d, bn);
+    int64_t next0 = g + 1 < num_groups ? item0_of(g + 1, cu, rows, d, bn) : INT64_MAX;
+    int s = 0;
+    while (t < t1) {
+      // the next number, taken now so that the atomic's latency overlaps
+      // this item (the numbers a warp takes only increase)
+      if (lane == 0) grabbed = atomicAdd(&next_item, 1ull);
+      while (t >= next0) {
+        ++g;
+        q = request_of(g, cu, rows, d, bn);
+        next0 = g + 1 < num_groups ? item0_of(g + 1, cu, rows, d, bn) : INT64_MAX;
+        s = 0;
+      }
+      const int64_t u = t - q.item0;
+      if (u >= 0 && u < q.n_items) {  // else a request outside the rows or a hole
+        const Item it = item_of(static_cast<int32_t>(u), s, q, tab, draft_block, bonus_block,
+                                group_d, group_b);
+        if (it.g == 1) {
+          const Piece pc =
+              piece_at<kBf16>(it, it.p0, true, tab, org_vocab, logits, ld_bytes, rows);
+          const sga_stat stat = piece_argmax<kBf16, 32>(pc, lane);
+          if (lane == 0) out[pc.out_idx] = stat;
+        } else if (it.g == 2) {
+          scan_group<kBf16, 16>(it, lane, tab, org_vocab, logits, ld_bytes, rows, out);
+        } else {
+          scan_group<kBf16, 8>(it, lane, tab, org_vocab, logits, ld_bytes, rows, out);
+        }
+      }
+      t = static_cast<int64_t>(__shfl_sync(0xffffffffu, grabbed, 0));
+    }
+  }
+  (void)step;
+#else
   if (t0 < t1) {
     int64_t g = request_at(t0, num_groups, cu, rows, d, bn);
     Request q = request_of(g, cu, rows, d, bn);
@@ -456,6 +515,7 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, SGA_BLOCKS_MIN_CTAS)
       t += step;
     }
   }
+#endif
   pdl_launch_dependents();
 
   const int64_t n_threads = n_warps * 32;
