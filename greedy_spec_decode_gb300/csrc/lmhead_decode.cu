@@ -25,10 +25,11 @@ namespace {
 // TMEM lane = vocab id, TMEM column = hidden row.  The epilogue reduces each
 // group of 32 (or 16) rows across the 32 lanes of a warp with a butterfly
 // transpose-reduce in the (value, id) order, after which each lane holds one
-// row's winner and keeps that row's running best; the four epilogue warps
-// merge through shared memory at the end and each CTA writes one partial per
-// row to the workspace (row stride = number of CTAs); the finalize kernel
-// merges the CTAs' partials.
+// row's winner and keeps that row's running best; at each shard edge the
+// four epilogue warps merge through shared memory and the CTA merges its
+// winners into library-owned keys (atomicMax); the last CTA writes the stats.
+// CTAs take tiles one at a time from a counter of the launch, so an SM that
+// the memory system serves faster streams more of the weight.
 // ---------------------------------------------------------------------------
 // K chunks (128-byte columns of the weight) per stage: 1 -> a stage holds 256
 // weight rows x 128 B (a 256-id tile in two 128-row halves); 2 -> 128 rows x
@@ -75,7 +76,14 @@ struct SharedDec {
   int is_last;
   float part_v[4][kN];
   int32_t part_i[4][kN];
+  // the CTA's tiles, in the order the producer took them: entry k % kTileQ
+  // holds the k-th (-1 after the last); ready: 1 arrival (the producer),
+  // free: 5 (the MMA lane and the four epilogue warps, once read)
+  uint64_t tile_ready[8];
+  uint64_t tile_free[8];
+  int32_t tile_q[8];
 };
+constexpr int kTileQ = 8;
 
 // Cross-CTA merge of a decode launch, in library-owned device memory: each
 // CTA folds its (shard, row) winners into 64-bit keys with atomicMax; the
@@ -87,6 +95,9 @@ constexpr int kMergeSlots = 32;
 constexpr int kMergeKeys = kMaxLmShards * SGA_LMHEAD_DECODE_MAX_M;  // shards x rows
 __device__ unsigned long long g_dec_keys[kMergeSlots][kMergeKeys];
 __device__ unsigned int g_dec_ticket[kMergeSlots];
+// the next tile of a launch: CTAs take tiles one at a time, so SMs that the
+// memory system serves faster take more (cleared with the slot)
+__device__ unsigned int g_dec_next[kMergeSlots];
 
 // Key of a (value, id) pair whose unsigned order is the argmax order: the
 // high word orders values (NaN above +inf, +0 and -0 equal), the low word
@@ -255,8 +266,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int n_tiles = tab.tile0[tab.n];
 
   if (SGA_LMHEAD_DEC_PREFETCH && threadIdx.x == 64 && blockIdx.x < n_tiles) {
-    // Warm L2 with what the ring loads first (this CTA's first tile, one
-    // ring's worth of K blocks) while the previous kernel drains.  A prefetch
+    // Warm L2 with what the ring loads first (tile blockIdx.x: the CTAs take
+    // their first tiles in about launch order; one ring's worth of K blocks)
+    // while the previous kernel drains.  A prefetch
     // only moves lines into L2, which stays coherent with any later write, so
     // it may precede griddepcontrol.wait.
     const int n = blockIdx.x;
@@ -278,6 +290,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(smem_u32(&sh->tmem_empty[b]), 4 * 32);
     }
     mbar_init(smem_u32(&sh->drain), 1);
+    for (int q = 0; q < kTileQ; ++q) {
+      mbar_init(smem_u32(&sh->tile_ready[q]), 1);
+      mbar_init(smem_u32(&sh->tile_free[q]), 1 + 4);
+    }
     sh->abort = 0;
     sh->is_last = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -306,8 +322,22 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
-      int s = 0;  // the shard of tile n (the tiles only increase)
-      for (int n = blockIdx.x; n < n_tiles && !*abort_flag; n += gridDim.x) {
+      // Tiles come from the launch's counter one at a time (the next one is
+      // taken while the current one streams) and go to the MMA lane and the
+      // epilogue through the tile queue; they only increase.
+      int s = 0;  // the shard of tile n
+      int n = static_cast<int>(atomicAdd(&g_dec_next[slot], 1u));
+      for (int k = 0; !*abort_flag; ++k) {
+        const int q = k % kTileQ;
+        if (k >= kTileQ &&
+            !mbar_wait(smem_u32(&sh->tile_free[q]), ((k / kTileQ) - 1) & 1, abort_flag)) {
+          raise_abort_dec(sh, err);
+          break;
+        }
+        sh->tile_q[q] = n < n_tiles ? n : -1;
+        mbar_arrive(smem_u32(&sh->tile_ready[q]));
+        if (n >= n_tiles) break;
+        const int n_next = static_cast<int>(atomicAdd(&g_dec_next[slot], 1u));
         while (n >= tab.tile0[s + 1]) ++s;
         const int row = tab.row0[s] + (n - tab.tile0[s]) * kTileIds;
         for (int kb = 0; kb < num_kb; kb += kChunks) {
@@ -332,6 +362,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             prod_phase ^= 1;
           }
         }
+        n = n_next;
       }
     }
   } else if (warp == 1) {
@@ -339,7 +370,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       // ----------------------------------------------------------- MMA issuer
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
-      for (int n = blockIdx.x; n < n_tiles && !*abort_flag; n += gridDim.x) {
+      for (int k = 0; !*abort_flag; ++k) {
+        const int q = k % kTileQ;
+        if (!mbar_wait(smem_u32(&sh->tile_ready[q]), (k / kTileQ) & 1, abort_flag)) {
+          raise_abort_dec(sh, err);
+          break;
+        }
+        const int n = sh->tile_q[q];
+        mbar_arrive(smem_u32(&sh->tile_free[q]));
+        if (n < 0) break;
         if (!mbar_wait(smem_u32(&sh->tmem_empty[acc]), acc_phase ^ 1, abort_flag)) {
           raise_abort_dec(sh, err);
           break;
@@ -425,9 +464,20 @@ __global__ void __launch_bounds__(THREADS, 1)
     int cur = 0;  // the shard whose bests rv / ri hold
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int n = blockIdx.x; n < n_tiles; n += gridDim.x) {
+    for (int t = 0;; ++t) {
+      const int q = t % kTileQ;
+      bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&sh->tile_ready[q]),
+                                                  (t / kTileQ) & 1, abort_flag));
+      if (!ok) {
+        if (lane == 0) raise_abort_dec(sh, err);
+        break;
+      }
+      const int n = sh->tile_q[q];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh->tile_free[q]));
+      if (n < 0) break;
       while (n >= tab.tile0[cur + 1]) flush(cur++);
-      bool ok = mbar_wait(smem_u32(&sh->tmem_full[acc]), acc_phase, abort_flag);
+      ok = mbar_wait(smem_u32(&sh->tmem_full[acc]), acc_phase, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
         if (lane == 0) raise_abort_dec(sh, err);
@@ -518,7 +568,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       out[r] = st;
     }
     __syncthreads();
-    if (threadIdx.x == 0) atomicExch(&g_dec_ticket[slot], 0u);
+    if (threadIdx.x == 0) {
+      atomicExch(&g_dec_next[slot], 0u);
+      atomicExch(&g_dec_ticket[slot], 0u);
+    }
   }
 }
 
