@@ -882,7 +882,9 @@ def decode_roofline(weight_bytes, kern_ms, num_shards, fp8, captured_shape=True,
                                "fp8" if fp8 else "bf16"),
             "peak_source": f"{pk_src} hbm_gbs (MEASURED_PEAKS.json copy bandwidth)"
             if pk_src == "measured" else "fallback 6.8 TB/s",
-            "bytes_per_step": weight_bytes, "launches_per_step": 1 if one_call else num_shards}
+            "bytes_per_step": weight_bytes, "launches_per_step": 1 if one_call else num_shards,
+            "timing": f"median of {KERNEL_LAUNCHES} isolated event-timed LM-head calls"
+                      + ("" if one_call else f" ({num_shards} launches in each interval)")}
 
 
 def setup_device():
@@ -1005,6 +1007,27 @@ def measure_lmhead(args, fp8, rank, world):
         kern_times = [sum(e[2 * s].elapsed_time(e[2 * s + 1]) for s in range(1 if one_call else S))
                       for e in ev]
         kern_ms = statistics.median(kern_times)
+    # M <= 64 runs the decode-size kernel: a weight stream bound by HBM, not
+    # by the tensor cores (2 M flops per weight element)
+    decode = M <= DECODE_MAX_M
+    iso_times = None
+    if decode:
+        # the decode kernel alone for its roofline: KERNEL_LAUNCHES calls, each
+        # between its own events (one launch per call: the CTAs merge in-kernel)
+        def lmhead_calls():
+            for s, (o, w) in enumerate([(None, None)] if one_call else shards):
+                if one_call and fp8:
+                    sga.sga_lmhead_argmax_shards_fp8(hidden, hscale, weight, c["weight_scale"],
+                                                     shards, c["org_vocab"], stats, ws)
+                elif one_call:
+                    sga.sga_lmhead_argmax_shards(hidden, weight, shards, c["org_vocab"], stats, ws)
+                elif fp8:
+                    sga.sga_lmhead_argmax_fp8(hidden, hscale, w_views[s], c["weight_scale"], o,
+                                              c["org_vocab"], stats[s * M:(s + 1) * M], ws)
+                else:
+                    sga.sga_lmhead_argmax(hidden, w_views[s], o, c["org_vocab"],
+                                          stats[s * M:(s + 1) * M], ws)
+        iso_times = time_launches(lmhead_calls, KERNEL_LAUNCHES, torch)
     flops = 2.0 * M * H * sum(w for _, w in shards)
     pk, pk_src = peaks()
     # the LM-head calls are timed one by one over a short loop: the burst
@@ -1016,9 +1039,6 @@ def measure_lmhead(args, fp8, rank, world):
         sustained *= FP8_TO_BF16_NOMINAL
     achieved = flops / (kern_ms * 1e-3) / 1e12
     assert sga.sga_device_error() == 0, "device error word set during the bench"
-    # M <= 64 runs the decode-size kernel: a weight stream bound by HBM, not
-    # by the tensor cores (2 M flops per weight element)
-    decode = M <= DECODE_MAX_M
     weight_bytes = weight.numel() * weight.element_size()
 
     # end to end: hidden states in from pinned host memory, ids back
@@ -1054,8 +1074,9 @@ def measure_lmhead(args, fp8, rank, world):
         "weight_gbs": weight.numel() * weight.element_size() / (kern_ms * 1e-3) / 1e9,
         "kernel_us": {"lmhead_argmax_per_step": (spread(kern_times) if kern_times is not None
                                                  else round(kern_ms * 1e3, 2)),
-                      "reduce_and_gaps": round((step_ms - kern_ms) * 1e3, 2)},
-        "roofline": decode_roofline(weight_bytes, kern_ms, S, fp8,
+                      "reduce_and_gaps": round((step_ms - kern_ms) * 1e3, 2),
+                      **({"lmhead_argmax_isolated": spread(iso_times)} if decode else {})},
+        "roofline": decode_roofline(weight_bytes, statistics.median(iso_times), S, fp8,
                                     S == 2 and H == 4096 and args.lmhead_vocab == 151936,
                                     one_call)
         if decode else

@@ -547,14 +547,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                  : "memory");
   }
   // Every CTA takes one ticket (also after an abort, so the count always
-  // returns to zero); its merges are ordered before the ticket.
-  if (threadIdx.x == 0) {
-    __threadfence();
-    sh->is_last = atomicAdd(&g_dec_ticket[slot], 1u) == gridDim.x - 1;
-  }
+  // returns to zero).  The keys, the tile counter and the ticket are touched
+  // by atomics alone, which are performed in L2: every merge of this CTA was
+  // performed before its epilogue threads passed their fence, so before the
+  // barrier above and before the ticket, and the last CTA's exchanges are
+  // issued after it has seen every ticket (no further fence needed; each
+  // measured at about 0.3 us on the launch's critical path).
+  if (threadIdx.x == 0) sh->is_last = atomicAdd(&g_dec_ticket[slot], 1u) == gridDim.x - 1;
   __syncthreads();
   if (sh->is_last) {
-    __threadfence();
     for (int r = threadIdx.x; r < tab.n * M; r += blockDim.x) {
       const unsigned long long key = atomicExch(&g_dec_keys[slot][r], 0ull);
       sga_stat st;
