@@ -437,7 +437,18 @@ def time_e2e_pipelined(paths, c, steps, torch):
     ms = start.elapsed_time(end) / steps
     h2d = logits_h.numel() * 2 + drafts_h.numel() * 4 + cu_h.numel() * 4
     d2h = sum(h.numel() * 4 for h in outs_h[0])
-    return ms, h2d, d2h
+    # the host link alone: the same logits copy with nothing beside it
+    # (median of 3); the pipelined step cannot beat it
+    x = paths[0].x.view(torch.int16)
+    link = []
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        x.copy_(logits_h, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        link.append(logits_h.numel() * 2 / (a.elapsed_time(b) * 1e-3) / 1e9)
+    return ms, h2d, d2h, statistics.median(link)
 
 
 # ---------------------------------------------------------------------------
@@ -598,7 +609,7 @@ def run_ours_verify(args, blocks=None):
     serial_ms, h2d, d2h = time_e2e(path, c, args.e2e_steps, torch)
     serial_ms = max_over_ranks(serial_ms, world, "cuda")
     path2 = VerifyPath(c, torch, sga, blocks)   # the second buffer set of the pipelined loop
-    e2e_ms, _, _ = time_e2e_pipelined([path, path2], c, args.e2e_steps, torch)
+    e2e_ms, _, _, link_gbs = time_e2e_pipelined([path, path2], c, args.e2e_steps, torch)
     e2e_ms = max_over_ranks(e2e_ms, world, "cuda")
     del path2
 
@@ -643,6 +654,13 @@ def run_ours_verify(args, blocks=None):
         "e2e": {"value": world * path.rows / (e2e_ms * 1e-3), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "note": "two buffer sets: step i+1's inputs are copied in while step i runs",
+                "host_link": {"h2d_gbs": link_gbs,
+                              "achieved_gbs": h2d / (e2e_ms * 1e-3) / 1e9,
+                              "frac": h2d / (e2e_ms * 1e-3) / 1e9 / link_gbs,
+                              "note": "the step's input bytes per e2e step time against one "
+                                      "plain copy of the logits from pinned host memory; "
+                                      "more streams or a kernel reading the pinned memory "
+                                      "directly move no more over this link"},
                 "serial": {"value": world * path.rows / (serial_ms * 1e-3),
                            "ms_per_step": serial_ms,
                            "note": "copy in, step, copy out, one after the other"}},
