@@ -289,12 +289,26 @@ class VerifyPath:
         self.run_verify()
 
 
+GRAPH_STEPS = 10   # steps per captured CUDA graph in the timed loop
+
+
 def time_device_steps(path, steps, warmup, torch, world, rank):
     """K steps back to back between two events (no event between the
     kernels, so each launch overlaps the previous one's tail through
-    programmatic dependent launch)."""
+    programmatic dependent launch).  The steps are replayed from a CUDA graph
+    of GRAPH_STEPS steps (the remainder of K launched directly): every
+    launch still runs, and the timed loop does not depend on how fast the
+    host can submit (eager submission measured the same 225 us step on an
+    idle host, and 13 % longer steps on one busy host)."""
     for _ in range(warmup):
         path.step()
+    torch.cuda.synchronize()
+    g_steps = min(GRAPH_STEPS, steps)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(g_steps):
+            path.step()
+    graph.replay()   # untimed
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
@@ -302,12 +316,15 @@ def time_device_steps(path, steps, warmup, torch, world, rank):
     sampler = ClockSampler(torch.cuda.current_device()).start()
     time.sleep(0.3)
     start.record()
-    for _ in range(steps):
+    for _ in range(steps // g_steps):
+        graph.replay()
+    for _ in range(steps % g_steps):
         path.step()
     end.record()
     torch.cuda.synchronize()
     clocks = sampler.stop()
     barrier(world)
+    del graph
     return start.elapsed_time(end), clocks
 
 
@@ -629,6 +646,9 @@ def run_ours_verify(args, blocks=None):
                    "stats_per_row": path.n_stats,
                    "l2": f"inputs ({c['logits'].nbytes / 1e9:.2f} GB) larger than L2 (129 MB); no flush",
                    "parallelism": f"{world} independent replica(s), emulated TP{len(path.shards)} per GPU"},
+        "step_timing": (f"K steps between two CUDA events, replayed from CUDA graphs of "
+                        f"{min(GRAPH_STEPS, args.steps)} steps (every launch runs; no event "
+                        f"between steps)"),
         "step_gbs": path.step_bytes / (step_ms * 1e-3) / 1e9,
         "step_frac_of_hbm": path.step_bytes / (step_ms * 1e-3) / 1e9 / hbm,
         "kernel_us": {("block_argmax_all_shards" if blocks else "local_argmax_all_shards"):
@@ -935,6 +955,57 @@ def run_ours_lmhead(args, fp8=False):
     return finish(measure_lmhead(args, fp8, rank, world), rank, world)
 
 
+def library_gemm_context(hidden, weight, fp8, torch):
+    """cuBLAS (bf16) or cuBLASLt (fp8, torch._scaled_mm) on the LM head's GEMM
+    shape, writing the logits and taking no argmax, and on an 8192^3 GEMM of
+    the same type: context for the fused kernel's tensor roofline (the fp8
+    roofline itself is the measured bf16 burst x the nominal fp8 / bf16
+    ratio).  Back-to-back calls between two events, median of 3 x 20."""
+    def rate(fn, flops):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        res = []
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(20):
+                fn()
+            b.record()
+            torch.cuda.synchronize()
+            res.append(flops / (a.elapsed_time(b) / 20 * 1e-3) / 1e12)
+        return statistics.median(res)
+    M, H = hidden.shape
+    V = weight.shape[0]
+    g = torch.Generator(device="cuda").manual_seed(0)
+    sq = 8192
+    try:
+        if fp8:
+            one = torch.ones((), dtype=torch.float32, device="cuda")
+            h8, w8 = hidden.view(torch.float8_e4m3fn), weight.view(torch.float8_e4m3fn)
+            same = rate(lambda: torch._scaled_mm(h8, w8.t(), scale_a=one, scale_b=one,
+                                                 out_dtype=torch.bfloat16), 2.0 * M * H * V)
+            a = torch.randn(sq, sq, device="cuda", generator=g).to(torch.float8_e4m3fn)
+            b = torch.randn(sq, sq, device="cuda", generator=g).to(torch.float8_e4m3fn)
+            square = rate(lambda: torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one,
+                                                   out_dtype=torch.bfloat16), 2.0 * sq ** 3)
+            lib = "cuBLASLt via torch._scaled_mm, E4M3 x E4M3 -> bf16"
+        else:
+            out = torch.empty(M, V, dtype=torch.bfloat16, device="cuda")
+            same = rate(lambda: torch.matmul(hidden, weight.t(), out=out), 2.0 * M * H * V)
+            del out
+            a = torch.randn(sq, sq, device="cuda", generator=g).to(torch.bfloat16)
+            b = torch.randn(sq, sq, device="cuda", generator=g).to(torch.bfloat16)
+            square = rate(lambda: torch.matmul(a, b.t()), 2.0 * sq ** 3)
+            lib = "cuBLAS via torch.matmul, bf16 -> bf16"
+        del a, b
+        torch.cuda.empty_cache()
+    except (RuntimeError, TypeError) as e:
+        return {"unavailable": str(e).splitlines()[0][:200]}
+    return {"library": lib, "same_shape_tflops": same, "square_8192_tflops": square,
+            "note": "the library GEMM writes the logits and takes no argmax; context only"}
+
+
 def measure_lmhead(args, fp8, rank, world):
     """The fused LM-head step timed on this GPU; returns its JSON record."""
     import torch
@@ -1077,6 +1148,7 @@ def measure_lmhead(args, fp8, rank, world):
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world, "cuda")
+    lib_ctx = None if decode else library_gemm_context(hidden, weight, fp8, torch)
 
     line = {
         "metric": LMHEAD_METRIC_FP8 if fp8 else LMHEAD_METRIC,
@@ -1132,6 +1204,8 @@ def measure_lmhead(args, fp8, rank, world):
                                       + 1),
         "clocks": clocks,
     }
+    if lib_ctx is not None:
+        line["library_gemm"] = lib_ctx
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"], line["parity"] = lmhead_cpu_baseline(
             c, fp8, ids.cpu().numpy(), args.cpu_seconds)
