@@ -38,8 +38,14 @@ namespace {
 //   N = 16 (M <= 16): 1 chunk 199 / 113 us, 2 chunks 201 / 113, 4 chunks
 //                     193 / 108 (3 stages of 72 KB)
 //   N = 32, 64:       1 chunk 203-208 / 117-122 us, 2 chunks 196-200 /
-//                     110-115, 4 chunks 201-206 / 115-119 (only 2 stages)
-// Longer contiguous runs per weight row pay more than extra bytes in flight.
+//                     110-115, 4 chunks 201-206 / 115-119 (only 2 stages);
+//                     later, alternating on one box (M = 24 / 32 / 48 / 64):
+//                     2 chunks (4-5 stages) 181.5 / 181.4 / 184.0 / 183.9
+//                     and 97.0 / 96.7 / 99.0 / 98.5 us, 3 chunks (3 stages)
+//                     180.8 / 180.6 / 183.4 / 183.3 and 96.5 / 96.3 / 98.7 /
+//                     98.4, 4 chunks 185.0-188.0 and 99.0-102.0
+// Longer contiguous runs per weight row pay more than extra bytes in flight,
+// up to the point where the ring has only 2 stages.
 #ifndef SGA_LMHEAD_DEC_PREFETCH
 // L2 prefetch of the first stages before the PDL wait.  Measured (graph
 // replay, 8 shards of 18992 ids): bf16 M = 1 223.7 -> 219.7 us per step, fp8
@@ -50,7 +56,7 @@ namespace {
 #define SGA_LMHEAD_DEC_CHUNKS_N16 4
 #endif
 #ifndef SGA_LMHEAD_DEC_CHUNKS
-#define SGA_LMHEAD_DEC_CHUNKS 2
+#define SGA_LMHEAD_DEC_CHUNKS 3
 #endif
 template <int kN>
 constexpr int dec_chunks = kN <= 16 ? SGA_LMHEAD_DEC_CHUNKS_N16 : SGA_LMHEAD_DEC_CHUNKS;
@@ -62,7 +68,7 @@ constexpr int dec_a_bytes = dec_chunks<kN> * dec_halves<kN> * DEC_SUB_BYTES;
 template <int kN>
 constexpr int dec_stage_bytes = dec_a_bytes<kN> + dec_chunks<kN> * kN * ROW_BYTES;
 template <int kN>
-constexpr int dec_stages = (227 * 1024 - 4096) / dec_stage_bytes<kN>;  // 3, 5, 4
+constexpr int dec_stages = (227 * 1024 - 4096) / dec_stage_bytes<kN>;  // 3, 3, 3
 
 template <int kN>
 struct SharedDec {
