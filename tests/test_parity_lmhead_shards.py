@@ -141,3 +141,48 @@ def test_decode_merge_slots_come_back_clean(sga_lib):
         h, w, sh, org, ref = cases[k % len(cases)]
         gh.assert_stats_equal(one_call(sga_lib, h, w, sh, org), ref)
     assert sga_lib.sga_device_error() == 0
+
+
+def test_decode_calls_on_concurrent_streams(sga_lib):
+    # Decode-size calls issued on four streams at once: each call takes its
+    # own merge slot (keys, ticket and tile counter), so calls whose launches
+    # overlap on the GPU must not disturb one another.  Every output is
+    # compared bit for bit with the same call run alone (itself checked
+    # against the oracle on every row).
+    H = 512
+    cases = []
+    for n in range(3):
+        M = [16, 3, 48][n]
+        vocab = 24000 + 1000 * n
+        shards = wl.random_shards(n + 401, vocab, 2 + n)
+        org = vocab - 37 * n
+        hidden = wl.normal_matrix(n + 501, M, H, 1.0)
+        weight = wl.normal_matrix(n + 601, vocab, H, 1.0 / np.sqrt(H))
+        st, v, i = lm.run_gpu(hidden, weight, shards, org)
+        lm.check_rows(np.arange(M), hidden, weight, shards, org, st, v, i)
+        h, w = gh.to_device(hidden), gh.to_device(weight)
+        ws = torch.empty(max(8, sga_lib.sga_lmhead_argmax_shards_workspace(M, shards)),
+                         dtype=torch.uint8, device="cuda")
+        cases.append((h, w, shards, org, ws, st))
+    streams = [torch.cuda.Stream() for _ in range(4)]
+    calls = []
+    for k in range(24):
+        h, w, sh, org, _, ref = cases[k % len(cases)]
+        # each call gets its own (unused at decode sizes) workspace and output,
+        # filled on the default stream before the side streams start
+        ws = torch.empty(max(8, sga_lib.sga_lmhead_argmax_shards_workspace(h.shape[0], sh)),
+                         dtype=torch.uint8, device="cuda")
+        out = torch.full((len(sh) * h.shape[0], 2), -5, dtype=torch.int32, device="cuda")
+        calls.append((h, w, sh, org, ws, out, ref))
+    start = torch.cuda.Event()
+    start.record()
+    for s in streams:
+        s.wait_event(start)
+    for k, (h, w, sh, org, ws, out, _) in enumerate(calls):
+        sga_lib.sga_lmhead_argmax_shards(h, w, sh, org, out, ws, stream=streams[k % len(streams)])
+    for s in streams:
+        torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    assert sga_lib.sga_device_error() == 0
+    for h, w, sh, org, ws, out, ref in calls:
+        gh.assert_stats_equal(gh.stats_to_numpy(out), ref)
