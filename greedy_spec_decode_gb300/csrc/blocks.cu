@@ -128,11 +128,7 @@ constexpr int kUnroll = SGA_BLOCKS_UNROLL;
 #endif
 constexpr int64_t kShortPieceBytes = SGA_BLOCKS_SHORT_PIECE_BYTES;
 
-// Pieces per work item for a block size (host side).  Tuning record: eight
-// 2 KB bonus pieces per item (groups of 4 lanes, every item 16 KB like a
-// draft item) measured slower, 251.9 / 153.1 us against 247.8 / 147.0 us per
-// launch (K_i = 15 / mixed K_i, alternating on one box), with bit-identical
-// statistics.
+// Pieces per work item for a block size (host side).
 inline int32_t group_for(int64_t block_ids, int elt) {
   const int64_t bytes = block_ids * elt;
   return bytes <= kShortPieceBytes ? 4 : (bytes <= 2 * kShortPieceBytes ? 2 : 1);
