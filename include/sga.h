@@ -377,10 +377,11 @@ int sga_lmhead_argmax_fp8(const void *hidden_q, const float *hidden_scale, int64
  * one weight buffer in a single call (one GPU holding the vocab slices of
  * several tensor-parallel ranks), as sga_local_argmax_shards is for the
  * per-shard argmax.  At decode sizes (M <= 64) every shard runs in one
- * launch of the decode-size kernel and one finalize launch, instead of a
- * launch pair per shard; for larger M each shard runs as in
- * sga_lmhead_argmax, one after the other.  The statistics are identical to
- * num_shards sga_lmhead_argmax calls.
+ * launch of the decode-size kernel, whose CTAs merge in library-owned memory
+ * as in sga_lmhead_argmax (same 32-call limit); for 65 <= M <= 128 each shard
+ * runs as in sga_lmhead_argmax, one after the other; from M = 129 every
+ * shard runs in one GEMM launch followed by one finalize launch.  The
+ * statistics are identical to num_shards sga_lmhead_argmax calls.
  * Page: as sga_lmhead_argmax (vLLM PR #62604, Purpose; PR #39419, Changes).
  *
  *   weight        device [rows, H] (bf16), 16-byte aligned; row g -
