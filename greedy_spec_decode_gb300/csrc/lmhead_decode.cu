@@ -272,9 +272,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int n_tiles = tab.tile0[tab.n];
 
   if (SGA_LMHEAD_DEC_PREFETCH && threadIdx.x == 64 && blockIdx.x < n_tiles) {
-    // Warm L2 with what the ring loads first (tile blockIdx.x: the CTAs take
-    // their first tiles in about launch order; one ring's worth of K blocks)
-    // while the previous kernel drains.  A prefetch
+    // Warm L2 with what the ring loads first (the CTA's first tile,
+    // blockIdx.x; one ring's worth of K blocks) while the previous kernel
+    // drains.  A prefetch
     // only moves lines into L2, which stays coherent with any later write, so
     // it may precede griddepcontrol.wait.
     const int n = blockIdx.x;
@@ -328,11 +328,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
-      // Tiles come from the launch's counter one at a time (the next one is
-      // taken while the current one streams) and go to the MMA lane and the
-      // epilogue through the tile queue; they only increase.
+      // The CTA's first tile is its own (blockIdx.x: no round trip before the
+      // first copy, and the tile the L2 prefetch warmed); the others come
+      // from the launch's counter, offset by the grid, one at a time (the
+      // next one is taken while the current one streams).  They go to the
+      // MMA lane and the epilogue through the tile queue and only increase.
       int s = 0;  // the shard of tile n
-      int n = static_cast<int>(atomicAdd(&g_dec_next[slot], 1u));
+      int n = blockIdx.x;
       for (int k = 0; !*abort_flag; ++k) {
         const int q = k % kTileQ;
         if (k >= kTileQ &&
@@ -343,7 +345,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         sh->tile_q[q] = n < n_tiles ? n : -1;
         mbar_arrive(smem_u32(&sh->tile_ready[q]));
         if (n >= n_tiles) break;
-        const int n_next = static_cast<int>(atomicAdd(&g_dec_next[slot], 1u));
+        const int n_next =
+            static_cast<int>(gridDim.x) + static_cast<int>(atomicAdd(&g_dec_next[slot], 1u));
         while (n >= tab.tile0[s + 1]) ++s;
         const int row = tab.row0[s] + (n - tab.tile0[s]) * kTileIds;
         for (int kb = 0; kb < num_kb; kb += kChunks) {
