@@ -69,7 +69,7 @@ def parse_args():
     p.add_argument("--lmhead-per-shard", action="store_true",
                    help="lmhead workloads: one sga_lmhead_argmax call per shard (each "
                         "emulated rank its own) instead of every shard through one "
-                        "sga_lmhead_argmax_shards call (one decode-size launch for M <= 64)")
+                        "sga_lmhead_argmax_shards call (one decode-size launch for M <= 128)")
     p.add_argument("--lmhead-shards", type=int, default=2,
                    help="vocab shards (emulated TP ranks) of the fused LM-head workload")
     p.add_argument("--lmhead-vocab", type=int, default=151936,
@@ -909,30 +909,34 @@ def lmhead_cpu_baseline(c, fp8, gpu_ids, target_seconds):
                   "of the cpu_baseline leg")
 
 
-DECODE_MAX_M = 64   # the library's decode-size LM-head kernel covers M <= 64
+DECODE_MAX_M = 128  # the library's decode-size LM-head kernels cover M <= 128
 
 
 def decode_roofline(weight_bytes, kern_ms, num_shards, fp8, captured_shape=True,
-                    one_call=True):
-    """HBM roofline of the decode-size LM-head kernel: the weight is read once
-    per step (one launch per shard)."""
+                    one_call=True, M=16):
+    """HBM roofline of the decode-size LM-head kernels: the weight is read once
+    per step (one launch per shard).  The committed captures are of M = 16
+    (one CTA per SM) and, for one call, M = 128 (CTA pairs)."""
     pk, pk_src = peaks()
     hbm = float(pk.get("hbm_gbs", FALLBACK_HBM_GBS))
     achieved = weight_bytes / (kern_ms * 1e-3) / 1e9
     # the captures are of the default shape (2 x 75968 ids, H = 4096): one
     # launch for both shards (one call), or one shard per launch
+    pair = M > 64
     key = ("dram_bytes_per_launch_all_shards" if one_call else "dram_bytes_per_launch") + \
-        ("_fp8" if fp8 else "")
+        ("_pair" if pair else "") + ("_fp8" if fp8 else "")
+    captured_shape = captured_shape and (one_call or not pair)
     traffic = ncu_traffic("lmhead_decode.md", ["greedy_spec_decode_gb300/csrc/lmhead_decode.cu",
                                                "greedy_spec_decode_gb300/csrc/tcgen05.cuh",
                                                "greedy_spec_decode_gb300/csrc/common.cuh"], key)
     return {"bound": "hbm",
-            "kernel": "lmhead_argmax_decode_kernel<%s>" % ("fp8" if fp8 else "bf16"),
+            "kernel": "lmhead_argmax_decode_%skernel<%s>" % ("pair_" if pair else "",
+                                                             "fp8" if fp8 else "bf16"),
             "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
             "traffic": traffic if captured_shape else None,
-            "traffic_unit": "DRAM bytes per decode launch (%s), %s M = 16 capture"
+            "traffic_unit": "DRAM bytes per decode launch (%s), %s M = %d capture"
                             % ("every shard" if one_call else "one shard",
-                               "fp8" if fp8 else "bf16"),
+                               "fp8" if fp8 else "bf16", 128 if pair else 16),
             "peak_source": f"{pk_src} hbm_gbs (MEASURED_PEAKS.json copy bandwidth)"
             if pk_src == "measured" else "fallback 6.8 TB/s",
             "bytes_per_step": weight_bytes, "launches_per_step": 1 if one_call else num_shards,
@@ -1111,7 +1115,7 @@ def measure_lmhead(args, fp8, rank, world):
         kern_times = [sum(e[2 * s].elapsed_time(e[2 * s + 1]) for s in range(1 if one_call else S))
                       for e in ev]
         kern_ms = statistics.median(kern_times)
-    # M <= 64 runs the decode-size kernel: a weight stream bound by HBM, not
+    # M <= 128 runs a decode-size kernel: a weight stream bound by HBM, not
     # by the tensor cores (2 M flops per weight element)
     decode = M <= DECODE_MAX_M
     iso_times = None
@@ -1183,7 +1187,7 @@ def measure_lmhead(args, fp8, rank, world):
                       **({"lmhead_argmax_isolated": spread(iso_times)} if decode else {})},
         "roofline": decode_roofline(weight_bytes, statistics.median(iso_times), S, fp8,
                                     S == 2 and H == 4096 and args.lmhead_vocab == 151936,
-                                    one_call)
+                                    one_call, M)
         if decode else
                     {"bound": "tensor",
                      "kernel": "lmhead_argmax_2sm_kernel<fp8>" if fp8 else "lmhead_argmax_2sm_kernel",

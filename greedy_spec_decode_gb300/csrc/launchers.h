@@ -80,8 +80,9 @@ constexpr int kMaxLmShards = 64;
 
 // Fused LM head + argmax of several shards of one weight buffer (row 0 =
 // global id starts[0]; shards ascending): stats of shard s to out[s * M ..];
-// one decode launch and one finalize for M <= 64, else one GEMM + finalize
-// per shard.  Workspace: lmhead_shards_workspace_bytes.
+// one decode launch for M <= 128 (the CTAs merge in-kernel), else one GEMM
+// launch and one finalize for every shard.  Workspace:
+// lmhead_shards_workspace_bytes.
 cudaError_t launch_lmhead_argmax_shards(const void *hidden, int64_t M, int64_t H,
                                         const void *weight, int num_shards,
                                         const int64_t *starts, const int64_t *widths,
@@ -91,7 +92,7 @@ cudaError_t launch_lmhead_argmax_shards(const void *hidden, int64_t M, int64_t H
                                         float w_scale = 1.0f);
 size_t lmhead_shards_workspace_bytes(int64_t M, int num_shards, const int64_t *widths);
 
-// Decode-size LM head (lmhead_decode.cu), M <= 64, over num_shards shards in
+// Decode-size LM head (lmhead_decode.cu), M <= 128, over num_shards shards in
 // one launch: shard s covers global ids [starts[s], starts[s] + valids[s])
 // at weight rows row0s[s] .. (ascending shards).  The CTAs merge their
 // winners in library-owned memory and the last one writes the statistics of

@@ -8,22 +8,22 @@
 // memory: each 128 x 256 logits tile is accumulated in tensor memory and the
 // epilogue keeps a running (max, id) per row.
 //
-// Kernel structure (one CTA per SM, persistent, warp-specialised):
-//   warp 0      TMA producer: A (hidden, 128 x 64) and B (weight, 256 x 64)
-//               bf16 tiles, 128-byte swizzle, into a 4-stage shared ring.
-//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators)
-//               and issues tcgen05.mma (M=128, N=256, K=16) from one lane.
-//   warps 2..5  epilogue: tcgen05.ld of each accumulator row (one TMEM lane
-//               per thread), argmax over the tile's valid columns, partial
-//               stat to the workspace, then release the accumulator so the
-//               MMA of the next tile overlaps this epilogue.
-// Work items are (vocab tile, row tile) with the row tile fastest, so the CTAs
-// running at the same time share weight tiles through L2 and the weight is
-// streamed from HBM about once.  A small second kernel reduces each row's
-// per-tile partials (one warp per row, row-major workspace).
+// Kernel structure (CTA pairs, persistent, warp-specialised; M > 128 rows):
+//   warp 0      TMA producer (both CTAs): its 128 hidden rows and 128 weight
+//               rows of the pair's 256 x 256 tile, 128-byte K blocks,
+//               128-byte swizzle, into a 6-stage shared ring.
+//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators
+//               per CTA); the leader's lane issues tcgen05.mma.cta_group::2
+//               (M = 256, N = 256, K = 16 bf16 / 32 fp8).
+//   warps 2..5  epilogue (both CTAs): tcgen05.ld of each accumulator row (one
+//               TMEM lane per thread), argmax over the tile's valid columns,
+//               then release the accumulator so the MMA of the next tile
+//               overlaps this epilogue; one partial per (shard, row, chunk)
+//               to the workspace.
+// A small second kernel reduces each row's partials (one warp per row).
 //
-// The decode-size kernel (M <= 64, weight as the MMA's 128-row operand) is in
-// lmhead_decode.cu; the PTX and host helpers both use are in tcgen05.cuh.
+// The decode-size kernels (M <= 128, weight as the MMA's 128-row operand) are
+// in lmhead_decode.cu; the PTX and host helpers all use are in tcgen05.cuh.
 //
 // Every mbarrier wait is bounded in time; on expiry the CTA records
 // SGA_DEVERR_TIMEOUT, stops issuing work, waits (bounded) for its own copies
@@ -33,261 +33,14 @@
 namespace sga {
 namespace {
 
-constexpr int BM = 128;          // rows of hidden per tile (TMEM lanes)
-#ifndef SGA_LMHEAD_STAGES
-#define SGA_LMHEAD_STAGES 4
-#endif
-#ifndef SGA_LMHEAD_2SM_MIN_M
-#define SGA_LMHEAD_2SM_MIN_M 129
-#endif
-constexpr int STAGES = SGA_LMHEAD_STAGES;
-constexpr int A_BYTES = BM * ROW_BYTES;   // 16 KB
-constexpr int B_BYTES = BN * ROW_BYTES;   // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 2 * BN;      // double-buffered accumulator
-// At least 120 KB so that one CTA (holding all 512 TMEM columns) runs per SM.
-constexpr int SMEM_NEEDED = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 256 /*barriers*/;
-constexpr int SMEM_BYTES = SMEM_NEEDED > 120 * 1024 ? SMEM_NEEDED : 120 * 1024;
-
-// One MMA of a K step (16 bf16 or 32 fp8 = 32 bytes of each row), M = BM,
-// N = BN, issued by one thread of this CTA.
-template <bool kFp8>
-__device__ __forceinline__ void mma_1sm(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                        uint32_t accumulate) {
-  constexpr uint32_t idesc = instr_desc<kFp8>(BM, BN);
-  if constexpr (kFp8) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  } else {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  }
-}
-
-struct Shared {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
-  uint64_t tmem_full[2];
-  uint64_t tmem_empty[2];
-  uint64_t drain;
-  uint32_t tmem_base;
-  int abort;
-};
-
-__device__ __forceinline__ void raise_abort(Shared *sh, uint32_t *err) {
-  *reinterpret_cast<volatile int *>(&sh->abort) = 1;
-  atomicOr(err, SGA_DEVERR_TIMEOUT);
-}
-
-template <bool kFp8>
-__global__ void __launch_bounds__(THREADS, 1)
-    lmhead_argmax_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                         const __grid_constant__ CUtensorMap tmap_b, int M, int num_kb,
-                         int m_tiles, int n_tiles, int valid, int shard_start,
-                         sga_stat *__restrict__ ws, uint32_t *err) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *base = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t *a_tiles = base;
-  uint8_t *b_tiles = base + STAGES * A_BYTES;
-  Shared *sh = reinterpret_cast<Shared *>(base + STAGES * STAGE_BYTES);
-  const volatile int *abort_flag = &sh->abort;
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&sh->full[s]), 1);
-      mbar_init(smem_u32(&sh->empty[s]), 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&sh->tmem_full[b]), 1);
-      mbar_init(smem_u32(&sh->tmem_empty[b]), 4 * 32);
-    }
-    mbar_init(smem_u32(&sh->drain), 1);
-    sh->abort = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(&sh->tmem_base)),
-                 "r"(TMEM_COLS)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = sh->tmem_base;
-  // launched with programmatic stream serialisation: everything above (barrier
-  // set-up, TMEM allocation) overlaps the previous kernel's tail; inputs and
-  // the workspace are touched only after that kernel has completed
-  pdl_wait();
-  const int total = m_tiles * n_tiles;
-
-  int prod_stage = 0;
-  uint32_t prod_phase = 0;
-  long long issued = 0;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ producer
-      for (int item = blockIdx.x; item < total && !*abort_flag; item += gridDim.x) {
-        const int n = item / m_tiles, m = item % m_tiles;
-        for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(smem_u32(&sh->empty[prod_stage]), prod_phase ^ 1, abort_flag)) {
-            raise_abort(sh, err);
-            break;
-          }
-          const uint32_t full = smem_u32(&sh->full[prod_stage]);
-          mbar_expect_tx(full, STAGE_BYTES);
-          tma_load_2d(smem_u32(a_tiles + prod_stage * A_BYTES), &tmap_a, kb * kBk<kFp8>, m * BM,
-                      full);
-          tma_load_2d(smem_u32(b_tiles + prod_stage * B_BYTES), &tmap_b, kb * kBk<kFp8>, n * BN,
-                      full);
-          ++issued;
-          if (++prod_stage == STAGES) {
-            prod_stage = 0;
-            prod_phase ^= 1;
-          }
-        }
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ----------------------------------------------------------- MMA issuer
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      for (int item = blockIdx.x; item < total && !*abort_flag; item += gridDim.x) {
-        if (!mbar_wait(smem_u32(&sh->tmem_empty[acc]), acc_phase ^ 1, abort_flag)) {
-          raise_abort(sh, err);
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * BN;
-        bool ok = true;
-        for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(smem_u32(&sh->full[stage]), phase, abort_flag)) {
-            raise_abort(sh, err);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t a_desc = smem_desc_sw128(smem_u32(a_tiles + stage * A_BYTES));
-          const uint64_t b_desc = smem_desc_sw128(smem_u32(b_tiles + stage * B_BYTES));
-#pragma unroll
-          for (int kk = 0; kk < ROW_BYTES / 32; ++kk)  // 32 bytes = 2 descriptor units
-            mma_1sm<kFp8>(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, (kb | kk) != 0);
-          mma_commit(smem_u32(&sh->empty[stage]));
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
-        if (!ok) break;
-        mma_commit(smem_u32(&sh->tmem_full[acc]));
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1;
-      }
-    }
-  } else {
-    // ------------------------------------------------------------- epilogue
-    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 belong to this warp
-    const int row_in_tile = quarter * 32 + lane;
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    for (int item = blockIdx.x; item < total; item += gridDim.x) {
-      const int n = item / m_tiles, m = item % m_tiles;
-      bool ok = mbar_wait(smem_u32(&sh->tmem_full[acc]), acc_phase, abort_flag);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) {
-        if (lane == 0) raise_abort(sh, err);
-        break;
-      }
-      tc_fence_after();
-      float best = __int_as_float(0xff800000);
-      int32_t best_id = kNoId;
-      const int col0 = n * BN;
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(taddr + c * 32, r);
-        tmem_ld_wait();
-        const int cbase = col0 + c * 32;
-        if (cbase < valid) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float x = __uint_as_float(r[i]);
-            if (cbase + i < valid && scan_better(x, best)) {
-              best = x;
-              best_id = shard_start + cbase + i;
-            }
-          }
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&sh->tmem_empty[acc]));
-      const int row = m * BM + row_in_tile;
-      if (row < M) {
-        sga_stat st;
-        st.v = best;
-        st.id = best_id;
-        ws[static_cast<size_t>(row) * n_tiles + n] = st;
-      }
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1;
-    }
-  }
-
-  pdl_launch_dependents();
-  __syncthreads();
-  if (*abort_flag) {
-    // Let this CTA's own copies and MMAs land before its shared memory and
-    // tensor memory are released (bounded as well).
-    const int zero = 0;
-    if (warp == 0 && lane == 0) {
-      const long long outstanding = issued < STAGES ? issued : STAGES;
-      for (long long i = 1; i <= outstanding; ++i) {
-        int s = prod_stage - static_cast<int>(i);
-        uint32_t ph = prod_phase;
-        if (s < 0) {
-          s += STAGES;
-          ph ^= 1;
-        }
-        mbar_wait(smem_u32(&sh->full[s]), ph, &zero);
-      }
-    }
-    if (warp == 1 && lane == 0) {
-      mma_commit(smem_u32(&sh->drain));
-      mbar_wait(smem_u32(&sh->drain), 0, &zero);
-    }
-  }
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "r"(TMEM_COLS)
-                 : "memory");
-  }
-}
 
 // ---------------------------------------------------------------------------
-// 2-SM variant (tcgen05 cta_group::2): a cluster of two CTAs computes a
+// 2-SM kernel (tcgen05 cta_group::2): a cluster of two CTAs computes a
 // 256-row x 256-id tile.  Each CTA stages its own 128 rows of hidden and its
 // own 128 weight rows (half of the tile's ids), so per SM the shared-memory
-// stage is 32 KB instead of 48 KB and the L2 traffic per MMA is 2/3 of the
-// 1-SM kernel's; six stages fit.  The even CTA (leader) issues every MMA; the
+// stage is 32 KB instead of the 48 KB a one-CTA 128 x 256 tile needs and the
+// L2 traffic per MMA is 2/3 of it; six stages fit.  The even CTA (leader) issues every MMA; the
 // tile's rows 0..127 accumulate in the leader's TMEM and rows 128..255 in the
 // follower's, all 256 ids in both.
 //   full[s]       leader only: 1 arrival (the leader's expect_tx of the
@@ -315,67 +68,6 @@ struct Shared2 {
   uint32_t tmem_base;
   int abort;
 };
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Address of the same shared variable in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-
-// TMA tile copy into this CTA's shared memory whose completion is counted on
-// an mbarrier that may live in the peer CTA of the pair (cluster address).
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                                 uint32_t bar_cluster) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
-      : "memory");
-}
-
-template <bool kFp8>
-__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t accumulate) {
-  constexpr uint32_t idesc = instr_desc<kFp8>(256, 256);  // M = 256 across the pair
-  if constexpr (kFp8) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  } else {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  }
-}
-
-// Arrive once on `bar` in both CTAs of the pair when the MMAs issued so far
-// have completed.
-__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
-  const uint16_t mask = 0x3;
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(mask)
-      : "memory");
-}
 
 __device__ __forceinline__ void raise_abort2(Shared2 *sh, uint32_t *err) {
   *reinterpret_cast<volatile int *>(&sh->abort) = 1;
@@ -783,28 +475,7 @@ int resident_pairs(int num_sms) {
   return cache[dev];
 }
 
-// 1-SM kernel (65 <= M <= 128) over one shard: one partial per (row, 256-id
-// tile) at ws[row * n_tiles + tile].
-template <bool kFp8>
-cudaError_t launch_gemm_1sm(const void *hidden, int64_t M, int64_t H, const void *weight,
-                            int64_t shard_start, int64_t valid, sga_stat *ws, int n_tiles,
-                            int num_sms, uint32_t *err, cudaStream_t stream) {
-  const int num_kb = static_cast<int>(H / kBk<kFp8>);
-  CUtensorMap map_a, map_b;
-  if (!make_map(&map_a, hidden, M, H, BM, kFp8) || !make_map(&map_b, weight, valid, H, BN, kFp8))
-    return cudaErrorInvalidValue;
-  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(lmhead_argmax_kernel<kFp8>),
-                                SMEM_BYTES, kFp8 ? 3 : 1);
-  if (e != cudaSuccess) return e;
-  const int m_tiles = static_cast<int>((M + BM - 1) / BM);
-  const int total = m_tiles * n_tiles;
-  const int grid = total < num_sms ? total : num_sms;
-  return launch_pdl(lmhead_argmax_kernel<kFp8>, grid, SMEM_BYTES, stream, map_a, map_b,
-                    static_cast<int>(M), num_kb, m_tiles, n_tiles, static_cast<int>(valid),
-                    static_cast<int>(shard_start), ws, err);
-}
-
-// 2-SM kernel (M >= 129) over every shard of the table in one launch; the
+// 2-SM kernel (M > SGA_LMHEAD_DECODE_MAX_M) over every shard of the table in one launch; the
 // weight map spans map_rows rows.  Sets *chunks to the partial slots per
 // (shard, row) (0 when there is no tile: nothing is launched).
 template <bool kFp8>
@@ -875,7 +546,6 @@ size_t lmhead_shards_workspace_bytes(int64_t M, int num_shards, const int64_t *w
     return static_cast<size_t>(num_shards) * static_cast<size_t>(M) * kDecMaxParts *
            sizeof(sga_stat);
   }
-  if (M < SGA_LMHEAD_2SM_MIN_M) return static_cast<size_t>(most_tiles * M) * sizeof(sga_stat);
   const int64_t chunks = all_tiles < kMaxChunks ? all_tiles : kMaxChunks;
   return static_cast<size_t>(num_shards) * static_cast<size_t>(M) *
          static_cast<size_t>(chunks) * sizeof(sga_stat);
@@ -922,7 +592,6 @@ cudaError_t launch_lmhead_argmax_shards(const void *hidden, int64_t M, int64_t H
                                         bool fp8, const float *row_scale, float w_scale) {
   (void)widths;
   sga_stat *ws = static_cast<sga_stat *>(workspace);
-  const size_t row_bytes = static_cast<size_t>(H) * (fp8 ? 1 : 2);
   FinalizeShards fs = {};
   fs.n = num_shards;
   for (int s = 0; s < num_shards; ++s) fs.start[s] = static_cast<int32_t>(starts[s]);
@@ -939,32 +608,6 @@ cudaError_t launch_lmhead_argmax_shards(const void *hidden, int64_t M, int64_t H
     if (e != cudaSuccess || launched) return e;
     // every shard is padding: the finalize with no partials reports them
     return launch_finalize(ws, M, 0, fs, out, row_scale, w_scale, fp8, stream);
-  }
-
-  if (M < SGA_LMHEAD_2SM_MIN_M) {
-    // 1-SM kernel: one GEMM + finalize per shard, the workspace reused (each
-    // launch waits for the previous one before touching it)
-    for (int s = 0; s < num_shards; ++s) {
-      const void *w = static_cast<const char *>(weight) +
-                      static_cast<size_t>(starts[s] - starts[0]) * row_bytes;
-      const int n_tiles = static_cast<int>((valids[s] + BN - 1) / BN);
-      if (n_tiles > 0) {
-        const cudaError_t e =
-            fp8 ? launch_gemm_1sm<true>(hidden, M, H, w, starts[s], valids[s], ws, n_tiles,
-                                        num_sms, err, stream)
-                : launch_gemm_1sm<false>(hidden, M, H, w, starts[s], valids[s], ws, n_tiles,
-                                         num_sms, err, stream);
-        if (e != cudaSuccess) return e;
-      }
-      FinalizeShards one = {};
-      one.n = 1;
-      one.start[0] = fs.start[s];
-      one.cnt[0] = n_tiles;
-      const cudaError_t e =
-          launch_finalize(ws, M, n_tiles, one, out + s * M, row_scale, w_scale, fp8, stream);
-      if (e != cudaSuccess) return e;
-    }
-    return cudaSuccess;
   }
 
   // 2-SM kernel: every shard in one launch, one finalize for all of them

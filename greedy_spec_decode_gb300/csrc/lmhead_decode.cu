@@ -105,6 +105,14 @@ __device__ unsigned int g_dec_ticket[kMergeSlots];
 // memory system serves faster take more (cleared with the slot)
 __device__ unsigned int g_dec_next[kMergeSlots];
 
+// The merge slot of a call: one counter for every decode launch of the
+// process (all kernels and types), so that at most 32 calls in flight never
+// share a slot.
+int take_merge_slot() {
+  static std::atomic<unsigned> next_slot{0};
+  return static_cast<int>(next_slot.fetch_add(1) % kMergeSlots);
+}
+
 // Key of a (value, id) pair whose unsigned order is the argmax order: the
 // high word orders values (NaN above +inf, +0 and -0 equal), the low word
 // (0xffffffff - id) puts the lower id above on equal values.  Key 0 is below
@@ -155,6 +163,42 @@ template <int kN>
 __device__ __forceinline__ void raise_abort_dec(SharedDec<kN> *sh, uint32_t *err) {
   *reinterpret_cast<volatile int *>(&sh->abort) = 1;
   atomicOr(err, SGA_DEVERR_TIMEOUT);
+}
+
+// The end of every decode launch, after the CTA's merges and its barrier:
+// each CTA takes one ticket (also after an abort, so the count always returns
+// to zero) and the last one turns the keys into statistics and clears the
+// slot (keys, tile counter, ticket) for a later launch.  The keys, the tile
+// counter and the ticket are touched by atomics alone, which are performed in
+// L2: every merge of a CTA was performed before its epilogue threads passed
+// their fence, so before the CTA's barrier and its ticket, and the last CTA's
+// exchanges are issued after it has seen every ticket (no further fence
+// needed; each measured at about 0.3 us on the launch's critical path).
+__device__ __forceinline__ void finish_launch(int *is_last, const DecShardTable &tab, int M,
+                                              int slot, sga_stat *__restrict__ out,
+                                              const float *__restrict__ row_scale,
+                                              float w_scale, int scaled) {
+  if (threadIdx.x == 0) *is_last = atomicAdd(&g_dec_ticket[slot], 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (*is_last) {
+    for (int r = threadIdx.x; r < tab.n * M; r += blockDim.x) {
+      const unsigned long long key = atomicExch(&g_dec_keys[slot][r], 0ull);
+      sga_stat st;
+      if (key == 0) {
+        st.v = __int_as_float(0xff800000);  // no element of the shard: its first id, -inf
+        st.id = tab.start[r / M];
+      } else {
+        merge_unkey(key, st.v, st.id);
+        if (scaled) st.v *= (row_scale ? row_scale[r % M] : 1.0f) * w_scale;
+      }
+      out[r] = st;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      atomicExch(&g_dec_next[slot], 0u);
+      atomicExch(&g_dec_ticket[slot], 0u);
+    }
+  }
 }
 
 // One MMA of a K step with M = 128 (weight rows) and N = kN (hidden rows).
@@ -555,34 +599,328 @@ __global__ void __launch_bounds__(THREADS, 1)
                  "r"(kCols)
                  : "memory");
   }
-  // Every CTA takes one ticket (also after an abort, so the count always
-  // returns to zero).  The keys, the tile counter and the ticket are touched
-  // by atomics alone, which are performed in L2: every merge of this CTA was
-  // performed before its epilogue threads passed their fence, so before the
-  // barrier above and before the ticket, and the last CTA's exchanges are
-  // issued after it has seen every ticket (no further fence needed; each
-  // measured at about 0.3 us on the launch's critical path).
-  if (threadIdx.x == 0) sh->is_last = atomicAdd(&g_dec_ticket[slot], 1u) == gridDim.x - 1;
-  __syncthreads();
-  if (sh->is_last) {
-    for (int r = threadIdx.x; r < tab.n * M; r += blockDim.x) {
-      const unsigned long long key = atomicExch(&g_dec_keys[slot][r], 0ull);
-      sga_stat st;
-      if (key == 0) {
-        st.v = __int_as_float(0xff800000);  // no element of the shard: its first id, -inf
-        st.id = tab.start[r / M];
-      } else {
-        merge_unkey(key, st.v, st.id);
-        if (scaled) st.v *= (row_scale ? row_scale[r % M] : 1.0f) * w_scale;
-      }
-      out[r] = st;
+  finish_launch(&sh->is_last, tab, M, slot, out, row_scale, w_scale, scaled);
+}
+
+// ---------------------------------------------------------------------------
+// Pair variant for 65 <= M <= 128 hidden rows (kN = 128): a cluster of two
+// CTAs issues tcgen05.mma.cta_group::2 with M = 256 weight rows (each CTA
+// holds 128 of them, a 256-id tile per pair) and N = kN hidden rows, each CTA
+// holding kN / 2 of those.  A one-CTA kernel at N = 128 must stage as many
+// hidden bytes as weight bytes per stage; split across the pair, a stage is
+// 2 K blocks x (128 weight rows + 64 hidden rows) per CTA, 4 stages.  Each
+// CTA's tensor memory receives its 128 ids x kN hidden rows, so the epilogue
+// is the one-CTA kernel's.  Pair p takes tiles p, p + pairs, ...
+// ---------------------------------------------------------------------------
+#ifndef SGA_LMHEAD_PAIR_CHUNKS
+// K blocks per stage: 2 (4 stages of 256 bytes per weight row); measured
+// against 3 (3 stages, 384 bytes) and 1 (9 stages, 128 bytes), alternating on
+// one box, M = 96 / 128, graph replay: bf16 191.0 / 192.0 us against 191.7 /
+// 192.8 and 190.4 / 191.3; fp8 106.2 / 107.7 against 106.9 / 109.0 and 108.1 /
+// 109.8.  A tile queue fed by the leader (tiles from the launch's counter, as
+// in the one-CTA kernel) was slower: 197.8 - 199.6 us against 195.5 - 197.3
+// (bf16) and 109.5 - 111.0 against 107.5 - 110.0 (fp8), on boxes where the
+// one-SM GEMM kernel it replaces took 205.7 - 206.8 and 116.5 - 117.4 us.
+#define SGA_LMHEAD_PAIR_CHUNKS 2
+#endif
+constexpr int kPairChunks = SGA_LMHEAD_PAIR_CHUNKS;           // K blocks per stage
+constexpr int kPairABytes = kPairChunks * DEC_SUB_BYTES;      // 128 weight rows
+template <int kN>
+constexpr int pair_b_bytes = kPairChunks * (kN / 2) * ROW_BYTES;  // this CTA's hidden rows
+template <int kN>
+constexpr int pair_stage_bytes = kPairABytes + pair_b_bytes<kN>;
+template <int kN>
+constexpr int pair_stages = (227 * 1024 - 4096) / pair_stage_bytes<kN>;
+
+template <int kN>
+struct SharedPair {
+  uint64_t full[pair_stages<kN>];   // leader: both CTAs' copies of a stage landed
+  uint64_t empty[pair_stages<kN>];  // both: the stage's MMAs are done
+  uint64_t tmem_full[2];            // both: an accumulator is complete
+  uint64_t tmem_empty[2];           // leader: the pair's 8 epilogue warps read it
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int is_last;
+  float part_v[4][kN];
+  int32_t part_i[4][kN];
+};
+
+template <int kN>
+constexpr int pair_smem_bytes =
+    1024 + pair_stages<kN> * pair_stage_bytes<kN> + static_cast<int>(sizeof(SharedPair<kN>));
+static_assert(pair_stages<128> >= 3 && pair_smem_bytes<128> <= 227 * 1024,
+              "pair decode ring exceeds shared memory");
+
+template <int kN>
+__device__ __forceinline__ void raise_abort_pair(SharedPair<kN> *sh, uint32_t *err) {
+  *reinterpret_cast<volatile int *>(&sh->abort) = 1;
+  atomicOr(err, SGA_DEVERR_TIMEOUT);
+}
+
+template <bool kFp8, int kN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    lmhead_argmax_decode_pair_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                                     const __grid_constant__ CUtensorMap tmap_h, int M,
+                                     int num_kb, const __grid_constant__ DecShardTable tab,
+                                     int slot, sga_stat *__restrict__ out,
+                                     const float *__restrict__ row_scale, float w_scale,
+                                     int scaled, uint32_t *err) {
+  constexpr int kStages = pair_stages<kN>;
+  constexpr int kStageBytes = pair_stage_bytes<kN>;
+  constexpr int kChunks = kPairChunks;
+  constexpr int kHalfN = kN / 2;           // hidden rows in each CTA's B half
+  constexpr int kTileIds = 256;            // 128 weight rows per CTA
+  constexpr int kCols = 2 * kN;            // two accumulator buffers
+  constexpr int kG = 32;                   // rows per butterfly group
+  constexpr int kSlots = kN / kG;          // groups (rows held per lane)
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *base = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  SharedPair<kN> *sh = reinterpret_cast<SharedPair<kN> *>(base + kStages * kStageBytes);
+  const volatile int *abort_flag = &sh->abort;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int pair = static_cast<int>(blockIdx.x >> 1);
+  const int num_pairs = static_cast<int>(gridDim.x >> 1);
+  const int n_tiles = tab.tile0[tab.n];
+
+  if (SGA_LMHEAD_DEC_PREFETCH && threadIdx.x == 64 && pair < n_tiles) {
+    // warm L2 with this CTA's rows of its first tile (one ring of K blocks)
+    int s = 0;
+    while (pair >= tab.tile0[s + 1]) ++s;
+    const int row = tab.row0[s] + (pair - tab.tile0[s]) * kTileIds + static_cast<int>(rank) * 128;
+    for (int kb = 0; kb < num_kb && kb < kStages * kChunks; ++kb)
+      tma_prefetch_2d(&tmap_w, kb * kBk<kFp8>, row);
+  }
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&sh->full[s]), 1);
+      mbar_init(smem_u32(&sh->empty[s]), 1);
     }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      atomicExch(&g_dec_next[slot], 0u);
-      atomicExch(&g_dec_ticket[slot], 0u);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&sh->tmem_full[b]), 1);
+      mbar_init(smem_u32(&sh->tmem_empty[b]), 8);
+    }
+    mbar_init(smem_u32(&sh->drain), 1);
+    sh->abort = 0;
+    sh->is_last = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&sh->tmem_base)),
+                 "r"(kCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+  tc_fence_after();
+  const uint32_t tmem_base = sh->tmem_base;
+  pdl_wait();
+
+  int prod_stage = 0;
+  uint32_t prod_phase = 0;
+  long long issued = 0;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------- producer (both CTAs)
+    int s = 0;
+    for (int n = pair; n < n_tiles && !*abort_flag; n += num_pairs) {
+      while (n >= tab.tile0[s + 1]) ++s;
+      const int row =
+          tab.row0[s] + (n - tab.tile0[s]) * kTileIds + static_cast<int>(rank) * 128;
+      for (int kb = 0; kb < num_kb; kb += kChunks) {
+        if (!mbar_wait(smem_u32(&sh->empty[prod_stage]), prod_phase ^ 1, abort_flag)) {
+          raise_abort_pair(sh, err);
+          break;
+        }
+        const int chunks = num_kb - kb < kChunks ? num_kb - kb : kChunks;
+        const uint32_t full_leader = map_to_rank(smem_u32(&sh->full[prod_stage]), 0);
+        const uint32_t stage_addr = smem_u32(base + prod_stage * kStageBytes);
+        // the leader's barrier counts the bytes of both CTAs
+        if (leader)
+          mbar_expect_tx(smem_u32(&sh->full[prod_stage]),
+                         2 * chunks * (DEC_SUB_BYTES + kHalfN * ROW_BYTES));
+        for (int c = 0; c < chunks; ++c) {
+          tma_load_2d_pair(stage_addr + c * DEC_SUB_BYTES, &tmap_w, (kb + c) * kBk<kFp8>, row,
+                           full_leader);
+          tma_load_2d_pair(stage_addr + kPairABytes + c * kHalfN * ROW_BYTES, &tmap_h,
+                           (kb + c) * kBk<kFp8>, static_cast<int>(rank) * kHalfN, full_leader);
+        }
+        ++issued;
+        if (++prod_stage == kStages) {
+          prod_stage = 0;
+          prod_phase ^= 1;
+        }
+      }
+    }
+  } else if (warp == 1 && lane == 0 && leader) {
+    // -------------------------------------------------- MMA issuer (leader)
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    for (int n = pair; n < n_tiles && !*abort_flag; n += num_pairs) {
+      if (!mbar_wait(smem_u32(&sh->tmem_empty[acc]), acc_phase ^ 1, abort_flag)) {
+        raise_abort_pair(sh, err);
+        break;
+      }
+      tc_fence_after();
+      bool ok = true;
+      for (int kb = 0; kb < num_kb; kb += kChunks) {
+        if (!mbar_wait(smem_u32(&sh->full[stage]), phase, abort_flag)) {
+          raise_abort_pair(sh, err);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int chunks = num_kb - kb < kChunks ? num_kb - kb : kChunks;
+        const uint32_t stage_addr = smem_u32(base + stage * kStageBytes);
+        for (int c = 0; c < chunks; ++c) {
+          const uint64_t a_desc = smem_desc_sw128(stage_addr + c * DEC_SUB_BYTES);
+          const uint64_t b_desc = smem_desc_sw128(stage_addr + kPairABytes + c * kHalfN * ROW_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < ROW_BYTES / 32; ++kk)  // 32 bytes = 2 descriptor units
+            mma_pair<kFp8, kN>(tmem_base + acc * kN, a_desc + 2 * kk, b_desc + 2 * kk,
+                               (kb | c | kk) != 0);
+        }
+        mma_commit_pair(smem_u32(&sh->empty[stage]));
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+      mma_commit_pair(smem_u32(&sh->tmem_full[acc]));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------- epilogue (both CTAs)
+    // As in the one-CTA kernel: TMEM lane = this CTA's weight row (vocab id),
+    // column = hidden row; every warp flushes every shard exactly once, in
+    // order, also after an abort, so the 128-thread barriers always match.
+    const int quarter = warp & 3;
+    const int e = static_cast<int>(threadIdx.x) - 64;  // epilogue thread 0 .. 127
+    const uint32_t empty_leader[2] = {map_to_rank(smem_u32(&sh->tmem_empty[0]), 0),
+                                      map_to_rank(smem_u32(&sh->tmem_empty[1]), 0)};
+    float rv[kSlots];
+    int32_t ri[kSlots];
+#pragma unroll
+    for (int g = 0; g < kSlots; ++g) {
+      rv[g] = __int_as_float(0xff800000);
+      ri[g] = kNoId;
+    }
+    auto flush = [&](int s) {
+#pragma unroll
+      for (int g = 0; g < kSlots; ++g) {
+        const int j = g * kG + lane;  // lane l holds row l of group g
+        sh->part_v[quarter][j] = rv[g];
+        sh->part_i[quarter][j] = ri[g];
+        rv[g] = __int_as_float(0xff800000);
+        ri[g] = kNoId;
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (e < M) {
+        float v = sh->part_v[0][e];
+        int32_t id = sh->part_i[0][e];
+#pragma unroll
+        for (int q = 1; q < 4; ++q) keep_better(v, id, sh->part_v[q][e], sh->part_i[q][e]);
+        if (id != kNoId) atomicMax(&g_dec_keys[slot][s * M + e], merge_key(v, id));
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");  // before the next flush's writes
+    };
+    int cur = 0;  // the shard whose bests rv / ri hold
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int n = pair; n < n_tiles; n += num_pairs) {
+      while (n >= tab.tile0[cur + 1]) flush(cur++);
+      bool ok = mbar_wait(smem_u32(&sh->tmem_full[acc]), acc_phase, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        if (lane == 0) raise_abort_pair(sh, err);
+        break;
+      }
+      tc_fence_after();
+      const int local = (n - tab.tile0[cur]) * kTileIds + static_cast<int>(rank) * 128 +
+                        quarter * 32 + lane;  // shard-local id of this lane
+      const bool live = local < tab.valid[cur];
+      const int32_t id = live ? tab.start[cur] + local : kNoId;
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kN;
+#pragma unroll
+      for (int g = 0; g < kSlots; ++g) {
+        uint32_t r[kG];
+        tmem_ld_cols<kG>(taddr + g * kG, r);
+        tmem_ld_wait();
+        float x[kG];
+#pragma unroll
+        for (int k = 0; k < kG; ++k)
+          x[k] = live ? __uint_as_float(r[k]) : __int_as_float(0xff800000);
+        float v;
+        int32_t i;
+        rows_argmax<kG>(x, id, lane, v, i);
+        keep_better(rv[g], ri[g], v, i);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (leader)
+          mbar_arrive(smem_u32(&sh->tmem_empty[acc]));
+        else
+          mbar_arrive_remote(empty_leader[acc]);
+      }
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+    while (cur < tab.n) flush(cur++);
+    __threadfence();  // this CTA's merges before its ticket
+  }
+
+  pdl_launch_dependents();
+  __syncthreads();
+  if (*abort_flag) {
+    const int zero = 0;
+    if (warp == 0 && lane == 0) {
+      if (leader) {
+        // the leader's full barriers count the copies of both CTAs
+        const long long outstanding = issued < kStages ? issued : kStages;
+        for (long long i = 1; i <= outstanding; ++i) {
+          int s = prod_stage - static_cast<int>(i);
+          uint32_t ph = prod_phase;
+          if (s < 0) {
+            s += kStages;
+            ph ^= 1;
+          }
+          mbar_wait(smem_u32(&sh->full[s]), ph, &zero);
+        }
+      } else if (issued > 0) {
+        // the follower's copies complete on the leader's barriers, which it
+        // cannot wait on: give them a bounded 1 ms to land
+        const unsigned long long t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 1000000ull) {
+        }
+      }
+    }
+    if (warp == 1 && lane == 0 && leader) {
+      mma_commit_pair(smem_u32(&sh->drain));
+      mbar_wait(smem_u32(&sh->drain), 0, &zero);
     }
   }
+  // the peer may still read this CTA's shared memory or write its TMEM
+  tc_fence_before();
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(kCols)
+                 : "memory");
+  }
+  finish_launch(&sh->is_last, tab, M, slot, out, row_scale, w_scale, scaled);
 }
 
 template <bool kFp8, int kN>
@@ -615,12 +953,48 @@ cudaError_t launch_decode(const void *hidden, int64_t M, int64_t H, const void *
   const int slot = 4 + (kFp8 ? 4 : 0) + (kN == 16 ? 0 : kN == 32 ? 1 : kN == 64 ? 2 : 3);
   cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), dec_smem_bytes<kN>, slot);
   if (e != cudaSuccess) return e;
-  // a merge slot per call, in turn (see g_dec_keys)
-  static std::atomic<unsigned> next_slot{0};
-  const int merge_slot = static_cast<int>(next_slot.fetch_add(1) % kMergeSlots);
+  const int merge_slot = take_merge_slot();
   return launch_pdl(kern, grid, dec_smem_bytes<kN>, stream, map_w, map_h, static_cast<int>(M),
                     static_cast<int>(H / kBk<kFp8>), tab, merge_slot, out, row_scale, w_scale,
                     kFp8 ? 1 : 0, err);
+}
+
+template <bool kFp8, int kN>
+cudaError_t launch_decode_pair(const void *hidden, int64_t M, int64_t H, const void *weight,
+                               int num_shards, const int64_t *starts, const int64_t *row0s,
+                               const int64_t *valids, sga_stat *out, const float *row_scale,
+                               float w_scale, int num_sms, uint32_t *err, cudaStream_t stream,
+                               bool *launched) {
+  constexpr int kTileIds = 256;  // per CTA pair
+  DecShardTable tab = {};
+  tab.n = num_shards;
+  int64_t map_rows = 0;
+  for (int s = 0; s < num_shards; ++s) {
+    tab.start[s] = static_cast<int32_t>(starts[s]);
+    tab.row0[s] = static_cast<int32_t>(row0s[s]);
+    tab.valid[s] = static_cast<int32_t>(valids[s]);
+    tab.tile0[s + 1] = tab.tile0[s] + static_cast<int32_t>((valids[s] + kTileIds - 1) / kTileIds);
+    if (valids[s] > 0 && row0s[s] + valids[s] > map_rows) map_rows = row0s[s] + valids[s];
+  }
+  const int n_tiles = tab.tile0[num_shards];
+  // one pair per two SMs, at most one per tile
+  int pairs = num_sms / 2;
+  if (pairs > n_tiles) pairs = n_tiles;
+  if (pairs > kDecMaxParts / 2) pairs = kDecMaxParts / 2;
+  *launched = pairs > 0;
+  if (pairs == 0) return cudaSuccess;  // every shard is padding: the caller reports it
+  CUtensorMap map_w, map_h;
+  if (!make_map(&map_w, weight, map_rows, H, 128, kFp8) ||
+      !make_map(&map_h, hidden, M, H, kN / 2, kFp8))
+    return cudaErrorInvalidValue;
+  auto kern = lmhead_argmax_decode_pair_kernel<kFp8, kN>;
+  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(kern), pair_smem_bytes<kN>,
+                                12 + (kFp8 ? 1 : 0));
+  if (e != cudaSuccess) return e;
+  const int merge_slot = take_merge_slot();
+  return launch_pdl(kern, 2 * pairs, pair_smem_bytes<kN>, stream, map_w, map_h,
+                    static_cast<int>(M), static_cast<int>(H / kBk<kFp8>), tab, merge_slot, out,
+                    row_scale, w_scale, kFp8 ? 1 : 0, err);
 }
 
 }  // namespace
@@ -635,8 +1009,15 @@ cudaError_t launch_lmhead_decode(bool fp8, const void *hidden, int64_t M, int64_
                       w_scale, num_sms, err, stream, launched)
   if (M <= 16) return fp8 ? SGA_DEC_LAUNCH(true, 16) : SGA_DEC_LAUNCH(false, 16);
   if (M <= 32) return fp8 ? SGA_DEC_LAUNCH(true, 32) : SGA_DEC_LAUNCH(false, 32);
-  return fp8 ? SGA_DEC_LAUNCH(true, 64) : SGA_DEC_LAUNCH(false, 64);
+  if (M <= kDecSingleMaxM) return fp8 ? SGA_DEC_LAUNCH(true, 64) : SGA_DEC_LAUNCH(false, 64);
 #undef SGA_DEC_LAUNCH
+  // 65 <= M <= 128: CTA pairs
+  return fp8 ? launch_decode_pair<true, 128>(hidden, M, H, weight, num_shards, starts, row0s,
+                                             valids, out, row_scale, w_scale, num_sms, err,
+                                             stream, launched)
+             : launch_decode_pair<false, 128>(hidden, M, H, weight, num_shards, starts, row0s,
+                                              valids, out, row_scale, w_scale, num_sms, err,
+                                              stream, launched);
 }
 
 }  // namespace sga

@@ -24,12 +24,16 @@ constexpr int kBk = kFp8 ? 128 : 64;
 constexpr int THREADS = 192;           // 6 warps per CTA in every LM-head kernel
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 #ifndef SGA_LMHEAD_DECODE_MAX_M
-// Swapped-operand decode kernel for M <= this (0: off; at most 64).  Measured:
-// an N = 128 variant for M = 65..128 was slower than the 1-SM kernel (graph
-// replay, 2 shards: M = 128 bf16 210 vs 201 us, fp8 122 vs 114 us).
-#define SGA_LMHEAD_DECODE_MAX_M 64
+// Swapped-operand decode kernels for M <= this (0: off; at most 128): one CTA
+// per SM up to M = 64, CTA pairs (cta_group::2, the hidden rows split between
+// the two CTAs) for M = 65..128.  Measured: a one-CTA N = 128 variant for M =
+// 65..128 was slower than the 1-SM GEMM kernel (graph replay, 2 shards: M =
+// 128 bf16 210 vs 201 us, fp8 122 vs 114 us): its stages held as many hidden
+// bytes as weight bytes.
+#define SGA_LMHEAD_DECODE_MAX_M 128
 #endif
-static_assert(SGA_LMHEAD_DECODE_MAX_M <= 64, "the decode kernel holds at most 64 hidden rows");
+static_assert(SGA_LMHEAD_DECODE_MAX_M <= 128, "the decode kernels hold at most 128 hidden rows");
+constexpr int kDecSingleMaxM = 64;  // one CTA per SM up to this M, CTA pairs above
 constexpr int kDecMaxParts = 256;  // CTAs (partials per row) of one decode launch, at most
 
 // ---------------------------------------------------------------- PTX helpers
@@ -189,12 +193,79 @@ bool make_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, int
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// ------------------------------------------------- CTA-pair (cta_group::2)
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address of the same shared variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+// TMA tile copy into this CTA's shared memory whose completion is counted on
+// an mbarrier that may live in the peer CTA of the pair (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                                 uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+      : "memory");
+}
+
+// One tcgen05.mma over the CTA pair: M = 256 rows of A (128 in each CTA's
+// shared memory), N columns of B (N / 2 rows in each CTA), issued by the
+// leader; each CTA's tensor memory receives its 128 rows x N columns.
+template <bool kFp8, int kN = 256>
+__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t accumulate) {
+  static_assert(kN % 16 == 0 && kN >= 32 && kN <= 256, "N of a pair MMA");
+  constexpr uint32_t idesc = instr_desc<kFp8>(256, kN);  // M = 256 across the pair
+  if constexpr (kFp8) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
+}
+
+// Arrive once on `bar` in both CTAs of the pair when the MMAs issued so far
+// have completed.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+  const uint16_t mask = 0x3;
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
 // Raise a kernel's dynamic shared-memory limit once per device and context
 // (slot picks the kernel), so that later calls, including calls inside a
 // stream capture, make no function-attribute call.
 cudaError_t set_smem_once(const void *kernel, int bytes, int slot) {
   static std::mutex mu;
-  static uintptr_t done_ctx[12][64] = {};
+  static uintptr_t done_ctx[16][64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

@@ -330,8 +330,9 @@ int sga_greedy_verify_prefill(const sga_stat *stats, int num_shards, int num_req
  *   workspace     device, >= sga_lmhead_argmax_workspace(M, shard_width)
  *                 bytes, 8-byte aligned; holds partial statistics.
  *                 Contents on entry are ignored; the caller must not use it
- *                 concurrently from two calls.  Unused for M <= 64.
- * Decode sizes (M <= 64): one kernel launch, whose CTAs merge their per-row
+ *                 concurrently from two calls.  Unused for M <= 128.
+ * Decode sizes (M <= 128; one CTA per SM up to M = 64, CTA pairs above):
+ * one kernel launch, whose CTAs merge their per-row
  * winners in library-owned device memory (32 merge slots per device, one
  * taken per call in turn; the last CTA writes out_stats and clears the
  * slot).  Calls whose kernels overlap on the GPU must not share a slot: at
@@ -376,12 +377,11 @@ int sga_lmhead_argmax_fp8(const void *hidden_q, const float *hidden_scale, int64
  * sga_lmhead_argmax_shards -- sga_lmhead_argmax for several vocab shards of
  * one weight buffer in a single call (one GPU holding the vocab slices of
  * several tensor-parallel ranks), as sga_local_argmax_shards is for the
- * per-shard argmax.  At decode sizes (M <= 64) every shard runs in one
- * launch of the decode-size kernel, whose CTAs merge in library-owned memory
- * as in sga_lmhead_argmax (same 32-call limit); for 65 <= M <= 128 each shard
- * runs as in sga_lmhead_argmax, one after the other; from M = 129 every
- * shard runs in one GEMM launch followed by one finalize launch.  The
- * statistics are identical to num_shards sga_lmhead_argmax calls.
+ * per-shard argmax.  At decode sizes (M <= 128) every shard runs in one
+ * launch of a decode-size kernel, whose CTAs merge in library-owned memory
+ * as in sga_lmhead_argmax (same 32-call limit); from M = 129 every shard
+ * runs in one GEMM launch followed by one finalize launch.  The statistics
+ * are identical to num_shards sga_lmhead_argmax calls.
  * Page: as sga_lmhead_argmax (vLLM PR #62604, Purpose; PR #39419, Changes).
  *
  *   weight        device [rows, H] (bf16), 16-byte aligned; row g -
@@ -435,7 +435,7 @@ int sga_lmhead_argmax_shards_fp8(const void *hidden_q, const float *hidden_scale
  *   Limit: sga_lmhead_argmax_workspace(M, shard_width) must not exceed
  *          SGA_LMHEAD_NOALLOC_SCRATCH_BYTES (M * P * 8 bytes, P partials per
  *          row: for M >= 129 P = min(ceil(shard_width / 256), 128); for
- *          65 <= M <= 128 P = ceil(shard_width / 256); for M <= 64 P =
+ *          M <= 128, where the scratch is not used, P =
  *          max(ceil(shard_width / 256), min(ceil(shard_width / 128), 256)));
  *          larger calls return SGA_ERR_WORKSPACE and enqueue nothing.
  *   Set-up: the first call on a device looks up the device address of the

@@ -106,8 +106,8 @@ def test_lmhead_shards_validation(sga_lib):
     # chunk), at most min(128, tiles of all shards) chunks
     assert wsf(512, 2, arr([75968, 1000])) == 2 * 512 * 128 * 8
     assert wsf(512, 2, arr([256, 300])) == 2 * 512 * 3 * 8          # 1 + 2 tiles
-    # 65 <= M <= 128: one 1-SM launch per shard, the workspace of the widest
-    assert wsf(100, 2, arr([75968, 1000])) == L.sga_lmhead_argmax_workspace(100, 75968)
+    # 65 <= M <= 128: decode sizes too (one CTA-pair launch), sized as below 65
+    assert wsf(100, 2, arr([75968, 1000])) == 2 * 100 * 256 * 8
     assert L.sga_lmhead_argmax_workspace(100, 75968) == 100 * 297 * 8
     assert L.sga_lmhead_argmax_workspace(512, 75968) == 512 * 128 * 8
     assert wsf(16, 0, arr([1])) == 0 and wsf(16, 65, None) == 0 and wsf(16, 1, arr([0])) == 0

@@ -82,6 +82,6 @@ def test_lmhead_decode_line():
     d = run_bench("--workload", "lmhead", "--lmhead-rows", "4", "--lmhead-vocab", "32768",
                   "--steps", "5", "--warmup", "3", "--e2e-steps", "1", "--cpu-seconds", "1")
     check_common(d, "rows/s")
-    assert d["roofline"]["bound"] == "hbm"            # M <= 64: the decode-size kernel
+    assert d["roofline"]["bound"] == "hbm"            # M <= 128: a decode-size kernel
     assert d["roofline"]["traffic"] is None           # not the captured shape
     assert "tolerance" in d["parity"]

@@ -93,11 +93,13 @@ def test_small_shapes(sga_lib, M, H, vocab, num_shards):
         check_rows(np.arange(M), hidden, weight, shards, org, st, v, i)
 
 
-@pytest.mark.parametrize("M", [1, 2, 15, 16, 17, 31, 32, 33, 48, 63, 64, 65])
+@pytest.mark.parametrize("M", [1, 2, 15, 16, 17, 31, 32, 33, 48, 63, 64, 65, 96, 127, 128, 129])
 def test_decode_sizes_around_kernel_boundaries(sga_lib, M):
     # M <= 64 runs the swapped-operand decode kernel with N = 16, 32 or 64
-    # hidden columns; 65 is the first size of the 1-SM kernel.  A ragged
-    # vocab (not a multiple of 128 or 256), 3 uneven shards, and padding.
+    # hidden columns; 65..128 its CTA-pair form (N = 128, 64 hidden rows in
+    # each CTA of the pair); 129 is the first size of the 2-SM GEMM kernel.
+    # A ragged vocab (not a multiple of 128 or 256), 3 uneven shards, and
+    # padding.
     H, vocab = 256, 4099
     hidden = wl.normal_matrix(900 + M, M, H, 1.0)
     weight = wl.normal_matrix(901 + M, vocab, H, 1.0 / np.sqrt(H))
@@ -127,11 +129,11 @@ def test_decode_size_vocab_narrower_than_a_tile(sga_lib):
     check_rows(np.arange(M), hidden, weight, [(0, vocab)], vocab, st, v, i)
 
 
-@pytest.mark.parametrize("M", [130, 40, 20, 5])
+@pytest.mark.parametrize("M", [130, 100, 40, 20, 5])
 def test_all_padding_shard_and_exact_one_hot(sga_lib, M):
     # one-hot weights: logit[r][j] = hidden[r][perm[j]] exactly, so ties and
-    # values are exact and the id must follow torch.argmax order (M <= 64:
-    # decode kernel, where ties are resolved across lanes, warps and CTAs)
+    # values are exact and the id must follow torch.argmax order (M <= 128:
+    # decode kernels, where ties are resolved across lanes, warps and CTAs)
     H, vocab = 128, 600
     hidden = wl.normal_matrix(7, M, H, 1.0)
     perm = np.random.default_rng(1).integers(0, H, vocab)

@@ -78,8 +78,9 @@ def make(M, H, vocab, seed):
 @pytest.mark.parametrize("M,H,vocab,num_shards", [
     (1, 128, 300, 1), (100, 256, 1000, 2), (128, 512, 5000, 3), (300, 256, 2311, 4),
     (513, 1024, 4099, 2), (16, 4096, 20000, 2),
-    # decode kernel with 16, 32 and 64 hidden columns
+    # decode kernel with 16, 32 and 64 hidden columns, and its CTA-pair form
     (7, 256, 3001, 3), (33, 512, 3001, 2), (64, 256, 1000, 3), (5, 384, 2000, 2),
+    (65, 384, 3001, 3), (127, 128, 4099, 2),
 ])
 def test_small_shapes(sga_lib, M, H, vocab, num_shards):
     hq, hs, wq, w_scale = make(M, H, vocab, M + H + vocab)

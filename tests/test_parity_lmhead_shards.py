@@ -36,7 +36,7 @@ def one_call(sga, h, w, shards, org_vocab, fp8=False, hs=None, w_scale=1.0):
     return gh.stats_to_numpy(stats)
 
 
-@pytest.mark.parametrize("M", [1, 7, 16, 17, 32, 33, 64, 65, 200, 513])
+@pytest.mark.parametrize("M", [1, 7, 16, 17, 32, 33, 64, 65, 96, 128, 200, 513])
 @pytest.mark.parametrize("layout", ["uneven3", "gap", "padded", "eight", "single"])
 def test_bf16_one_call_equals_per_shard_calls(sga_lib, M, layout):
     H = 256

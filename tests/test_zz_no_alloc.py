@@ -8,9 +8,9 @@ synchronise the device.  For them the library keeps the partial statistics in
 a fixed scratch array of its own.
 
 The test calls that entry point through the C ABI on several shapes in a row
--- 2-SM GEMM sizes first, then decode sizes (M <= 64, whose kernel keeps one
-partial per CTA, more partials per row than 256-id tiles) -- so that each
-call finds the previous call's leftovers in the shared scratch.  Each result
+-- 2-SM GEMM sizes first, then decode sizes (M <= 128, whose kernels merge
+in library-owned memory and leave the scratch alone) -- so that each call
+finds the previous call's leftovers in the shared scratch.  Each result
 must equal the workspace entry point sga_lmhead_argmax bit for bit (the same
 kernels run), and must agree with the CPU oracle's fp64 logits under the
 LM-head tolerance (ids equal where the oracle's top-1 minus top-2 exceeds
@@ -33,8 +33,10 @@ pytestmark = pytest.mark.gpu
 GAP, REL, ABS = 1e-2, 1e-2, 1e-3
 
 # (M, H, shard width, shard start, org_vocab): 2-SM GEMM sizes, then decode sizes
+# (one CTA per SM up to M = 64, CTA pairs above)
 CASES = [(300, 256, 3000, 1200, 2950), (200, 512, 1500, 0, 1500),
-         (16, 256, 2000, 512, 2500), (1, 128, 700, 0, 650), (64, 256, 5000, 100, 5100)]
+         (16, 256, 2000, 512, 2500), (1, 128, 700, 0, 650), (64, 256, 5000, 100, 5100),
+         (100, 256, 3000, 640, 3500)]
 
 
 def _dev(bits):
