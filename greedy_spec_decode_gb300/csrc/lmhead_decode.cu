@@ -1,11 +1,11 @@
 // lmhead_decode.cu -- fused LM head + per-shard argmax at decode sizes
-// (M <= 64 hidden rows) on the tcgen05 tensor cores, with the weight as the
-// MMA's 128-row operand.
+// (M <= 128 hidden rows: one CTA per SM up to M = 64, CTA pairs above) on the
+// tcgen05 tensor cores, with the weight as the MMA's 128-row operand.
 //
 // vLLM PR #62604, Purpose (vocab-parallel LM head) and item 2 (fused
 // get_top_tokens); vLLM PR #39419, Changes (lm_head on the hidden states,
 // then the local argmax).  At decode sizes the step is a weight stream, so
-// this kernel is shaped for HBM, not for the tensor pipe.
+// these kernels are shaped for HBM, not for the tensor pipe.
 #include <atomic>
 
 #include "tcgen05.cuh"
@@ -14,7 +14,7 @@ namespace sga {
 namespace {
 
 // ---------------------------------------------------------------------------
-// Decode-size variant (M <= 64 hidden rows): the operands swap roles.  The
+// One-CTA decode kernel (M <= 64 hidden rows): the operands swap roles.  The
 // weight tile is the MMA's A operand (M = 128 vocab ids per MMA, two MMAs per
 // 256-id tile) and the hidden rows are its B operand (N = kN = 16, 32 or 64
 // columns).  A stage then holds 32-64 KB of weight and only kN x 128 B of
