@@ -726,15 +726,21 @@ def run_ours_verify(args, blocks=None):
 def add_extra_records(line, args, rank, world):
     """The other configurations of the metric, each as a nested record of the
     default line: the fused LM head (512 x 4096 . [151936 x 4096]^T bf16, 2
-    shards; tensor roofline) and the two L2-resident latency workloads (draft
-    get_top_tokens, small greedy verify)."""
+    shards; tensor roofline), the same head at a decode size (16 rows, bf16
+    and fp8, the step replayed from a CUDA graph; HBM roofline) and the two
+    L2-resident latency workloads (draft get_top_tokens, small greedy
+    verify)."""
     import argparse as ap
     sub = ap.Namespace(**vars(args))
     sub.graph, sub.lmhead_per_shard, sub.e2e_steps = False, False, 5
     sub.lmhead_rows, sub.lmhead_vocab, sub.lmhead_shards = 512, 151936, 2
     sub.steps, sub.warmup, sub.cpu_seconds = 100, 5, min(args.cpu_seconds, 6.0)
     line["lmhead"] = measure_lmhead(sub, False, rank, world)
-    sub.steps, sub.cpu_seconds = 200, min(args.cpu_seconds, 2.0)
+    sub.graph, sub.lmhead_rows, sub.steps, sub.cpu_seconds = True, 16, 200, min(args.cpu_seconds,
+                                                                                  3.0)
+    line["lmhead_decode"] = measure_lmhead(sub, False, rank, world)
+    line["lmhead_decode_fp8"] = measure_lmhead(sub, True, rank, world)
+    sub.graph, sub.steps, sub.cpu_seconds = False, 200, min(args.cpu_seconds, 2.0)
     line["draft_top_tokens"] = measure_small(sub, wl.draft_top_tokens, rank, world)
     line["greedy_verify_small"] = measure_small(sub, wl.greedy_verify_small, rank, world)
 

@@ -58,6 +58,12 @@ def test_large_verify_line_with_oracle_leg_and_nested_records():
     assert lm["roofline"]["bound"] == "tensor" and lm["roofline"]["unit"] == "TFLOP/s"
     assert lm["config"]["M"] == 512 and lm["config"]["shards"] == [75968, 75968]
     assert lm["cpu_baseline"]["kind"] == "oracle" and "tolerance" in lm["parity"]
+    for key in ("lmhead_decode", "lmhead_decode_fp8"):
+        dec = d[key]
+        check_common(dec, "rows/s")
+        assert dec["config"]["M"] == 16 and dec["roofline"]["bound"] == "hbm"
+        assert dec["kernel_us"]["lmhead_argmax_isolated"]["launches"] >= 20
+        assert "tolerance" in dec["parity"]
     for key in ("draft_top_tokens", "greedy_verify_small"):
         check_common(d[key], "rows/s")
         assert "bit-exact" in d[key]["parity"]
