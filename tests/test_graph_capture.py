@@ -5,8 +5,9 @@ benchmarks run vLLM with full CUDA graphs, vLLM PR #34049 Test Plan).  The
 entry points enqueue kernels only (no synchronisation, no allocation), so a
 step can be captured once and replayed on new inputs copied into the same
 buffers.  These tests capture (a) the one-launch shard argmax + fused verify
-and (b) the fused LM-head argmax of two shards + shard reduce, replay them on
-fresh inputs and check parity with the oracle.
+and (b) the fused LM-head argmax of two shards + shard reduce (at a GEMM size
+and at both decode sizes), replay them on fresh inputs and check parity with
+the oracle.
 """
 import numpy as np
 import pytest
@@ -67,8 +68,9 @@ def test_captured_verify_step_replays_on_new_inputs(sga_lib):
     assert sga_lib.sga_device_error() == 0
 
 
-def test_captured_lmhead_step_replays_on_new_inputs(sga_lib):
-    M, H, vocab = 300, 512, 6000
+@pytest.mark.parametrize("M", [300, 100, 16])   # 2-SM GEMM, CTA-pair and one-CTA decode kernels
+def test_captured_lmhead_step_replays_on_new_inputs(sga_lib, M):
+    H, vocab = 512, 6000
     shards = wl.even_shards(vocab, 2)
     w_np = wl.normal_matrix(3, vocab, H, 1.0 / np.sqrt(H))
     w = gh.to_device(w_np)

@@ -90,7 +90,7 @@ def test_small_shapes(sga_lib, M, H, vocab, num_shards):
         check(np.arange(M), hq, hs, wq, w_scale, shards, org, st, v, i)
 
 
-@pytest.mark.parametrize("M", [200, 40, 12])
+@pytest.mark.parametrize("M", [200, 100, 40, 12])
 def test_no_row_scales_and_nan_code(sga_lib, M):
     H, vocab = 256, 700
     hq, _, wq, w_scale = make(M, H, vocab, 9)

@@ -92,7 +92,7 @@ def test_fused_lmhead_decode_shape_every_shard_in_one_launch(sga_lib):
         gh.assert_stats_equal(one, gh.stats_to_numpy(per))
 
 
-@pytest.mark.parametrize("M", [1, 16, 64, 130, 300])
+@pytest.mark.parametrize("M", [1, 16, 64, 100, 130, 300])
 @pytest.mark.parametrize("case", ["sixty_four_narrow", "padding_after_first", "tiny_widths"])
 def test_one_call_edge_layouts(sga_lib, M, case):
     # the epilogue's per-shard flushes where most CTAs hold tiles of few or no
