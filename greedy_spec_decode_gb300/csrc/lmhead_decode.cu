@@ -70,6 +70,8 @@ constexpr int dec_stage_bytes = dec_a_bytes<kN> + dec_chunks<kN> * kN * ROW_BYTE
 template <int kN>
 constexpr int dec_stages = (227 * 1024 - 4096) / dec_stage_bytes<kN>;  // 3, 3, 3
 
+constexpr int kTileQ = 8;  // entries of the tile queue
+
 template <int kN>
 struct SharedDec {
   uint64_t full[dec_stages<kN>];
@@ -85,11 +87,10 @@ struct SharedDec {
   // the CTA's tiles, in the order the producer took them: entry k % kTileQ
   // holds the k-th (-1 after the last); ready: 1 arrival (the producer),
   // free: 5 (the MMA lane and the four epilogue warps, once read)
-  uint64_t tile_ready[8];
-  uint64_t tile_free[8];
-  int32_t tile_q[8];
+  uint64_t tile_ready[kTileQ];
+  uint64_t tile_free[kTileQ];
+  int32_t tile_q[kTileQ];
 };
-constexpr int kTileQ = 8;
 
 // Cross-CTA merge of a decode launch, in library-owned device memory: each
 // CTA folds its (shard, row) winners into 64-bit keys with atomicMax; the
