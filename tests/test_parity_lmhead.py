@@ -81,8 +81,9 @@ def check_rows(rows, hidden, weight, shards, org_vocab, gpu_stats, gpu_vals, gpu
 @pytest.mark.parametrize("M,H,vocab,num_shards", [
     (1, 64, 300, 1), (100, 128, 1000, 2), (128, 512, 5000, 3), (300, 256, 2311, 4),
     (257, 64, 256, 1), (513, 1024, 4099, 2),
-    # decode-size batches (one to a few dozen rows against a large head)
-    (1, 4096, 20000, 2), (16, 4096, 20000, 2), (64, 1024, 30011, 3),
+    # decode-size batches (one to a few dozen rows against a large head), and
+    # the CTA-pair kernel with a single K block (H = 64: a partial stage)
+    (1, 4096, 20000, 2), (16, 4096, 20000, 2), (64, 1024, 30011, 3), (96, 64, 3000, 2),
 ])
 def test_small_shapes(sga_lib, M, H, vocab, num_shards):
     hidden = wl.normal_matrix(M + H, M, H, 1.0)
