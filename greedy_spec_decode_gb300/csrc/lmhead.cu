@@ -518,10 +518,11 @@ cudaError_t launch_selftest_timeout(unsigned long long limit_ns, uint32_t *err,
 }
 
 // Workspace (partial statistics) of one call:
-//   M <= 64 (decode kernel): one partial per (shard, row, CTA), the CTAs of a
-//     launch at most kDecMaxParts; for one shard at least one per 256-id tile;
-//   65 <= M <= 128 (1-SM kernel, one launch per shard, the workspace reused):
-//     one partial per (row, 256-id tile) of the widest shard;
+//   M <= 128 (decode kernels): not used (the CTAs merge in library-owned
+//     memory); the size keeps the earlier per-CTA partials' count, one
+//     partial per (shard, row, CTA), the CTAs of a launch at most
+//     kDecMaxParts, for one shard at least one per 256-id tile, so that
+//     callers' buffers stay valid;
 //   M >= 129 (2-SM kernel, one launch for every shard): one partial per
 //     (shard, row, chunk), at most min(kMaxChunks, tiles of all shards)
 //     chunks.

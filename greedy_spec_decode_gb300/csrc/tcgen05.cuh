@@ -1,5 +1,5 @@
-// tcgen05.cuh -- pieces shared by the LM-head kernels (lmhead.cu: the 1-SM
-// and 2-SM GEMM kernels, lmhead_decode.cu: the decode-size kernel): tile and
+// tcgen05.cuh -- pieces shared by the LM-head kernels (lmhead.cu: the 2-SM
+// GEMM kernel, lmhead_decode.cu: the decode-size kernels): tile and
 // thread constants, inline PTX for mbarriers, TMA (cp.async.bulk.tensor),
 // tcgen05 fences, shared-memory matrix descriptors, the MMA instruction
 // descriptor and tensor-memory loads, and the host-side tensor-map encoding,
@@ -27,9 +27,9 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 // Swapped-operand decode kernels for M <= this (0: off; at most 128): one CTA
 // per SM up to M = 64, CTA pairs (cta_group::2, the hidden rows split between
 // the two CTAs) for M = 65..128.  Measured: a one-CTA N = 128 variant for M =
-// 65..128 was slower than the 1-SM GEMM kernel (graph replay, 2 shards: M =
-// 128 bf16 210 vs 201 us, fp8 122 vs 114 us): its stages held as many hidden
-// bytes as weight bytes.
+// 65..128 was slower than the one-CTA GEMM kernel then in use (graph replay,
+// 2 shards: M = 128 bf16 210 vs 201 us, fp8 122 vs 114 us): its stages held
+// as many hidden bytes as weight bytes.
 #define SGA_LMHEAD_DECODE_MAX_M 128
 #endif
 static_assert(SGA_LMHEAD_DECODE_MAX_M <= 128, "the decode kernels hold at most 128 hidden rows");
