@@ -151,8 +151,8 @@ def test_decode_calls_on_concurrent_streams(sga_lib):
     # against the oracle on every row).
     H = 512
     cases = []
-    for n in range(3):
-        M = [16, 3, 48][n]
+    for n in range(4):
+        M = [16, 3, 48, 100][n]   # one-CTA kernel (N = 16, 16, 64) and CTA pairs
         vocab = 24000 + 1000 * n
         shards = wl.random_shards(n + 401, vocab, 2 + n)
         org = vocab - 37 * n
